@@ -1,0 +1,336 @@
+"""Seeded synthetic inputs for paged decode attention.
+
+This module only builds inputs: query rows, a paged K/V pool, a block table
+and per-sequence lengths.  It holds none of the attention arithmetic, so the
+CUDA path and the CPU oracle can both read the same tensors without sharing
+any of the method.
+
+Shapes follow the decode-attention API of the ROCm RDNA3.5 decode kernels
+(vllm.v1.attention.ops.rocm_rdna_hip, ``KernelVariant`` fields and
+``expected_kv_cache_strides``) and the decode metadata of the Octave backend
+(vllm.v1.attention.backends.rocm_octave_attn, ``forward``):
+
+* ``q`` / ``out``: ``[S*M, Hq, D]``; tokens of sequence ``s`` are rows
+  ``s*M .. s*M+M-1`` (uniform decode, M query tokens per sequence).
+* K/V pool, layout NHD: ``[NB, P, Hkv, D]``; layout HND: ``[NB, Hkv, P, D]``.
+  ``packed=True`` stores K and V side by side in one row of ``2*D``
+  (the packed-cache stride order of ``expected_kv_cache_strides``), so
+  ``v_cache`` is the view ``k_cache + D`` with the same strides.
+* ``block_table``: int32 ``[S, W]``, logical page -> physical page.
+* ``seq_lens``: int32 ``[S]``, keys of each sequence *including* its M new
+  query tokens.
+
+Every value is drawn in fp32 from a ``torch.Generator`` seeded per stream
+(q, k, v, page permutation, lengths) and rounded once (round to nearest even)
+to fp16 or bf16.  Pool slots that hold no key of any sequence (the tail of a
+partial last page, pages a sliding window never reaches, slack pages) are
+filled with NaN so that any read of them shows up in the output.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import torch
+
+NHD = 0
+HND = 1
+
+_STREAM_Q, _STREAM_K, _STREAM_V, _STREAM_PERM, _STREAM_LEN = range(5)
+
+
+def _gen(seed: int, stream: int, device: str = "cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000003 + stream * 7919 + 17)
+    return g
+
+
+@dataclasses.dataclass
+class DecodeCase:
+    """One decode call's inputs (all tensors on ``device``)."""
+
+    name: str
+    dtype: torch.dtype
+    head_size: int
+    num_q_heads: int
+    num_kv_heads: int
+    page_size: int
+    max_query_len: int
+    window: int
+    scale: float
+    layout: int
+    q: torch.Tensor
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    block_table: torch.Tensor
+    seq_lens: torch.Tensor
+    packed: bool = False
+    # host copy of seq_lens (the inputs are made on the host; kept for sizing)
+    seq_lens_host: Optional[list] = None
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    def to(self, device) -> "DecodeCase":
+        """Copy every tensor to ``device``; a packed pool stays one allocation."""
+        if self.packed:
+            pool = self.k_cache.as_strided(
+                self._pool_shape(), self._pool_strides(), self.k_cache.storage_offset()
+            )
+            pool_d = pool.to(device)
+            k = pool_d[..., : self.head_size]
+            v = pool_d[..., self.head_size :]
+        else:
+            k = self.k_cache.to(device)
+            v = self.v_cache.to(device)
+        return dataclasses.replace(
+            self,
+            q=self.q.to(device),
+            k_cache=k,
+            v_cache=v,
+            block_table=self.block_table.to(device),
+            seq_lens=self.seq_lens.to(device),
+        )
+
+    def _pool_shape(self):
+        s = list(self.k_cache.shape)
+        s[-1] = 2 * self.head_size
+        return tuple(s)
+
+    def _pool_strides(self):
+        return tuple(self.k_cache.stride())
+
+    def kv_bytes_touched(self) -> int:
+        """Bytes of K and V that the M rows of every sequence can see (union
+        over rows): the algorithmic K+V read of one call."""
+        e = self.q.element_size()
+        total = 0
+        lens = self.seq_lens_host or self.seq_lens.tolist()
+        for L in lens:
+            L = max(int(L), 0)
+            u = min(L, self.window + self.max_query_len - 1) if self.window else L
+            total += u * self.num_kv_heads * 2 * self.head_size * e
+        return total
+
+    def pages_touched(self) -> int:
+        lens = self.seq_lens_host or self.seq_lens.tolist()
+        n = 0
+        for L in lens:
+            L = max(int(L), 0)
+            lo = max(0, L - self.max_query_len + 1 - self.window) if self.window else 0
+            if L > lo:
+                n += (L - 1) // self.page_size - lo // self.page_size + 1
+        return n
+
+    def algorithmic_bytes(self) -> int:
+        """K+V read, Q read and O write, block-table entries and seq_lens."""
+        e = self.q.element_size()
+        qo = 2 * self.num_seqs * self.max_query_len * self.num_q_heads * self.head_size * e
+        return self.kv_bytes_touched() + qo + 4 * self.pages_touched() + 4 * self.num_seqs
+
+
+def _rounded_normal(shape, std, mean, dtype, gen, device="cpu"):
+    x = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+    if std != 1.0:
+        x.mul_(std)
+    if mean != 0.0:
+        x.add_(mean)
+    return x.to(dtype)
+
+
+def make_case(
+    name: str,
+    *,
+    seed: int,
+    dtype: torch.dtype,
+    head_size: int,
+    num_q_heads: int,
+    num_kv_heads: int,
+    page_size: int,
+    max_query_len: int,
+    seq_lens: Sequence[int],
+    layout: int = HND,
+    window: int = 0,
+    std: float = 1.0,
+    v_mean: float = 0.0,
+    scale: Optional[float] = None,
+    pool_pages: Optional[int] = None,
+    table_width: Optional[int] = None,
+    window_pages_only: bool = False,
+    packed: bool = False,
+    poison: bool = True,
+    device: str = "cpu",
+) -> DecodeCase:
+    """Build one call's inputs.
+
+    ``pool_pages``: physical pages in the pool (default: exactly the pages
+    used, plus one poison page when ``window_pages_only``).  Logical pages are
+    mapped to a random permutation of the pool.  ``window_pages_only`` keeps
+    only the pages a sliding window reaches in the block table; entries
+    before the window's first page point at a NaN page, as in a block table
+    that holds only the blocks the window reaches.
+    """
+    D, P = head_size, page_size
+    S, M = len(seq_lens), max_query_len
+    lens = [max(int(x), 0) for x in seq_lens]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    pages_needed = [(L + P - 1) // P for L in lens]
+    W = table_width if table_width is not None else max(1, max(pages_needed))
+    assert W >= max(pages_needed)
+    first_page = []
+    for L in lens:
+        if window_pages_only and window and L > 0:
+            lo = max(0, L - M + 1 - window)
+            first_page.append(lo // P)
+        else:
+            first_page.append(0)
+    used = [pn - fp for pn, fp in zip(pages_needed, first_page)]
+    n_used = sum(used)
+    extra_poison = 1 if window_pages_only else 0
+    NB = pool_pages if pool_pages is not None else n_used + extra_poison
+    assert NB >= n_used + extra_poison, (NB, n_used)
+
+    g_perm = _gen(seed, _STREAM_PERM)
+    perm = torch.randperm(NB, generator=g_perm)
+    poison_page = int(perm[-1]) if extra_poison else None
+    block_table = torch.zeros((S, W), dtype=torch.int32)
+    cursor = 0
+    for s in range(S):
+        for j in range(W):
+            if first_page[s] <= j < pages_needed[s]:
+                block_table[s, j] = int(perm[cursor])
+                cursor += 1
+            elif j < first_page[s]:
+                block_table[s, j] = poison_page
+            else:
+                # past the sequence end: a valid page index that is never read
+                block_table[s, j] = int(perm[0]) if n_used else 0
+
+    shape_pool = (NB, P, num_kv_heads, D) if layout == NHD else (NB, num_kv_heads, P, D)
+    if packed:
+        full = list(shape_pool)
+        full[-1] = 2 * D
+        pool = torch.full(full, float("nan") if poison else 0.0, dtype=dtype, device=device)
+        k_cache, v_cache = pool[..., :D], pool[..., D:]
+    else:
+        fill = float("nan") if poison else 0.0
+        k_cache = torch.full(shape_pool, fill, dtype=dtype, device=device)
+        v_cache = torch.full(shape_pool, fill, dtype=dtype, device=device)
+
+    g_q, g_k, g_v = _gen(seed, _STREAM_Q), _gen(seed, _STREAM_K), _gen(seed, _STREAM_V)
+    q = _rounded_normal((S * M, num_q_heads, D), std, 0.0, dtype, g_q)
+    for s in range(S):
+        L = lens[s]
+        lo_pos = first_page[s] * P
+        n = L - lo_pos
+        if n <= 0:
+            continue
+        kvals = _rounded_normal((n, num_kv_heads, D), std, 0.0, dtype, g_k)
+        vvals = _rounded_normal((n, num_kv_heads, D), std, v_mean, dtype, g_v)
+        pos = torch.arange(lo_pos, L)
+        phys = block_table[s, (pos // P)].long()
+        tok = (pos % P).long()
+        if layout == NHD:
+            k_cache[phys, tok] = kvals.to(device)
+            v_cache[phys, tok] = vvals.to(device)
+        else:
+            k_cache.permute(0, 2, 1, 3)[phys, tok] = kvals.to(device)
+            v_cache.permute(0, 2, 1, 3)[phys, tok] = vvals.to(device)
+    if window_pages_only and window and not poison:
+        raise ValueError("window_pages_only needs poison=True")
+    return DecodeCase(
+        name=name,
+        dtype=dtype,
+        head_size=D,
+        num_q_heads=num_q_heads,
+        num_kv_heads=num_kv_heads,
+        page_size=P,
+        max_query_len=M,
+        window=window,
+        scale=float(scale),
+        layout=layout,
+        q=q.to(device),
+        k_cache=k_cache,
+        v_cache=v_cache,
+        block_table=block_table.to(device),
+        seq_lens=torch.tensor(lens, dtype=torch.int32, device=device),
+        packed=packed,
+        seq_lens_host=list(lens),
+    )
+
+
+# ---------------------------------------------------------------------------
+# The five workloads.  Sizes follow the decode configurations the kernel is
+# specified on; the pages' own harness (vLLM's attention_benchmarks, HND,
+# batch 1) is not available, so these seeded shapes stand in for it.
+# ---------------------------------------------------------------------------
+
+def single_seq_nhd(seed: int = 0, device: str = "cpu") -> DecodeCase:
+    """fp16, D=128, 8 q / 2 kv heads, M=1, one sequence of 300 keys (the last
+    of 19 pages holds 12 keys), P=16, NHD, 19 random pages of a 64-page pool."""
+    return make_case(
+        "single_seq_nhd_fp16_d128_L300",
+        seed=seed, dtype=torch.float16, head_size=128, num_q_heads=8,
+        num_kv_heads=2, page_size=16, max_query_len=1, seq_lens=[300],
+        layout=NHD, pool_pages=64, device=device,
+    )
+
+
+def spec_decode_hnd(M: int, L: int, seed: int = 0, device: str = "cpu") -> DecodeCase:
+    """bf16, D=128, 32 q / 8 kv heads, P=16, HND, batch 1, M in 1..4."""
+    return make_case(
+        f"spec_decode_hnd_bf16_d128_M{M}_L{L}",
+        seed=seed, dtype=torch.bfloat16, head_size=128, num_q_heads=32,
+        num_kv_heads=8, page_size=16, max_query_len=M, seq_lens=[L],
+        layout=HND, device=device,
+    )
+
+
+def sliding_window(dtype: torch.dtype, M: int, L: int, seed: int = 0,
+                   device: str = "cpu") -> DecodeCase:
+    """D=256, 8 q / 1 kv head, window 512, P=32; the block table holds only
+    the pages the window reaches (earlier entries point at a NaN page)."""
+    tag = "fp16" if dtype == torch.float16 else "bf16"
+    return make_case(
+        f"sliding_window_{tag}_d256_w512_M{M}_L{L}",
+        seed=seed, dtype=dtype, head_size=256, num_q_heads=8, num_kv_heads=1,
+        page_size=32, max_query_len=M, seq_lens=[L], layout=HND, window=512,
+        window_pages_only=True, device=device,
+    )
+
+
+def wide_head(M: int, L: int, seed: int = 0, device: str = "cpu") -> DecodeCase:
+    """fp16, D=512, 8 q / 1 kv head, full causal, P=16, values N(0, 0.5)."""
+    return make_case(
+        f"wide_head_fp16_d512_M{M}_L{L}",
+        seed=seed, dtype=torch.float16, head_size=512, num_q_heads=8,
+        num_kv_heads=1, page_size=16, max_query_len=M, seq_lens=[L],
+        layout=HND, std=0.5, device=device,
+    )
+
+
+def batched_hybrid_pages(seed: int = 0, num_seqs: int = 64, max_len: int = 16384,
+                         device: str = "cpu") -> DecodeCase:
+    """bf16, D=256, 16 q / 2 kv heads, P=1056, M=4, 64 sequences with lengths
+    uniform in [1, max_len] and one empty (padded) slot; a shared pool with
+    10 % slack pages, randomly permuted."""
+    g = _gen(seed, _STREAM_LEN)
+    lens = torch.randint(1, max_len + 1, (num_seqs,), generator=g).tolist()
+    lens[num_seqs // 3] = 0
+    P = 1056
+    used = sum((L + P - 1) // P for L in lens)
+    return make_case(
+        f"batched_hybrid_bf16_d256_P1056_S{num_seqs}",
+        seed=seed, dtype=torch.bfloat16, head_size=256, num_q_heads=16,
+        num_kv_heads=2, page_size=P, max_query_len=4, seq_lens=lens,
+        layout=HND, pool_pages=used + max(1, used // 10),
+        table_width=(max_len + P - 1) // P, device=device,
+    )
+
+
+SPEC_DECODE_CONTEXTS = (128, 1024, 4096, 16384, 32768)
+SPEC_DECODE_M = (1, 2, 3, 4)
