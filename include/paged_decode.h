@@ -1,0 +1,194 @@
+/*
+ * paged_decode.h — C ABI of the GB300 (sm_103a) paged decode-attention library.
+ *
+ * The operation (vllm.v1.attention.ops.rocm_rdna_hip, the decode entry point
+ * `_Builtin.decode_attn(q, kv_cache, block_table, out, *scratch_and_args)`,
+ * and vllm.v1.attention.backends.rocm_octave_attn, `RocmOctaveAttentionImpl
+ * .forward` / `_decode`):
+ *
+ *   For every sequence s (L_s = seq_lens[s] keys, which include its M new
+ *   query tokens), query token i in [0, M) and query head hq:
+ *     h   = hq / G, G = Hq / Hkv             (contiguous GQA groups)
+ *     n_i = L_s - M + i + 1                  (keys query i sees; the K
+ *                                             length of rocm_octave_attn
+ *                                             `_fill_query_maps`)
+ *     keys k in [lo_i, n_i), lo_i = window ? max(0, n_i - window) : 0
+ *                                            (window in keys, 0 = full
+ *                                             causal: KernelVariant.window)
+ *     K_k = k_cache[block_table[s][k / P]] at token k % P, kv head h
+ *     out[s*M + i][hq] = softmax_k(scale * q . K_k) . V_k, fp32 arithmetic,
+ *                        rounded to the input dtype; 0 if no key is visible.
+ *
+ * Split-KV (KernelVariant.max_segments, scratch_shapes, make_scratch): the
+ * keys of one (sequence, kv head, row group) are cut into segments, one CTA
+ * each; each writes unnormalised partials (acc, m, l) to the caller's
+ * scratch, and the CTA that arrives last at a per-group counter merges them
+ * and resets the counter to 0, so "every launch leaves them zeroed".
+ *
+ * Threading and streams: every call is asynchronous on `stream`, performs
+ * no host synchronisation and allocates nothing (no cudaMalloc, no host
+ * allocation that outlives the call), so a call may be captured in a CUDA
+ * graph.  A scratch buffer may serve one stream at a time: two calls in
+ * flight on different streams with one scratch race on its counters.
+ *
+ * Errors: every function returns PD_OK (0) or a negative pd_status, checked
+ * on the host before any launch.  Nothing falls back to another
+ * implementation.  Faults the host cannot see (a page id outside the pool,
+ * a seq_len beyond the block table, an internal wait that timed out) are
+ * recorded in a device status word (paged_decode_device_status) and the
+ * kernel clamps the access instead of faulting.
+ */
+#ifndef PAGED_DECODE_H
+#define PAGED_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PD_API __attribute__((visibility("default")))
+#else
+#define PD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  q, the caches and out share one of PD_F16 / PD_BF16
+ * (KernelVariant.__post_init__: fp16 or bf16 only); block_table and
+ * seq_lens are PD_I32. */
+typedef enum { PD_F16 = 0, PD_BF16 = 1, PD_I32 = 2 } pd_dtype;
+
+/* Cache layouts (KernelVariant.layout: 0 = NHD, 1 = HND).
+ *   PD_NHD: [num_blocks, page_size, num_kv_heads, head_size]
+ *   PD_HND: [num_blocks, num_kv_heads, page_size, head_size]            */
+typedef enum { PD_NHD = 0, PD_HND = 1 } pd_layout;
+
+/* A strided view of device memory.  Strides are in elements; the innermost
+ * (head_size) stride must be 1.  `data` is a device pointer; the library
+ * never frees it or keeps it past the call. */
+typedef struct pd_tensor {
+  void *data;
+  int32_t dtype; /* pd_dtype */
+  int32_t ndim;
+  int64_t shape[4];
+  int64_t stride[4];
+} pd_tensor;
+
+/* Caller-owned split-KV scratch (make_scratch / scratch_bytes).  Filled by
+ * paged_decode_scratch_init; the library reads the fields, never resizes or
+ * frees `data`. */
+typedef struct pd_scratch {
+  void *data;             /* device memory, 256-byte aligned                  */
+  size_t bytes;           /* its size                                          */
+  int64_t counter_slots;  /* int32 counters at the start of data (set by init) */
+} pd_scratch;
+
+typedef enum {
+  PD_OK = 0,
+  PD_EINVAL = -1,    /* null pointer, size <= 0, Hq % Hkv != 0, shape or
+                        descriptor mismatch, window < 0, page_size % 16 != 0 */
+  PD_EDTYPE = -2,    /* not fp16/bf16, or q/k/v/out dtypes differ            */
+  PD_EHEAD = -3,     /* head_size not in {64, 128, 256, 512}                 */
+  PD_EQLEN = -4,     /* max_query_len < 1 or > 8                             */
+  PD_EALIGN = -5,    /* a row or base not 16-byte aligned, inner stride != 1 */
+  PD_ESCRATCH = -6,  /* scratch missing, not initialised or too small        */
+  PD_ECUDA = -7,     /* a CUDA runtime call failed (launch, attribute, ...)  */
+  PD_ENODEV = -8     /* no CUDA device, or not an sm_103 device              */
+} pd_status;
+
+/* Bits of the device status word. */
+#define PD_DEV_WAIT_TIMEOUT 0x1u  /* an internal barrier wait gave up       */
+#define PD_DEV_BAD_PAGE     0x2u  /* a block-table entry outside the pool   */
+#define PD_DEV_BAD_SEQLEN   0x4u  /* seq_len > block-table width * page_size */
+
+/* Bytes of scratch for calls of up to `max_num_seqs` sequences
+ * (scratch_bytes: 4 * (rows * D + 2 * rows + counters) per sequence).
+ * `max_splits` is the most KV segments (split-KV partials) one
+ * (sequence, kv head) may use; a larger buffer allows more segments.
+ * Returns 0 on invalid arguments. */
+PD_API size_t paged_decode_scratch_bytes(int max_num_seqs, int num_q_heads, int num_kv_heads,
+                                  int head_size, int max_query_len, int max_splits);
+
+/* Prepare a scratch buffer: record its counter area and zero the counters
+ * once, asynchronously on `stream` (make_scratch: "Zeroed once; every launch
+ * leaves them zeroed").  `data` must stay allocated while calls use it.
+ * Call it outside graph capture. */
+PD_API int paged_decode_scratch_init(pd_scratch *scratch, void *data, size_t bytes, int max_num_seqs,
+                              int num_kv_heads, void *stream);
+
+/* The decode call.
+ *   q           [S*M, Hq, D]  fp16/bf16, rows of sequence s at s*M .. s*M+M-1
+ *   k_cache     NHD or HND pool (any strides, innermost 1)
+ *   v_cache     same shape and dtype as k_cache; may alias k_cache + D with
+ *               the packed K|V strides of expected_kv_cache_strides
+ *   block_table [S, W] int32, logical page -> physical page
+ *   seq_lens    [S] int32 device array: keys per sequence, including the M
+ *               new tokens (0 = empty slot: its rows are written as zeros)
+ *   out         [S*M, Hq, D], same dtype as q; may not overlap the inputs
+ *   scale       multiplies q . k before the softmax (usually 1/sqrt(D))
+ *   scratch     from paged_decode_scratch_init; NULL allowed when a call
+ *               needs no split (then every (sequence, kv head) is one CTA)
+ *   stream      cudaStream_t (NULL = the legacy default stream)
+ * The library reads block_table only for pages that hold visible keys, so
+ * entries before a sliding window's first page may be anything. */
+PD_API int paged_decode_attn(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_cache,
+                      const pd_tensor *block_table, const pd_tensor *seq_lens, pd_tensor *out,
+                      int num_q_heads, int num_kv_heads, int head_size, int page_size,
+                      int max_query_len, int window, float scale, int layout,
+                      pd_scratch *scratch, void *stream);
+
+/* Launch knobs (KernelVariant's max_segments / row_groups / waves /
+ * dot_product knobs, chosen per call here).  Zero means "choose". */
+typedef struct pd_options {
+  int segments;      /* KV segments per (sequence, kv head, row group)        */
+  int row_groups;    /* CTAs sharing one kv head's packed query rows          */
+  int key_groups;    /* warp groups of a CTA that take alternate KV tiles     */
+  int stages;        /* shared-memory ring stages (32 KiB each)               */
+  int cluster;       /* thread-block cluster size of the merge (1, 2, 4, 8)   */
+  int path;          /* 0 = auto, 1 = tensor-core (mma.sync), 2 = warp dot     */
+  int max_ctas_hint; /* CTAs the split aims for (0 = the SM count)            */
+} pd_options;
+
+/* paged_decode_attn with explicit knobs (opts may be NULL). */
+PD_API int paged_decode_attn_opts(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_cache,
+                           const pd_tensor *block_table, const pd_tensor *seq_lens, pd_tensor *out,
+                           int num_q_heads, int num_kv_heads, int head_size, int page_size,
+                           int max_query_len, int window, float scale, int layout,
+                           pd_scratch *scratch, void *stream, const pd_options *opts);
+
+/* The launch plan chosen for a call shape, computed on the host only (no
+ * device access), for inspection and tests. */
+typedef struct pd_plan {
+  int path;          /* 1 = mma, 2 = dot                                       */
+  int rows;          /* packed rows per kv head, G * M                         */
+  int row_groups, rows_per_cta, n_tiles, key_groups, stages;
+  int seg_blocks;    /* 16-key blocks per segment                              */
+  int max_segments;  /* segments per (sequence, kv head, row group) in the grid */
+  int cluster;
+  int max_parts;     /* partial slots per group in the scratch                 */
+  int grid_x, grid_y, block_threads;
+  int smem_bytes;
+  int64_t scratch_needed; /* bytes of scratch this call needs (0 = none)       */
+} pd_plan;
+
+PD_API int paged_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+                      int page_size, int max_query_len, int window, int block_table_width,
+                      int num_sms, const pd_scratch *scratch, const pd_options *opts,
+                      pd_plan *plan);
+
+/* Read the device status word (PD_DEV_* bits) of the current device after
+ * synchronising `stream`; reset it to 0 when `reset` is non-zero. */
+PD_API int paged_decode_device_status(unsigned int *status, int reset, void *stream);
+
+/* A static description of a status code. */
+PD_API const char *paged_decode_strerror(int code);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+PD_API int paged_decode_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_DECODE_H */

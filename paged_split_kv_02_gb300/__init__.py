@@ -1,0 +1,261 @@
+"""GB300 (sm_103a) paged split-KV decode attention.
+
+Thin Python binding of ``libpaged_decode.so`` (C ABI in
+``include/paged_decode.h``).  This module only marshals torch tensors into
+the ABI's descriptors: every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if the library is missing the calls
+raise, and ``build()`` compiles it with nvcc.
+
+Names follow the C ABI:
+
+* ``paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, out,
+  num_q_heads, num_kv_heads, head_size, page_size, max_query_len, window,
+  scale, layout, scratch, stream)``
+* ``paged_decode_scratch_bytes(...)`` / ``Scratch`` (``paged_decode_scratch_init``)
+* ``paged_decode_plan(...)``, ``paged_decode_device_status(...)``
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+import torch
+
+from . import _build
+
+NHD = 0
+HND = 1
+PATH_AUTO, PATH_MMA, PATH_DOT = 0, 1, 2
+
+PD_OK = 0
+STATUS_NAMES = {
+    0: "PD_OK", -1: "PD_EINVAL", -2: "PD_EDTYPE", -3: "PD_EHEAD", -4: "PD_EQLEN",
+    -5: "PD_EALIGN", -6: "PD_ESCRATCH", -7: "PD_ECUDA", -8: "PD_ENODEV",
+}
+DEV_WAIT_TIMEOUT, DEV_BAD_PAGE, DEV_BAD_SEQLEN = 0x1, 0x2, 0x4
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "paged_decode.h")
+
+
+class PagedDecodeError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)} ({_strerror(code)})")
+
+
+class PdTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class PdScratch(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("bytes", ctypes.c_size_t),
+                ("counter_slots", ctypes.c_int64)]
+
+
+class PdOptions(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("segments", "row_groups", "key_groups", "stages", "cluster", "path",
+                 "max_ctas_hint")]
+
+
+class PdPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("path", "rows", "row_groups", "rows_per_cta", "n_tiles", "key_groups", "stages",
+                 "seg_blocks", "max_segments", "cluster", "max_parts", "grid_x", "grid_y",
+                 "block_threads", "smem_bytes")] + [("scratch_needed", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libpaged_decode.so in-tree for sm_103a."""
+    global _lib
+    path = _build.build(force=force, verbose=verbose)
+    return path
+
+
+def lib():
+    """The loaded C library; raises if it was never built."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with paged_split_kv_02_gb300.build() "
+                "(there is no fallback implementation)")
+        L = ctypes.CDLL(path)
+        vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                 ctypes.c_size_t)
+        T = ctypes.POINTER(PdTensor)
+        L.paged_decode_scratch_bytes.argtypes = [i32] * 6
+        L.paged_decode_scratch_bytes.restype = sz
+        L.paged_decode_scratch_init.argtypes = [ctypes.POINTER(PdScratch), vp, sz, i32, i32, vp]
+        L.paged_decode_scratch_init.restype = i32
+        attn_args = [T, T, T, T, T, T, i32, i32, i32, i32, i32, i32, f32, i32,
+                     ctypes.POINTER(PdScratch), vp]
+        L.paged_decode_attn.argtypes = attn_args
+        L.paged_decode_attn.restype = i32
+        L.paged_decode_attn_opts.argtypes = attn_args + [ctypes.POINTER(PdOptions)]
+        L.paged_decode_attn_opts.restype = i32
+        L.paged_decode_plan.argtypes = [i32] * 9 + [ctypes.POINTER(PdScratch),
+                                                    ctypes.POINTER(PdOptions),
+                                                    ctypes.POINTER(PdPlan)]
+        L.paged_decode_plan.restype = i32
+        L.paged_decode_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32, vp]
+        L.paged_decode_device_status.restype = i32
+        L.paged_decode_strerror.argtypes = [i32]
+        L.paged_decode_strerror.restype = ctypes.c_char_p
+        L.paged_decode_version.argtypes = []
+        L.paged_decode_version.restype = i32
+        _lib = L
+    return _lib
+
+
+def declared_symbols() -> list:
+    """Function names the public header declares."""
+    text = open(HEADER).read()
+    return re.findall(r"PD_API\s+[\w\s\*]*?\b(paged_decode_\w+)\s*\(", text)
+
+
+def _strerror(code: int) -> str:
+    try:
+        return lib().paged_decode_strerror(int(code)).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+_DTYPES = {torch.float16: 0, torch.bfloat16: 1, torch.int32: 2}
+
+
+def tensor_desc(t: torch.Tensor) -> PdTensor:
+    """Descriptor of a tensor: pointer, dtype code, shape and element strides."""
+    d = PdTensor()
+    d.data = t.data_ptr()
+    d.dtype = _DTYPES.get(t.dtype, 99)  # 99: a type the library does not take
+    d.ndim = t.dim()
+    for i in range(min(t.dim(), 4)):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def options(**kw) -> PdOptions:
+    o = PdOptions()
+    for k, v in kw.items():
+        setattr(o, k, int(v))
+    return o
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def paged_decode_scratch_bytes(max_num_seqs, num_q_heads, num_kv_heads, head_size,
+                               max_query_len, max_splits=256) -> int:
+    return int(lib().paged_decode_scratch_bytes(max_num_seqs, num_q_heads, num_kv_heads,
+                                                head_size, max_query_len, max_splits))
+
+
+class Scratch:
+    """Caller-owned split-KV scratch in device memory (torch allocation)
+    prepared by ``paged_decode_scratch_init``; create it outside graph
+    capture and reuse it for every call of one stream."""
+
+    def __init__(self, max_num_seqs, num_q_heads, num_kv_heads, head_size, max_query_len,
+                 max_splits=256, device=None, stream=None, nbytes=None):
+        if nbytes is None:
+            nbytes = paged_decode_scratch_bytes(max_num_seqs, num_q_heads, num_kv_heads,
+                                                head_size, max_query_len, max_splits)
+            if nbytes == 0:
+                raise PagedDecodeError(-1, "paged_decode_scratch_bytes")
+        self.buffer = torch.empty(int(nbytes) + 256, dtype=torch.uint8, device=device or "cuda")
+        off = (-self.buffer.data_ptr()) % 256
+        self.view = self.buffer[off: off + int(nbytes)]
+        self.desc = PdScratch()
+        rc = lib().paged_decode_scratch_init(ctypes.byref(self.desc), self.view.data_ptr(),
+                                             int(nbytes), int(max_num_seqs), int(num_kv_heads),
+                                             _stream_handle(stream))
+        if rc != PD_OK:
+            raise PagedDecodeError(rc, "paged_decode_scratch_init")
+
+    def counters(self) -> torch.Tensor:
+        """The int32 counter area (every call leaves it zero)."""
+        n = int(self.desc.counter_slots)
+        return self.view[: 4 * n].view(torch.int32)
+
+
+def paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, out, num_q_heads,
+                      num_kv_heads, head_size, page_size, max_query_len, window, scale, layout,
+                      scratch: Optional[Scratch] = None, stream=None,
+                      opts: Optional[PdOptions] = None, check: bool = True) -> int:
+    """Launch the decode kernel; raises PagedDecodeError on a non-zero status
+    (returns the status when ``check`` is False)."""
+    L = lib()
+    descs = [tensor_desc(t) for t in (q, k_cache, v_cache, block_table, seq_lens, out)]
+    sp = ctypes.byref(scratch.desc) if scratch is not None else None
+    args = [ctypes.byref(d) for d in descs] + [
+        int(num_q_heads), int(num_kv_heads), int(head_size), int(page_size), int(max_query_len),
+        int(window), float(scale), int(layout), sp, _stream_handle(stream)]
+    if opts is None:
+        rc = L.paged_decode_attn(*args)
+    else:
+        rc = L.paged_decode_attn_opts(*args, ctypes.byref(opts))
+    if check and rc != PD_OK:
+        raise PagedDecodeError(rc, "paged_decode_attn")
+    return rc
+
+
+def paged_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_size, page_size, max_query_len,
+                      window, block_table_width, num_sms, scratch: Optional[Scratch] = None,
+                      opts: Optional[PdOptions] = None, scratch_desc: Optional[PdScratch] = None
+                      ) -> dict:
+    plan = PdPlan()
+    sd = scratch.desc if scratch is not None else scratch_desc
+    rc = lib().paged_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_size, page_size,
+                                 max_query_len, window, block_table_width, num_sms,
+                                 ctypes.byref(sd) if sd is not None else None,
+                                 ctypes.byref(opts) if opts is not None else None,
+                                 ctypes.byref(plan))
+    if rc != PD_OK:
+        raise PagedDecodeError(rc, "paged_decode_plan")
+    return plan.as_dict()
+
+
+def paged_decode_device_status(reset: bool = False, stream=None) -> int:
+    v = ctypes.c_uint(0)
+    rc = lib().paged_decode_device_status(ctypes.byref(v), int(bool(reset)), _stream_handle(stream))
+    if rc != PD_OK:
+        raise PagedDecodeError(rc, "paged_decode_device_status")
+    return int(v.value)
+
+
+def paged_decode_version() -> int:
+    return int(lib().paged_decode_version())
+
+
+def decode_case(case, out=None, scratch=None, stream=None, opts=None):
+    """Run the kernel on a ``workloads.DecodeCase`` (tensors on the GPU)."""
+    if out is None:
+        out = torch.empty_like(case.q)
+    paged_decode_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, out,
+                      case.num_q_heads, case.num_kv_heads, case.head_size, case.page_size,
+                      case.max_query_len, case.window, case.scale, case.layout, scratch,
+                      stream, opts)
+    return out

@@ -1,0 +1,536 @@
+// C ABI of the paged decode-attention library: argument checks, the launch
+// plan (segments, clusters, warp groups, ring stages), TMA tensor maps of
+// the paged caches, scratch handling and the device status word.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/paged_decode.h"
+#include "pd_internal.h"
+
+namespace pd {
+
+__device__ unsigned int g_status;  // PD_DEV_* bits; read by paged_decode_device_status
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block on sm_100-class parts
+constexpr int kMaxDevices = 64;
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------
+// Device facts (cached per device).
+struct DeviceInfo {
+  int ok = 0;        // 1 = sm_103 device
+  int num_sms = 0;
+  unsigned int *status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return PD_ENODEV;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return PD_ENODEV;
+    }
+    if (major != 10 || minor != 3) return PD_ENODEV;  // built for sm_103a only
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) {
+      cudaGetLastError();
+      return PD_ECUDA;
+    }
+    d.num_sms = sms;
+    d.status = static_cast<unsigned int *>(ptr);
+    d.ok = 1;
+  }
+  *out = d;
+  return PD_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TMA tensor maps of the caches, cached by (address, shape, strides).
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+struct MapKey {
+  const void *ptr;
+  int layout;
+  int64_t dims[4];
+  int64_t strides[3];
+  bool operator==(const MapKey &o) const {
+    return ptr == o.ptr && layout == o.layout && std::memcmp(dims, o.dims, sizeof dims) == 0 &&
+           std::memcmp(strides, o.strides, sizeof strides) == 0;
+  }
+};
+struct MapEntry {
+  int dev = -1;
+  MapKey key{};
+  CUtensorMap map;
+};
+constexpr int kMapCache = 64;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+std::mutex g_map_mu;
+
+// Box: 64 head-dim elements (128 bytes, one swizzle row) x 16 tokens of one
+// kv head of one page.
+int encode_cache_map(const pd_tensor *t, int layout, CUtensorMap *out) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  if (!g_encode) return PD_ECUDA;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  // logical dims (innermost first): d, then the two middle dims, then block
+  MapKey key{};
+  key.ptr = t->data;
+  key.layout = layout;
+  // tensor shape: NHD [NB, P, Hkv, D]; HND [NB, Hkv, P, D]
+  key.dims[0] = t->shape[3];
+  key.dims[1] = t->shape[2];
+  key.dims[2] = t->shape[1];
+  key.dims[3] = t->shape[0];
+  key.strides[0] = t->stride[2];
+  key.strides[1] = t->stride[1];
+  key.strides[2] = t->stride[0];
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  for (auto &e : g_maps)
+    if (e.dev == dev && e.key == key) {
+      *out = e.map;
+      return PD_OK;
+    }
+  cuuint64_t dims[4];
+  cuuint64_t strides[3];
+  for (int i = 0; i < 4; ++i) dims[i] = (cuuint64_t)key.dims[i];
+  for (int i = 0; i < 3; ++i) strides[i] = (cuuint64_t)key.strides[i] * 2;  // bytes
+  cuuint32_t box[4] = {64, 1, 1, 1};
+  // the token dim is dims[1] for HND ([.., P, D]) and dims[2] for NHD
+  if (layout == PD_HND)
+    box[1] = kBlockKeys;
+  else
+    box[2] = kBlockKeys;
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUtensorMap m;
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, t->data, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return PD_EALIGN;
+  MapEntry &e = g_maps[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCache;
+  e.dev = dev;
+  e.key = key;
+  e.map = m;
+  *out = m;
+  return PD_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Argument checks.
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_rows_tensor(const pd_tensor *t, int64_t rows, int Hq, int D) {
+  if (!t || !t->data || t->ndim != 3) return PD_EINVAL;
+  if (t->shape[0] != rows || t->shape[1] != Hq || t->shape[2] != D) return PD_EINVAL;
+  if (t->dtype != PD_F16 && t->dtype != PD_BF16) return PD_EDTYPE;
+  if (t->stride[2] != 1) return PD_EALIGN;
+  if (t->stride[0] % 8 != 0 || t->stride[1] % 8 != 0 || !aligned16(t->data)) return PD_EALIGN;
+  if (t->stride[0] < 0 || t->stride[1] < 0) return PD_EINVAL;
+  return PD_OK;
+}
+
+int check_cache(const pd_tensor *t, int layout, int Hkv, int P, int D) {
+  if (!t || !t->data || t->ndim != 4) return PD_EINVAL;
+  const int64_t hdim = layout == PD_NHD ? t->shape[2] : t->shape[1];
+  const int64_t pdim = layout == PD_NHD ? t->shape[1] : t->shape[2];
+  if (t->shape[0] < 1 || hdim != Hkv || pdim != P || t->shape[3] != D) return PD_EINVAL;
+  if (t->dtype != PD_F16 && t->dtype != PD_BF16) return PD_EDTYPE;
+  if (t->stride[3] != 1) return PD_EALIGN;
+  for (int i = 0; i < 3; ++i) {
+    if (t->stride[i] <= 0) return PD_EINVAL;
+    if (t->stride[i] % 8 != 0) return PD_EALIGN;  // TMA: strides are multiples of 16 bytes
+  }
+  if (!aligned16(t->data)) return PD_EALIGN;
+  if (t->shape[0] > INT32_MAX) return PD_EINVAL;
+  return PD_OK;
+}
+
+// ---------------------------------------------------------------------------
+// The launch plan.
+struct PlanOut {
+  pd_plan pub;
+  int nt, kg, ns;
+};
+
+int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_width, int num_sms,
+              const pd_scratch *scratch, const pd_options *opts, pd_plan *plan) {
+  pd_options o{};
+  if (opts) o = *opts;
+  if (S < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || P <= 0 || P % kBlockKeys != 0 ||
+      window < 0 || bt_width < 1 || num_sms <= 0)
+    return PD_EINVAL;
+  if (D != 64 && D != 128 && D != 256 && D != 512) return PD_EHEAD;
+  if (M < 1 || M > 8) return PD_EQLEN;
+  if (o.path == 2) return PD_EINVAL;  // the warp-dot path is not part of this build
+  const int G = Hq / Hkv, R = G * M;
+  int rg = o.row_groups > 0 ? o.row_groups : (int)std::max<int64_t>(1, cdiv(R, 64));
+  if (rg > kMaxRowGroups || rg > R) return PD_EINVAL;
+  const int rows_cta = (int)cdiv(R, rg);
+  const int NT = (int)cdiv(rows_cta, 8);
+  if (NT > kMaxConsumerWarps) return PD_EINVAL;
+  const int TB = kStageBytes / 2 / (kBlockKeys * D * 2);
+  const int fixed = smem_bytes(D, NT, 0);
+  const int ns_max = std::min(8, (kSmemLimit - fixed - 16 * 8) / kStageBytes);
+  int KG = o.key_groups > 0 ? o.key_groups : std::max(1, std::min(4, kMaxConsumerWarps / NT));
+  int NS = 0;
+  while (true) {
+    NS = o.stages > 0 ? o.stages : (ns_max / KG) * KG;
+    // the warp groups' partials (KG copies of NT*8 x D fp32) must fit in the
+    // dead ring at the end; fewer groups when they do not
+    if (o.key_groups > 0 || KG == 1 || NS < 1 ||
+        epilogue_floats(D, NT, KG, 1, 1) * 4 <= epilogue_bytes(D, NT, NS))
+      break;
+    KG /= 2;
+  }
+  if (NT * KG > kMaxConsumerWarps) return PD_EINVAL;
+  if (NS < 1 || NS > ns_max || NS % KG != 0 || (NS < 2 && o.stages == 0)) return PD_EINVAL;
+
+  // KV blocks (16 keys) a (sequence, kv head, row group) can span at most.
+  int64_t nb_max = cdiv((int64_t)bt_width * P, kBlockKeys);
+  if (window > 0) nb_max = std::min<int64_t>(nb_max, cdiv(window + M - 1, kBlockKeys) + 1);
+  const int64_t units = (int64_t)S * Hkv * rg;
+  const int64_t target = o.max_ctas_hint > 0 ? o.max_ctas_hint : num_sms;
+  // a segment reads at least one stage per warp group, and at least four
+  // keys per packed row so its partial stays small next to the keys it read
+  const int64_t min_seg_blocks = std::max<int64_t>({4, (int64_t)TB * KG, 2LL * NT});
+  int64_t nseg;
+  if (o.segments > 0) {
+    nseg = o.segments;
+  } else if (S <= 1) {
+    nseg = std::max<int64_t>(1, target / std::max<int64_t>(units, 1));
+    nseg = std::min(nseg, std::max<int64_t>(1, nb_max / min_seg_blocks));
+  } else {
+    // a batch: lengths are only known on the device; aim at ~4 waves of
+    // equal segments assuming an average length of half the table width
+    const int64_t est = std::max<int64_t>(1, units * nb_max / 2);
+    int64_t sb = std::max(min_seg_blocks, cdiv(est, 4 * target));
+    nseg = cdiv(nb_max, sb);
+  }
+  nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, nb_max));
+  const int64_t part_floats = 8LL * NT * D;  // one partial's acc
+  int CS = o.cluster > 0 ? o.cluster : 1;
+  // clusters only in the one-wave regime: a batch runs several waves, where
+  // the last-arriving CTA's merge overlaps other CTAs' work
+  if (o.cluster == 0 && S <= 1 && nseg >= 8 && nseg * part_floats * 4 > (256 << 10)) CS = 8;
+  if (CS != 1 && CS != 2 && CS != 4 && CS != 8) return PD_EINVAL;
+  if (CS > 1) {
+    if (o.segments > 0) {
+      if (nseg % CS) return PD_EINVAL;
+    } else {
+      nseg = std::max<int64_t>(CS, (nseg / CS) * CS);
+    }
+  }
+  int64_t max_parts = nseg > CS ? nseg / CS : 0;  // partial slots per group (0: none)
+
+  // Scratch: counters for every group, partials for every cluster.
+  const int64_t counter_need = units;
+  auto partial_bytes = [&](int64_t parts) -> int64_t {
+    const int64_t acc = ((units * parts * part_floats * 4) + 255) / 256 * 256;
+    const int64_t ml = ((units * parts * 8LL * NT * 2 * 4) + 255) / 256 * 256;
+    return acc + ml;
+  };
+  int64_t avail = -1;
+  if (scratch && scratch->data) {
+    const int64_t cbytes = (scratch->counter_slots * 4 + 255) / 256 * 256;
+    avail = (int64_t)scratch->bytes - cbytes;
+    if (scratch->counter_slots < counter_need) avail = -1;
+  }
+  if (max_parts > 0) {
+    if (avail < 0 || partial_bytes(max_parts) > avail) {
+      if (o.segments > 0) return PD_ESCRATCH;
+      // shrink the split to what the scratch holds (one cluster needs none)
+      int64_t fit = 0;
+      if (avail > 0) {
+        int64_t lo = 0, hi = max_parts;
+        while (lo < hi) {
+          const int64_t mid = (lo + hi + 1) / 2;
+          if (partial_bytes(mid) <= avail) lo = mid; else hi = mid - 1;
+        }
+        fit = lo;
+      }
+      if (fit >= 2) {
+        max_parts = fit;
+        nseg = max_parts * CS;
+      } else {
+        if (CS == 1) {
+          nseg = 1;
+        } else {
+          nseg = CS;
+        }
+        max_parts = 0;
+      }
+    }
+  }
+  // The epilogue must fit in the ring + Q region.
+  while (max_parts > 0 &&
+         epilogue_floats(D, NT, KG, CS, (int)max_parts) * 4 > epilogue_bytes(D, NT, NS)) {
+    if (o.segments > 0) return PD_EINVAL;
+    max_parts = max_parts - 1;
+    nseg = max_parts > 1 ? max_parts * CS : CS;
+    if (max_parts <= 1) max_parts = 0;
+  }
+  if (epilogue_floats(D, NT, KG, CS, 1) * 4 > epilogue_bytes(D, NT, NS)) return PD_EINVAL;
+  const int64_t seg_blocks = cdiv(nb_max, nseg);
+  if ((int64_t)Hkv * rg * nseg > INT32_MAX || S > 65535) return PD_EINVAL;
+
+  plan->path = 1;
+  plan->rows = R;
+  plan->row_groups = rg;
+  plan->rows_per_cta = rows_cta;
+  plan->n_tiles = NT;
+  plan->key_groups = KG;
+  plan->stages = NS;
+  plan->seg_blocks = (int)seg_blocks;
+  plan->max_segments = (int)nseg;
+  plan->cluster = CS;
+  plan->max_parts = (int)max_parts;
+  plan->grid_x = (int)(Hkv * rg * nseg);
+  plan->grid_y = S;
+  plan->block_threads = 32 * (NT * KG + 1);
+  plan->smem_bytes = smem_bytes(D, NT, NS);
+  plan->scratch_needed = max_parts > 0 ? partial_bytes(max_parts) : 0;
+  return PD_OK;
+}
+
+int element_dtype_ok(const pd_tensor *t, int want) { return t->dtype == want; }
+
+int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_cache,
+              const pd_tensor *block_table, const pd_tensor *seq_lens, pd_tensor *out,
+              int num_q_heads, int num_kv_heads, int head_size, int page_size, int max_query_len,
+              int window, float scale, int layout, pd_scratch *scratch, void *stream,
+              const pd_options *opts) {
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PD_EINVAL;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return PD_EINVAL;
+  if (head_size != 64 && head_size != 128 && head_size != 256 && head_size != 512) return PD_EHEAD;
+  if (max_query_len < 1 || max_query_len > 8) return PD_EQLEN;
+  if (page_size <= 0 || page_size % kBlockKeys != 0) return PD_EINVAL;
+  if (window < 0 || !std::isfinite(scale)) return PD_EINVAL;
+  if (layout != PD_NHD && layout != PD_HND) return PD_EINVAL;
+  if (seq_lens->ndim != 1 || !seq_lens->data || seq_lens->stride[0] != 1) return PD_EINVAL;
+  if (!element_dtype_ok(seq_lens, PD_I32) || !element_dtype_ok(block_table, PD_I32)) return PD_EDTYPE;
+  const int64_t S = seq_lens->shape[0];
+  if (S < 0) return PD_EINVAL;
+  if (block_table->ndim != 2 || !block_table->data || block_table->shape[0] != S ||
+      block_table->shape[1] < 1 || block_table->stride[1] != 1 || block_table->stride[0] < 0)
+    return PD_EINVAL;
+  int rc;
+  if ((rc = check_rows_tensor(q, S * max_query_len, num_q_heads, head_size)) != PD_OK) return rc;
+  if ((rc = check_rows_tensor(out, S * max_query_len, num_q_heads, head_size)) != PD_OK) return rc;
+  if ((rc = check_cache(k_cache, layout, num_kv_heads, page_size, head_size)) != PD_OK) return rc;
+  if ((rc = check_cache(v_cache, layout, num_kv_heads, page_size, head_size)) != PD_OK) return rc;
+  if (q->dtype != out->dtype || q->dtype != k_cache->dtype || q->dtype != v_cache->dtype)
+    return PD_EDTYPE;
+  for (int i = 0; i < 4; ++i)
+    if (k_cache->shape[i] != v_cache->shape[i]) return PD_EINVAL;
+  if (block_table->shape[1] > INT32_MAX || block_table->shape[1] * (int64_t)page_size > INT32_MAX)
+    return PD_EINVAL;
+  if (S == 0) return PD_OK;
+
+  DeviceInfo dev;
+  if ((rc = device_info(&dev)) != PD_OK) return rc;
+  pd_plan plan;
+  rc = make_plan((int)S, num_q_heads, num_kv_heads, head_size, page_size, max_query_len, window,
+                 (int)block_table->shape[1], dev.num_sms, scratch, opts, &plan);
+  if (rc != PD_OK) return rc;
+
+  CUtensorMap tk, tv;
+  if ((rc = encode_cache_map(k_cache, layout, &tk)) != PD_OK) return rc;
+  if ((rc = encode_cache_map(v_cache, layout, &tv)) != PD_OK) return rc;
+
+  Params p{};
+  p.q = q->data;
+  p.q_s0 = q->stride[0];
+  p.q_s1 = q->stride[1];
+  p.out = out->data;
+  p.o_s0 = out->stride[0];
+  p.o_s1 = out->stride[1];
+  p.block_table = static_cast<const int32_t *>(block_table->data);
+  p.bt_stride = block_table->stride[0];
+  p.bt_width = (int)block_table->shape[1];
+  p.seq_lens = static_cast<const int32_t *>(seq_lens->data);
+  p.num_pool_blocks = (int)k_cache->shape[0];
+  p.Hq = num_q_heads;
+  p.Hkv = num_kv_heads;
+  p.G = num_q_heads / num_kv_heads;
+  p.M = max_query_len;
+  p.P = page_size;
+  p.window = window;
+  p.layout = layout;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.R = plan.rows;
+  p.rg = plan.row_groups;
+  p.rows_cta = plan.rows_per_cta;
+  p.NT = plan.n_tiles;
+  p.KG = plan.key_groups;
+  p.NS = plan.stages;
+  p.seg_blocks = plan.seg_blocks;
+  p.max_seg = plan.max_segments;
+  p.CS = plan.cluster;
+  p.max_parts = std::max(plan.max_parts, 1);
+  p.status = dev.status;
+  if (plan.max_parts > 0) {
+    char *base = static_cast<char *>(scratch->data);
+    const int64_t cbytes = (scratch->counter_slots * 4 + 255) / 256 * 256;
+    const int64_t units = S * num_kv_heads * plan.row_groups;
+    const int64_t acc_bytes =
+        (units * plan.max_parts * 8LL * plan.n_tiles * head_size * 4 + 255) / 256 * 256;
+    p.counters = reinterpret_cast<int *>(base);
+    p.part_acc = reinterpret_cast<float *>(base + cbytes);
+    p.part_ml = reinterpret_cast<float *>(base + cbytes + acc_bytes);
+  }
+
+  Launch l;
+  l.grid = dim3(plan.grid_x, plan.grid_y, 1);
+  l.block = dim3(plan.block_threads, 1, 1);
+  l.smem = plan.smem_bytes;
+  l.cluster = plan.cluster;
+  cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, tk, tv, p, l,
+                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PD_ECUDA;
+  }
+  return PD_OK;
+}
+
+}  // namespace
+}  // namespace pd
+
+using namespace pd;
+
+extern "C" {
+
+size_t paged_decode_scratch_bytes(int max_num_seqs, int num_q_heads, int num_kv_heads,
+                                  int head_size, int max_query_len, int max_splits) {
+  if (max_num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads != 0 || max_query_len < 1 || max_query_len > 8 ||
+      max_splits < 0)
+    return 0;
+  if (head_size != 64 && head_size != 128 && head_size != 256 && head_size != 512) return 0;
+  const int64_t R = (int64_t)(num_q_heads / num_kv_heads) * max_query_len;
+  const int64_t rg = std::max<int64_t>(1, cdiv(R, 64));
+  const int64_t nt8 = rg * 8 * cdiv(cdiv(R, rg), 8);  // padded rows over all row groups
+  const int64_t counters = ((int64_t)max_num_seqs * num_kv_heads * kMaxRowGroups * 4 + 255) / 256 * 256;
+  const int64_t parts = (int64_t)max_num_seqs * num_kv_heads * max_splits;
+  const int64_t acc = (parts * nt8 * head_size * 4 + 255) / 256 * 256;
+  const int64_t ml = (parts * nt8 * 2 * 4 + 255) / 256 * 256;
+  return (size_t)(counters + acc + ml + 256);
+}
+
+int paged_decode_scratch_init(pd_scratch *scratch, void *data, size_t bytes, int max_num_seqs,
+                              int num_kv_heads, void *stream) {
+  if (!scratch || !data || max_num_seqs < 0 || num_kv_heads <= 0) return PD_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(data) & 255u) != 0) return PD_EALIGN;
+  const int64_t slots = (int64_t)max_num_seqs * num_kv_heads * kMaxRowGroups;
+  const int64_t cbytes = (slots * 4 + 255) / 256 * 256;
+  if ((int64_t)bytes < cbytes) return PD_ESCRATCH;
+  scratch->data = data;
+  scratch->bytes = bytes;
+  scratch->counter_slots = slots;
+  if (cbytes > 0 &&
+      cudaMemsetAsync(data, 0, (size_t)cbytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return PD_ECUDA;
+  }
+  return PD_OK;
+}
+
+int paged_decode_attn(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_cache,
+                      const pd_tensor *block_table, const pd_tensor *seq_lens, pd_tensor *out,
+                      int num_q_heads, int num_kv_heads, int head_size, int page_size,
+                      int max_query_len, int window, float scale, int layout,
+                      pd_scratch *scratch, void *stream) {
+  return attn_impl(q, k_cache, v_cache, block_table, seq_lens, out, num_q_heads, num_kv_heads,
+                   head_size, page_size, max_query_len, window, scale, layout, scratch, stream,
+                   nullptr);
+}
+
+int paged_decode_attn_opts(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_cache,
+                           const pd_tensor *block_table, const pd_tensor *seq_lens, pd_tensor *out,
+                           int num_q_heads, int num_kv_heads, int head_size, int page_size,
+                           int max_query_len, int window, float scale, int layout,
+                           pd_scratch *scratch, void *stream, const pd_options *opts) {
+  return attn_impl(q, k_cache, v_cache, block_table, seq_lens, out, num_q_heads, num_kv_heads,
+                   head_size, page_size, max_query_len, window, scale, layout, scratch, stream,
+                   opts);
+}
+
+int paged_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+                      int page_size, int max_query_len, int window, int block_table_width,
+                      int num_sms, const pd_scratch *scratch, const pd_options *opts,
+                      pd_plan *plan) {
+  if (!plan) return PD_EINVAL;
+  return make_plan(num_seqs, num_q_heads, num_kv_heads, head_size, page_size, max_query_len,
+                   window, block_table_width, num_sms, scratch, opts, plan);
+}
+
+int paged_decode_device_status(unsigned int *status, int reset, void *stream) {
+  if (!status) return PD_EINVAL;
+  DeviceInfo dev;
+  int rc = device_info(&dev);
+  if (rc != PD_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  if (cudaMemcpyAsync(&v, dev.status, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return PD_ECUDA;
+  }
+  if (reset && cudaMemsetAsync(dev.status, 0, sizeof v, st) != cudaSuccess) {
+    cudaGetLastError();
+    return PD_ECUDA;
+  }
+  *status = v;
+  return PD_OK;
+}
+
+const char *paged_decode_strerror(int code) {
+  switch (code) {
+    case PD_OK: return "ok";
+    case PD_EINVAL: return "invalid argument (null pointer, size, shape, layout or option)";
+    case PD_EDTYPE: return "unsupported or mismatched dtype (q, caches and out must share fp16 or bf16; block_table and seq_lens int32)";
+    case PD_EHEAD: return "head_size must be 64, 128, 256 or 512";
+    case PD_EQLEN: return "max_query_len must be in 1..8";
+    case PD_EALIGN: return "misaligned tensor (16-byte rows and bases, innermost stride 1)";
+    case PD_ESCRATCH: return "scratch missing, not initialised or too small";
+    case PD_ECUDA: return "CUDA runtime error";
+    case PD_ENODEV: return "no sm_103 CUDA device";
+    default: return "unknown status";
+  }
+}
+
+int paged_decode_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Internal host/device contract between the C ABI (pd_api.cu) and the
+// decode kernels (pd_kernel.cuh, instantiated per head size).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace pd {
+
+constexpr int kBlockKeys = 16;        // keys per TMA box and per mma m-tile
+constexpr int kStageBytes = 32768;    // K + V bytes of one shared-memory ring stage
+constexpr int kMaxRowGroups = 8;      // counters reserved per (sequence, kv head)
+constexpr int kMaxConsumerWarps = 8;  // warps that compute; one more loads
+constexpr int kMaxThreads = 32 * (kMaxConsumerWarps + 1);
+constexpr int kSmemAlign = 1024;      // the 128-byte TMA swizzle repeats every 1 KiB
+
+// Everything a launch needs besides the two tensor maps.
+struct Params {
+  const void *q;
+  int64_t q_s0, q_s1;  // element strides of q[t][hq][:]
+  void *out;
+  int64_t o_s0, o_s1;
+  const int32_t *block_table;
+  int64_t bt_stride;
+  int bt_width;
+  const int32_t *seq_lens;
+  int num_pool_blocks;  // pages in the pool, for the page-id bounds check
+  int Hq, Hkv, G, M, P, window, layout;
+  float scale_log2;  // scale * log2(e): softmax runs on exp2
+  int R;             // packed rows per kv head, G * M
+  int rg;            // row groups (CTAs per kv head and segment)
+  int rows_cta;      // packed rows per CTA, ceil(R / rg)
+  int NT;            // 8-row mma n-tiles per CTA
+  int KG;            // consumer warp groups; group g takes tiles g, g + KG, ...
+  int NS;            // ring stages
+  int seg_blocks;    // 16-key blocks per segment (lower bound)
+  int max_seg;       // segments per (sequence, kv head, row group) in the grid
+  int CS;            // cluster size of the merge
+  int max_parts;     // partial slots per group, max_seg / CS
+  float *part_acc;   // [S][Hkv][rg][max_parts][NT*8][D]
+  float *part_ml;    // [S][Hkv][rg][max_parts][NT*8][2]
+  int *counters;     // [S][Hkv][rg]
+  unsigned int *status;
+};
+
+struct Launch {
+  dim3 grid;
+  dim3 block;
+  int smem;
+  int cluster;
+};
+
+// Dynamic shared memory of a launch: ring + Q tile + barriers + flags.
+inline int smem_bytes(int D, int NT, int NS) {
+  return kSmemAlign + NS * kStageBytes + NT * D * 16 + 2 * NS * 8 + 64;
+}
+
+// Bytes of the epilogue region (the ring and the Q tile once they are dead).
+inline int64_t epilogue_bytes(int D, int NT, int NS) {
+  return (int64_t)NS * kStageBytes + (int64_t)NT * D * 16;
+}
+
+// Floats the epilogue needs: combine phase and final-merge phase.
+inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
+  const int64_t nt8 = 8LL * NT;
+  const int64_t combine = KG * nt8 * D + 2LL * KG * nt8 + 2 * nt8 + nt8 * (D / CS) + 2 * nt8 +
+                          (int64_t)CS * nt8 + 16;
+  const int64_t final_merge = 2LL * ncl_max * nt8 + nt8 + 16;
+  return combine > final_merge ? combine : final_merge;
+}
+
+cudaError_t launch_mma(int D, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const Params &p, const Launch &l, cudaStream_t stream);
+
+unsigned int *device_status_ptr();
+
+}  // namespace pd

@@ -1,0 +1,664 @@
+// Paged split-KV decode attention on sm_103a, tensor-core path.
+//
+// One CTA per (kv head, row group, KV segment), one sequence per grid.y
+// (the work unit of the gfx1151 decode kernel: "one workgroup per (kv head,
+// row group, KV segment), packing every query row of a kv head so its KV is
+// read once"; batched decode takes "one sequence per grid.y").
+//
+// Warp roles
+//   * one producer warp: per 32 KiB ring stage, TMA-loads the K and V
+//     16-key x 64-dim boxes of the stage's keys, one box per lane, straight
+//     from the physical page the block table names (the page gather);
+//   * NT * KG consumer warps: warp (t, g) owns the 8 packed query rows of
+//     n-tile t and consumes the stages g, g + KG, g + 2 KG, ...
+//
+// Per stage, a consumer warp computes for each 16-key block
+//   S^T[16 keys x 8 rows] = K[16 x D] . Q^T[D x 8]        (mma m16n8k16)
+// so keys sit on the MMA's M side and the packed rows on its 8-wide N side:
+// few rows (G * M = 4 .. 64) waste at most 7 rows of the tile.  The online
+// softmax (running max m, sum l, in exp2 form, all fp32) needs no cross-warp
+// exchange because every row lives in one warp.  P^T is cast to the input
+// dtype and moved into the B-operand layout with movmatrix.trans, then
+//   O^T[D x 8] += V^T[D x 16 keys] . P^T[16 x 8]           (mma m16n8k16)
+// with V^T read by ldmatrix.trans from the same swizzled stage.
+//
+// Epilogue: the KG warp groups merge their (acc, m, l) in shared memory.  A
+// sequence cut into several segments then combines the segments of one
+// thread-block cluster through distributed shared memory (each CTA one
+// slice of the head dim), writes the cluster's partial to scratch and
+// increments a per-(sequence, kv head, row group) counter; the cluster that
+// arrives last merges every cluster partial and resets the counter to 0
+// (split-KV with an in-kernel merge; the counters of make_scratch are
+// "zeroed once; every launch leaves them zeroed").  With a cluster size of 1
+// this is the plain last-arriving-CTA merge.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "pd_internal.h"
+#include "pd_ptx.cuh"
+
+namespace pd {
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, std::true_type /*bf16*/) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, std::false_type /*fp16*/) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Column swizzle of the fp32 partial tiles in shared memory: rows 2x and 2x+1
+// of an n-tile are spread over four 8-word bank groups.
+__device__ __forceinline__ int psw(int d, int r) { return d ^ (((r >> 1) & 3) << 3); }
+
+template <bool BF16>
+__device__ __forceinline__ void store8(void *dst, const float (&v)[8]) {
+  using tag = std::integral_constant<bool, BF16>;
+  uint4 w;
+  w.x = pack2(v[0], v[1], tag{});
+  w.y = pack2(v[2], v[3], tag{});
+  w.z = pack2(v[4], v[5], tag{});
+  w.w = pack2(v[6], v[7], tag{});
+  *reinterpret_cast<uint4 *>(dst) = w;
+}
+
+template <bool BF16>
+__device__ __forceinline__ void store4(void *dst, const float (&v)[4]) {
+  using tag = std::integral_constant<bool, BF16>;
+  uint2 w;
+  w.x = pack2(v[0], v[1], tag{});
+  w.y = pack2(v[2], v[3], tag{});
+  *reinterpret_cast<uint2 *>(dst) = w;
+}
+
+__device__ __forceinline__ float exp2_or_zero(float x, float m) {
+  // e^(x - m) in exp2 form; 0 for an empty row (x = -inf)
+  return x == -INFINITY ? 0.f : exp2f(x - m);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    pd_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ Params p) {
+  using tag = std::integral_constant<bool, BF16>;
+  using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
+  constexpr int NBOX = D / 64;                  // 128-byte boxes across the head dim
+  constexpr int BLOCK_BYTES = kBlockKeys * D * 2;
+  constexpr int TB = kStageBytes / 2 / BLOCK_BYTES;  // 16-key blocks per stage
+  constexpr int KS = D / 16;                    // mma k-steps over d, and m-tiles of O^T
+  constexpr bool Q_IN_REGS = D <= 256;
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + kSmemAlign - 1) & ~uintptr_t(kSmemAlign - 1));
+  const int NS = p.NS, NT = p.NT, KG = p.KG, NC = NT * KG;
+  const int NT8 = NT * 8;
+  unsigned char *ring = smem;
+  unsigned char *qs = ring + NS * kStageBytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(qs + NT * D * 16);
+  uint64_t *empty = full + NS;
+  volatile int *flags = reinterpret_cast<volatile int *>(empty + NS);  // [0] abort, [1] last
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int s = blockIdx.y;
+  const int seg = blockIdx.x % p.max_seg;
+  const int hg = blockIdx.x / p.max_seg;
+  const int h = hg / p.rg, grow = hg % p.rg;
+
+  // ---- key ranges --------------------------------------------------------
+  int L = __ldg(p.seq_lens + s);
+  if (L < 0) L = 0;
+  if (L > p.bt_width * p.P) {
+    if (tid == 0 && seg == 0) atomicOr(p.status, 0x4u);
+    L = p.bt_width * p.P;
+  }
+  const int rr0 = grow * p.rows_cta;
+  const int rr1 = min(p.R, rr0 + p.rows_cta);
+  int u_lo = 0, u_hi = 0, v_lo = 0, v_hi = 0;  // union / intersection of the rows' key ranges
+  if (rr1 > rr0) {
+    const int n0 = max(L - p.M + rr0 / p.G + 1, 0);
+    const int n1 = max(L - p.M + (rr1 - 1) / p.G + 1, 0);
+    u_hi = n1;
+    v_hi = n0;
+    u_lo = p.window ? max(0, n0 - p.window) : 0;
+    v_lo = p.window ? max(0, n1 - p.window) : 0;
+  }
+  const int b_first = u_lo / kBlockKeys;
+  const int nb = u_hi > u_lo ? (u_hi + kBlockKeys - 1) / kBlockKeys - b_first : 0;
+  const int sb = max(p.seg_blocks, (nb + p.max_seg - 1) / p.max_seg);
+  const int nseg = max(1, (nb + sb - 1) / sb);
+  const int ncl = (nseg + p.CS - 1) / p.CS;
+  const int cl_id = seg / p.CS;
+  if (cl_id >= ncl) return;         // uniform over the cluster
+  if (nseg == 1 && seg > 0) return;  // no merge: only segment 0 works
+  const int my_b0 = b_first + seg * sb;
+  const int my_nb = max(0, min(b_first + nb, my_b0 + sb) - my_b0);
+  const int ntile = (my_nb + TB - 1) / TB;
+
+  // ---- set-up: barriers and the Q tile --------------------------------------
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(full + i), 1);
+      mbar_init(smem_u32(empty + i), NT);
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  {
+    const T *qbase = static_cast<const T *>(p.q);
+    for (int idx = tid; idx < NT8 * (D / 8); idx += blockDim.x) {
+      const int r = idx / (D / 8), c = idx % (D / 8);
+      const int rr = rr0 + r;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < p.rows_cta && rr < p.R) {
+        const int i = rr / p.G, j = rr % p.G;
+        v = __ldg(reinterpret_cast<const uint4 *>(qbase + (int64_t)(s * p.M + i) * p.q_s0 +
+                                                  (int64_t)(h * p.G + j) * p.q_s1 + c * 8));
+      }
+      const int tn = r >> 3, rw = r & 7, box = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4 *>(qs + (tn * NBOX + box) * 1024 + rw * 128 + ((cc ^ rw) << 4)) = v;
+    }
+  }
+  __syncthreads();
+
+  // Consumer state (kept in registers across the main loop).
+  float acc[KS][4];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  const int t_n = warp % NT, g_k = warp / NT;
+  const int r0 = t_n * 8 + 2 * (lane & 3), r1 = r0 + 1;
+
+  if (warp == NC) {
+    // ================= producer: the page gather ===========================
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
+    const int32_t *bt_row = p.block_table + (int64_t)s * p.bt_stride;
+    int issued = 0;
+    for (int j = 0; j < ntile; ++j) {
+      const int slot = j % NS;
+      if (j >= NS) {
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait_bounded(smem_u32(empty + slot), ((j / NS) - 1) & 1);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0) {
+            flags[0] = 1;
+            atomicOr(p.status, 0x1u);
+          }
+          break;
+        }
+      }
+      if (flags[0]) break;
+      const int nbt = min(TB, my_nb - j * TB);
+      if (lane == 0) mbar_arrive_expect_tx(smem_u32(full + slot), nbt * 2 * BLOCK_BYTES);
+      __syncwarp();
+      if (lane < nbt * NBOX * 2) {
+        const int kv = lane / (nbt * NBOX);
+        const int rem = lane % (nbt * NBOX);
+        const int b = rem / NBOX, box = rem % NBOX;
+        const int key0 = (my_b0 + j * TB + b) * kBlockKeys;
+        const int page = key0 / p.P, tok = key0 % p.P;
+        int phys = __ldg(bt_row + page);
+        if ((unsigned)phys >= (unsigned)p.num_pool_blocks) {
+          atomicOr(p.status, 0x2u);
+          phys = 0;
+        }
+        const uint32_t dst =
+            smem_u32(ring + slot * kStageBytes + kv * (TB * BLOCK_BYTES) + (b * NBOX + box) * 2048);
+        const int c1 = p.layout == 1 ? tok : h;
+        const int c2 = p.layout == 1 ? h : tok;
+        tma_load_4d(dst, kv ? &tmV : &tmK, smem_u32(full + slot), box * 64, c1, c2, phys, pol);
+      }
+      issued = j + 1;
+    }
+    // Leave no copy in flight: wait (bounded) for the last stages issued.
+    if (lane == 0) {
+      for (int j = max(0, issued - NS); j < issued; ++j)
+        if (!mbar_wait_bounded(smem_u32(full + j % NS), (j / NS) & 1)) atomicOr(p.status, 0x1u);
+    }
+  } else {
+    // ================= consumers ==========================================
+    // Visible key range of this thread's two rows (empty for padding rows).
+    int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+    {
+      const int rra = rr0 + r0, rrb = rr0 + r1;
+      if (r0 < p.rows_cta && rra < p.R) {
+        hi0 = max(L - p.M + rra / p.G + 1, 0);
+        lo0 = p.window ? max(0, hi0 - p.window) : 0;
+      }
+      if (r1 < p.rows_cta && rrb < p.R) {
+        hi1 = max(L - p.M + rrb / p.G + 1, 0);
+        lo1 = p.window ? max(0, hi1 - p.window) : 0;
+      }
+    }
+    const uint32_t qs_u32 = smem_u32(qs) + t_n * NBOX * 1024;
+    uint32_t qf[Q_IN_REGS ? KS : 1][2];
+    if constexpr (Q_IN_REGS) {
+#pragma unroll
+      for (int ks = 0; ks < KS; ks += 2) {
+        const int row = lane & 7, chunk = 2 * ks + (lane >> 3);
+        uint32_t r[4];
+        ldsm_x4(qs_u32 + (chunk >> 3) * 1024 + row * 128 + (((chunk & 7) ^ row) << 4), r);
+        qf[ks][0] = r[0];
+        qf[ks][1] = r[1];
+        qf[ks + 1][0] = r[2];
+        qf[ks + 1][1] = r[3];
+      }
+    }
+    const int k_row = lane & 15, k_hi = lane >> 4;                     // K ldmatrix roles
+    const int v_row = (lane & 7) + ((lane >> 4) << 3), v_hi = (lane >> 3) & 1;  // V^T roles
+
+    for (int j = g_k; j < ntile; j += KG) {
+      const int slot = j % NS;
+      if (!mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1)) {
+        if (lane == 0) {
+          flags[0] = 1;
+          atomicOr(p.status, 0x1u);
+        }
+        break;
+      }
+      const int nbt = min(TB, my_nb - j * TB);
+      const uint32_t kbase = smem_u32(ring + slot * kStageBytes);
+      const uint32_t vbase = kbase + TB * BLOCK_BYTES;
+      const int key_t0 = (my_b0 + j * TB) * kBlockKeys;
+
+      // S^T = K Q^T for every block of the stage
+      float sc[TB][4];
+#pragma unroll
+      for (int b = 0; b < TB; ++b) sc[b][0] = sc[b][1] = sc[b][2] = sc[b][3] = 0.f;
+      if constexpr (Q_IN_REGS) {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const int chunk = 2 * ks + k_hi;
+          const uint32_t off = (chunk >> 3) * 2048 + k_row * 128 + (((chunk & 7) ^ (k_row & 7)) << 4);
+#pragma unroll
+          for (int b = 0; b < TB; ++b) {
+            if (b < nbt) {
+              uint32_t a[4];
+              ldsm_x4(kbase + b * BLOCK_BYTES + off, a);
+              mma_16816<BF16>(sc[b], a, qf[ks][0], qf[ks][1]);
+            }
+          }
+        }
+      } else {
+        // D = 512: one block per stage; two accumulators break the k-step chain
+        float sc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < KS; ks += 2) {
+          uint32_t qr[4];
+          {
+            const int row = lane & 7, chunk = 2 * ks + (lane >> 3);
+            ldsm_x4(qs_u32 + (chunk >> 3) * 1024 + row * 128 + (((chunk & 7) ^ row) << 4), qr);
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int chunk = 2 * (ks + u) + k_hi;
+            uint32_t a[4];
+            ldsm_x4(kbase + (chunk >> 3) * 2048 + k_row * 128 +
+                        (((chunk & 7) ^ (k_row & 7)) << 4),
+                    a);
+            if (u == 0)
+              mma_16816<BF16>(sc[0], a, qr[0], qr[1]);
+            else
+              mma_16816<BF16>(sc2, a, qr[2], qr[3]);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[0][e] += sc2[e];
+      }
+
+      // scale, mask, running max
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int b = 0; b < TB; ++b) {
+        const int key0 = key_t0 + b * kBlockKeys;
+        if (b >= nbt) {
+          sc[b][0] = sc[b][1] = sc[b][2] = sc[b][3] = -INFINITY;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[b][e] *= p.scale_log2;
+          if (!(key0 >= v_lo && key0 + kBlockKeys <= v_hi)) {
+            const int ka = key0 + (lane >> 2), kb = ka + 8;
+            if (!(ka >= lo0 && ka < hi0)) sc[b][0] = -INFINITY;
+            if (!(ka >= lo1 && ka < hi1)) sc[b][1] = -INFINITY;
+            if (!(kb >= lo0 && kb < hi0)) sc[b][2] = -INFINITY;
+            if (!(kb >= lo1 && kb < hi1)) sc[b][3] = -INFINITY;
+          }
+        }
+        mx0 = fmaxf(mx0, fmaxf(sc[b][0], sc[b][2]));
+        mx1 = fmaxf(mx1, fmaxf(sc[b][1], sc[b][3]));
+      }
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+      const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = exp2_or_zero(m0, mu0), al1 = exp2_or_zero(m1, mu1);
+      m0 = mn0;
+      m1 = mn1;
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+          acc[i][0] *= al0;
+          acc[i][1] *= al1;
+          acc[i][2] *= al0;
+          acc[i][3] *= al1;
+        }
+      }
+      l0 *= al0;
+      l1 *= al1;
+
+      // P = exp2(S - m); PV
+#pragma unroll
+      for (int b = 0; b < TB; ++b) {
+        if (b < nbt) {
+          const float p0 = exp2_or_zero(sc[b][0], mu0), p1 = exp2_or_zero(sc[b][1], mu1);
+          const float p2 = exp2_or_zero(sc[b][2], mu0), p3 = exp2_or_zero(sc[b][3], mu1);
+          l0 += p0 + p2;
+          l1 += p1 + p3;
+          const uint32_t pb0 = movmatrix_trans(pack2(p0, p1, tag{}));
+          const uint32_t pb1 = movmatrix_trans(pack2(p2, p3, tag{}));
+          const int key0 = key_t0 + b * kBlockKeys;
+          const bool vmask = !(key0 >= u_lo && key0 + kBlockKeys <= u_hi);
+          uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+          if (vmask) {
+            // zero V of keys outside every row's range (stale or NaN slots)
+            const int ke = key0 + 2 * (lane & 3);
+            mlo = ((ke >= u_lo && ke < u_hi) ? 0x0000ffffu : 0u) |
+                  ((ke + 1 >= u_lo && ke + 1 < u_hi) ? 0xffff0000u : 0u);
+            mhi = ((ke + 8 >= u_lo && ke + 8 < u_hi) ? 0x0000ffffu : 0u) |
+                  ((ke + 9 >= u_lo && ke + 9 < u_hi) ? 0xffff0000u : 0u);
+          }
+          const uint32_t vb = vbase + b * BLOCK_BYTES;
+#pragma unroll
+          for (int mt = 0; mt < KS; ++mt) {
+            const int chunk = 2 * mt + v_hi;
+            uint32_t a[4];
+            ldsm_x4_trans(vb + (chunk >> 3) * 2048 + v_row * 128 + (((chunk & 7) ^ (v_row & 7)) << 4),
+                          a);
+            if (vmask) {
+              a[0] &= mlo;
+              a[1] &= mlo;
+              a[2] &= mhi;
+              a[3] &= mhi;
+            }
+            mma_16816<BF16>(acc[mt], a, pb0, pb1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(empty + slot));
+    }
+    // full row sums: the 8 lanes of one (lane & 3) class hold one row pair
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+  }
+
+  // ================= epilogue ==============================================
+  __syncthreads();  // ring and Q tile are dead from here on
+  float *ep = reinterpret_cast<float *>(smem);
+  float *cp = ep;                          // [KG][NT8][D] (swizzled columns)
+  float *mrow = cp + (size_t)KG * NT8 * D;  // [KG][NT8]
+  float *lrow = mrow + KG * NT8;
+  float *mfin = lrow + KG * NT8;  // [NT8]
+  float *lfin = mfin + NT8;
+
+  if (warp < NC && lane < 4) {
+    mrow[g_k * NT8 + r0] = m0;
+    mrow[g_k * NT8 + r1] = m1;
+    lrow[g_k * NT8 + r0] = l0;
+    lrow[g_k * NT8 + r1] = l1;
+  }
+  __syncthreads();
+  if (warp < NC) {
+    float ms0 = -INFINITY, ms1 = -INFINITY;
+    for (int gg = 0; gg < KG; ++gg) {
+      ms0 = fmaxf(ms0, mrow[gg * NT8 + r0]);
+      ms1 = fmaxf(ms1, mrow[gg * NT8 + r1]);
+    }
+    const float f0 = exp2_or_zero(m0, ms0 == -INFINITY ? 0.f : ms0);
+    const float f1 = exp2_or_zero(m1, ms1 == -INFINITY ? 0.f : ms1);
+    float *dst = cp + (size_t)g_k * NT8 * D;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      const int d = mt * 16 + (lane >> 2);
+      dst[r0 * D + psw(d, r0)] = acc[mt][0] * f0;
+      dst[r1 * D + psw(d, r1)] = acc[mt][1] * f1;
+      dst[r0 * D + psw(d + 8, r0)] = acc[mt][2] * f0;
+      dst[r1 * D + psw(d + 8, r1)] = acc[mt][3] * f1;
+    }
+  }
+  __syncthreads();
+  if (KG > 1) {
+    for (int idx = tid; idx < NT8 * D / 4; idx += blockDim.x) {
+      float4 a = reinterpret_cast<float4 *>(cp)[idx];
+      for (int gg = 1; gg < KG; ++gg) {
+        const float4 b = reinterpret_cast<float4 *>(cp + (size_t)gg * NT8 * D)[idx];
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+      }
+      reinterpret_cast<float4 *>(cp)[idx] = a;
+    }
+  }
+  for (int r = tid; r < NT8; r += blockDim.x) {
+    float ms = -INFINITY;
+    for (int gg = 0; gg < KG; ++gg) ms = fmaxf(ms, mrow[gg * NT8 + r]);
+    const float mu = ms == -INFINITY ? 0.f : ms;
+    float lsum = 0.f;
+    for (int gg = 0; gg < KG; ++gg) lsum += lrow[gg * NT8 + r] * exp2_or_zero(mrow[gg * NT8 + r], mu);
+    mfin[r] = ms;
+    lfin[r] = lsum;
+  }
+  __syncthreads();
+
+  T *obase = static_cast<T *>(p.out);
+  auto out_row = [&](int r) -> T * {
+    const int rr = rr0 + r;
+    const int i = rr / p.G, j = rr % p.G;
+    return obase + (int64_t)(s * p.M + i) * p.o_s0 + (int64_t)(h * p.G + j) * p.o_s1;
+  };
+  const int nrows = max(0, rr1 - rr0);  // valid rows of this CTA
+
+  if (nseg == 1) {
+    // one segment: normalise and store
+    for (int idx = tid; idx < nrows * (D / 8); idx += blockDim.x) {
+      const int r = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
+      const float lr = lfin[r];
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
+      const float4 a = *reinterpret_cast<const float4 *>(cp + r * D + psw(c8, r));
+      const float4 b = *reinterpret_cast<const float4 *>(cp + r * D + psw(c8 + 4, r));
+      const float v[8] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv,
+                          b.x * inv, b.y * inv, b.z * inv, b.w * inv};
+      store8<BF16>(out_row(r) + c8, v);
+    }
+    return;
+  }
+
+  // ---- combine the segments of this cluster (cluster size 1: a copy) ----
+  const int CS = p.CS;
+  const int DS = D / CS;
+  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
+  float *clp = lfin + NT8;               // [NT8][DS] cluster partial slice
+  float *mcl = clp + NT8 * DS;           // [NT8]
+  float *lcl = mcl + NT8;                // [NT8]
+  float *wts = lcl + NT8;                // [CS][NT8]
+  if (CS > 1) cluster_sync();            // every CTA's partial is in its shared memory
+  for (int r = tid; r < NT8; r += blockDim.x) {
+    float mr[8];
+    float ms = -INFINITY;
+    for (int x = 0; x < CS; ++x) {
+      mr[x] = CS > 1 ? ld_dsmem_f32(mapa(smem_u32(mfin + r), x)) : mfin[r];
+      ms = fmaxf(ms, mr[x]);
+    }
+    const float mu = ms == -INFINITY ? 0.f : ms;
+    float lsum = 0.f;
+    for (int x = 0; x < CS; ++x) {
+      const float w = exp2_or_zero(mr[x], mu);
+      const float lx = CS > 1 ? ld_dsmem_f32(mapa(smem_u32(lfin + r), x)) : lfin[r];
+      lsum += lx * w;
+      wts[x * NT8 + r] = w;
+    }
+    mcl[r] = ms;
+    lcl[r] = lsum;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < NT8 * (DS / 4); idx += blockDim.x) {
+    const int r = idx / (DS / 4), d = (int)rank * DS + (idx % (DS / 4)) * 4;
+    const uint32_t local = smem_u32(cp + r * D + psw(d, r));
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int x = 0; x < CS; ++x) {
+      const float w = wts[x * NT8 + r];
+      const float4 b = CS > 1 ? ld_dsmem_f32x4(mapa(local, x))
+                              : *reinterpret_cast<const float4 *>(cp + r * D + psw(d, r));
+      a.x += w * b.x;
+      a.y += w * b.y;
+      a.z += w * b.z;
+      a.w += w * b.w;
+    }
+    *reinterpret_cast<float4 *>(clp + r * DS + (d - (int)rank * DS)) = a;
+  }
+  if (CS > 1)
+    cluster_sync();  // no CTA reads another's shared memory after this
+  else
+    __syncthreads();
+
+  if (ncl == 1) {
+    for (int idx = tid; idx < nrows * (DS / 8); idx += blockDim.x) {
+      const int r = idx / (DS / 8), c8 = (idx % (DS / 8)) * 8;
+      const float lr = lcl[r];
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
+      const float *src = clp + r * DS + c8;
+      const float v[8] = {src[0] * inv, src[1] * inv, src[2] * inv, src[3] * inv,
+                          src[4] * inv, src[5] * inv, src[6] * inv, src[7] * inv};
+      store8<BF16>(out_row(r) + (int)rank * DS + c8, v);
+    }
+    return;
+  }
+
+  // ---- several clusters: publish this cluster's partial, count arrivals ----
+  const int group = (s * p.Hkv + h) * p.rg + grow;
+  const int64_t gbase = (int64_t)group * p.max_parts;
+  {
+    float *pa = p.part_acc + (gbase + cl_id) * NT8 * D + (int)rank * DS;
+    for (int idx = tid; idx < NT8 * (DS / 4); idx += blockDim.x) {
+      const int r = idx / (DS / 4), d4 = (idx % (DS / 4)) * 4;
+      __stcg(reinterpret_cast<float4 *>(pa + (int64_t)r * D + d4),
+             *reinterpret_cast<const float4 *>(clp + r * DS + d4));
+    }
+    if (rank == 0) {
+      float *pm = p.part_ml + (gbase + cl_id) * NT8 * 2;
+      for (int r = tid; r < NT8; r += blockDim.x) __stcg(reinterpret_cast<float2 *>(pm) + r, make_float2(mcl[r], lcl[r]));
+    }
+  }
+  __threadfence();
+  if (CS > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+  if (rank == 0 && tid == 0) {
+    const int old = atomicAdd(p.counters + group, 1);
+    const int last = old == ncl - 1;
+    if (last) atomicExch(p.counters + group, 0);
+    __threadfence();
+    flags[1] = last;
+    for (int x = 1; x < CS; ++x) st_dsmem_u32(mapa(smem_u32((const void *)(flags + 1)), x), (uint32_t)last);
+  }
+  if (CS > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+  if (!flags[1]) return;
+  __threadfence();
+
+  // ---- the last cluster merges every cluster partial (its own slice) ----
+  float *pm_s = ep;                 // [ncl][NT8] max, then weights
+  float *pl_s = pm_s + ncl * NT8;   // [ncl][NT8] sums
+  float *lall = pl_s + ncl * NT8;   // [NT8]
+  for (int idx = tid; idx < ncl * NT8; idx += blockDim.x) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + gbase * NT8 * 2) + idx);
+    pm_s[idx] = ml.x;
+    pl_s[idx] = ml.y;
+  }
+  __syncthreads();
+  for (int r = tid; r < NT8; r += blockDim.x) {
+    float ms = -INFINITY;
+    for (int c = 0; c < ncl; ++c) ms = fmaxf(ms, pm_s[c * NT8 + r]);
+    const float mu = ms == -INFINITY ? 0.f : ms;
+    float lsum = 0.f;
+    for (int c = 0; c < ncl; ++c) {
+      const float w = exp2_or_zero(pm_s[c * NT8 + r], mu);
+      pm_s[c * NT8 + r] = w;
+      lsum += pl_s[c * NT8 + r] * w;
+    }
+    lall[r] = lsum;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < nrows * (DS / 4); idx += blockDim.x) {
+    const int r = idx / (DS / 4), d = (int)rank * DS + (idx % (DS / 4)) * 4;
+    const float *src = p.part_acc + gbase * NT8 * D + (int64_t)r * D + d;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int c = 0; c < ncl; ++c) {
+      const float w = pm_s[c * NT8 + r];
+      const float4 b = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)c * NT8 * D));
+      a.x += w * b.x;
+      a.y += w * b.y;
+      a.z += w * b.z;
+      a.w += w * b.w;
+    }
+    const float lr = lall[r];
+    const float inv = lr > 0.f ? 1.f / lr : 0.f;
+    const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
+    store4<BF16>(out_row(r) + d, v);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_mma_t(const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
+                         const Launch &l, cudaStream_t stream) {
+  auto kern = pd_decode_mma<D, BF16>;
+  // largest dynamic shared memory opted into so far, per device
+  static int configured_smem[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (l.smem > configured_smem[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, l.smem);
+    if (e != cudaSuccess) return e;
+    configured_smem[dev] = l.smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = l.grid;
+  cfg.blockDim = l.block;
+  cfg.dynamicSmemBytes = l.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (l.cluster > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = l.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+}  // namespace pd

@@ -1,0 +1,12 @@
+// Instantiation of the tensor-core decode kernel for head size 64.
+#include "pd_kernel.cuh"
+
+namespace pd {
+
+cudaError_t launch_mma_d64(bool bf16, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const Params &p, const Launch &l, cudaStream_t stream) {
+  return bf16 ? launch_mma_t<64, true>(tk, tv, p, l, stream)
+              : launch_mma_t<64, false>(tk, tv, p, l, stream);
+}
+
+}  // namespace pd

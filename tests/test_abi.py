@@ -1,0 +1,167 @@
+"""The C ABI on the CPU: the library loads, exports every declared symbol,
+and its host-side logic (argument checks, plan, scratch sizing) behaves,
+all without a GPU."""
+
+import ctypes
+
+import pytest
+import torch
+
+import paged_split_kv_02_gb300 as pd
+from paged_split_kv_02_gb300 import workloads as W
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pd.build()
+    return pd.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = pd.declared_symbols()
+    assert len(names) == 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_strerror(lib):
+    assert pd.paged_decode_version() == 10000
+    for code in range(0, -9, -1):
+        assert lib.paged_decode_strerror(code)
+    assert b"unknown" in lib.paged_decode_strerror(-99)
+
+
+def test_scratch_bytes():
+    a = pd.paged_decode_scratch_bytes(1, 32, 8, 128, 4, 16)
+    b = pd.paged_decode_scratch_bytes(1, 32, 8, 128, 4, 32)
+    c = pd.paged_decode_scratch_bytes(2, 32, 8, 128, 4, 16)
+    assert 0 < a < b and a < c
+    # acc (rows * D) + m, l (2 * rows), per partial: rows = 16 at G=4, M=4
+    assert b - a == pytest.approx(16 * 8 * 16 * (128 + 2) * 4, abs=1024)
+    assert pd.paged_decode_scratch_bytes(1, 32, 8, 96, 4, 16) == 0      # head size
+    assert pd.paged_decode_scratch_bytes(1, 32, 8, 128, 9, 16) == 0     # M > 8
+    assert pd.paged_decode_scratch_bytes(1, 30, 8, 128, 1, 16) == 0     # Hq % Hkv
+
+
+def _fake_scratch(S, Hq, Hkv, D, M, splits):
+    d = pd.PdScratch()
+    d.data = 1 << 30
+    d.bytes = pd.paged_decode_scratch_bytes(S, Hq, Hkv, D, M, splits)
+    d.counter_slots = S * Hkv * 8
+    return d
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 8, 2, 128, 16, 1, 0, 19),       # single sequence, NHD test case
+    (1, 32, 8, 128, 16, 4, 0, 2048),    # spec decode, 32k
+    (1, 8, 1, 256, 32, 4, 512, 1024),   # sliding window
+    (1, 8, 1, 512, 16, 8, 0, 2048),     # wide head, 64 packed rows
+    (64, 16, 2, 256, 1056, 4, 0, 16),   # batched, hybrid pages
+])
+def test_plan_invariants(shape):
+    S, Hq, Hkv, D, P, M, w, Wd = shape
+    sd = _fake_scratch(S, Hq, Hkv, D, M, 256)
+    p = pd.paged_decode_plan(S, Hq, Hkv, D, P, M, w, Wd, 152, scratch_desc=sd)
+    G = Hq // Hkv
+    assert p["rows"] == G * M
+    assert p["rows_per_cta"] * p["row_groups"] >= G * M
+    assert p["n_tiles"] * 8 >= p["rows_per_cta"]
+    assert p["n_tiles"] * p["key_groups"] <= 8
+    assert p["stages"] % p["key_groups"] == 0          # slot -> warp group is static
+    assert p["max_segments"] % p["cluster"] == 0
+    assert p["grid_x"] == Hkv * p["row_groups"] * p["max_segments"]
+    assert p["grid_y"] == S
+    assert p["block_threads"] == 32 * (p["n_tiles"] * p["key_groups"] + 1)
+    assert p["smem_bytes"] <= 232448
+    assert p["scratch_needed"] <= sd.bytes
+    # the segments cover every 16-key block a row can see
+    nb_max = -(-Wd * P // 16)
+    if w:
+        nb_max = min(nb_max, -(-(w + M - 1) // 16) + 1)
+    assert p["seg_blocks"] * p["max_segments"] >= nb_max
+    if S == 1 and Wd * P >= 32768 and not w:
+        assert p["grid_x"] >= 128                      # a long sequence fills the SMs
+
+
+def test_plan_without_scratch_does_not_split():
+    p = pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 2048, 152)
+    assert p["max_parts"] == 0 and p["scratch_needed"] == 0
+    assert p["max_segments"] == 1
+
+
+def test_plan_shrinks_to_small_scratch():
+    small = _fake_scratch(1, 32, 8, 128, 4, 3)
+    p = pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 2048, 152, scratch_desc=small)
+    assert 0 < p["scratch_needed"] <= small.bytes
+    assert p["max_parts"] <= 3
+
+
+def test_plan_forced_knobs_and_errors():
+    sd = _fake_scratch(1, 32, 8, 128, 4, 64)
+    p = pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 256, 152, scratch_desc=sd,
+                             opts=pd.options(segments=16, cluster=4, key_groups=2, stages=4))
+    assert (p["max_segments"], p["cluster"], p["key_groups"], p["stages"]) == (16, 4, 2, 4)
+    assert p["max_parts"] == 4
+    with pytest.raises(pd.PagedDecodeError):   # stages not a multiple of the warp groups
+        pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 256, 152, scratch_desc=sd,
+                             opts=pd.options(key_groups=4, stages=6))
+    with pytest.raises(pd.PagedDecodeError):   # segments not a multiple of the cluster
+        pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 256, 152, scratch_desc=sd,
+                             opts=pd.options(segments=6, cluster=4))
+    with pytest.raises(pd.PagedDecodeError) as e:
+        pd.paged_decode_plan(1, 32, 8, 96, 16, 4, 0, 256, 152)
+    assert e.value.code == -3
+    with pytest.raises(pd.PagedDecodeError) as e:
+        pd.paged_decode_plan(1, 32, 8, 128, 16, 9, 0, 256, 152)
+    assert e.value.code == -4
+    with pytest.raises(pd.PagedDecodeError) as e:
+        pd.paged_decode_plan(1, 32, 8, 128, 24, 4, 0, 256, 152)   # page size % 16
+    assert e.value.code == -1
+    big = _fake_scratch(1, 32, 8, 128, 4, 1)
+    with pytest.raises(pd.PagedDecodeError) as e:  # forced split that the scratch cannot hold
+        pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 2048, 152, scratch_desc=big,
+                             opts=pd.options(segments=64))
+    assert e.value.code == -6
+
+
+def _cpu_case(**kw):
+    base = dict(seed=0, dtype=torch.float16, head_size=128, num_q_heads=8, num_kv_heads=2,
+                page_size=16, max_query_len=2, seq_lens=[40, 7], layout=W.HND)
+    base.update(kw)
+    return W.make_case("abi", **base)
+
+
+def _call(case, **over):
+    args = dict(q=case.q, k_cache=case.k_cache, v_cache=case.v_cache,
+                block_table=case.block_table, seq_lens=case.seq_lens, out=torch.empty_like(case.q),
+                num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads,
+                head_size=case.head_size, page_size=case.page_size,
+                max_query_len=case.max_query_len, window=case.window, scale=case.scale,
+                layout=case.layout)
+    args.update(over)
+    return pd.paged_decode_attn(**args, stream=0, check=False)
+
+
+def test_argument_checks_on_host():
+    """Every malformed call is refused before any CUDA call (these run on a
+    machine without a GPU)."""
+    c = _cpu_case()
+    assert _call(c, head_size=96) == -3
+    assert _call(c, max_query_len=0) == -4
+    assert _call(c, max_query_len=9) == -4
+    assert _call(c, num_q_heads=6) == -1              # Hq % Hkv, and q's shape
+    assert _call(c, page_size=8) == -1
+    assert _call(c, window=-1) == -1
+    assert _call(c, layout=3) == -1
+    assert _call(c, scale=float("nan")) == -1
+    assert _call(c, out=torch.empty_like(c.q, dtype=torch.bfloat16)) == -2
+    assert _call(c, q=c.q.float()) == -2
+    assert _call(c, seq_lens=c.seq_lens.long()) == -2
+    assert _call(c, block_table=c.block_table[:1]) == -1
+    assert _call(c, q=c.q[:, :, :64]) == -1
+    q_odd = torch.empty(c.q.shape[0], c.q.shape[1], 129, dtype=c.q.dtype)[:, :, 1:]
+    assert _call(c, q=q_odd) == -5                    # rows not 16-byte aligned
+    assert _call(c, k_cache=c.k_cache.transpose(1, 2)) == -1
+    # a well-formed call on a machine without an sm_103 device
+    if not torch.cuda.is_available():
+        assert _call(c) == -8
