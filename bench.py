@@ -1,0 +1,436 @@
+"""Benchmark of the paged decode-attention kernel on GB300.
+
+Workload (the spec-decode sweep the headline metric is quoted on): bf16,
+head size 128, 32 q / 8 kv heads, page size 16, HND cache, batch 1,
+M in {1, 2, 3, 4} query tokens x contexts {128, 1k, 4k, 16k, 32k}.
+One step = one decode call for each of those 20 cases.
+
+Every input is seeded synthetic data made on the device.  Between two uses
+of a replica at least the rest of the sweep (~850 MB, more than the 126 MB
+L2) passes, so every call reads its K/V from HBM.  Per-case times come from
+CUDA graphs that cycle through enough replicas of the case to exceed 2.2x
+the L2 size.  Times are CUDA events on the launching stream around graph
+replays; the clocks are sampled with nvidia-smi during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs the same workload on its own GPU (replicas
+only: the path has no cross-GPU exchange); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "KV-read GB/s and % of GB300 HBM peak; µs per decode attention call"
+UNIT = "GB/s"
+CONTEXTS = (128, 1024, 4096, 16384, 32768)
+MS = (1, 2, 3, 4)
+WORKLOAD = ("spec-decode sweep: bf16, head_size 128, 32 q / 8 kv heads, page_size 16, HND, "
+            "batch 1, M in {1,2,3,4} x contexts {128, 1k, 4k, 16k, 32k}; one step = one call "
+            "per case")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during a timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in self.samples if num(p[0]) is not None]
+        mx = [num(p[1]) for p in self.samples if num(p[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for p in self.samples for n, v in zip(names, p[3:7]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+def build_sweep(device, l2_bytes, only=None, rep_factor=2.2, seed0=0):
+    """Per case: replicas of the inputs, enough to exceed rep_factor x L2."""
+    from paged_split_kv_02_gb300 import workloads as W
+
+    cases = {}
+    for M in MS:
+        for L in CONTEXTS:
+            if only and (M, L) not in only:
+                continue
+            probe = W.spec_decode_hnd(M, 16)
+            kv = L * probe.num_kv_heads * 2 * probe.head_size * 2
+            n_rep = max(2, math.ceil(rep_factor * l2_bytes / kv))
+            reps = [W.spec_decode_hnd(M, L, seed=seed0 + 1000 * M + r, device=device,
+                                      gen_device=device) for r in range(n_rep)]
+            cases[(M, L)] = reps
+    return cases
+
+
+def run_ours(args, world, rank, local):
+    import paged_split_kv_02_gb300 as pd
+
+    pd.build()
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 << 20))
+    peak, peak_kind = _peaks()
+    cases = build_sweep(device, l2, only=args.only)
+    first = next(iter(cases.values()))[0]
+    scratch = pd.Scratch(1, first.num_q_heads, first.num_kv_heads, first.head_size, max(MS),
+                         max_splits=256, device=device)
+    outs = {k: [torch.empty_like(r.q) for r in reps] for k, reps in cases.items()}
+    stream = torch.cuda.Stream(device=device)
+    keys = sorted(cases)
+
+    def call(k, r, st=None):
+        pd.decode_case(cases[k][r], out=outs[k][r], scratch=scratch, stream=st)
+
+    # warm the library (attributes, tensor maps) outside capture
+    with torch.cuda.stream(stream):
+        for k in keys:
+            for r in range(len(cases[k])):
+                call(k, r)
+    torch.cuda.synchronize()
+
+    # ---- step graphs: one call per case, replicas alternating ------------
+    n_step_graphs = 2
+    step_graphs = []
+    for gi in range(n_step_graphs):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in keys:
+                call(k, gi % len(cases[k]))
+        step_graphs.append(g)
+    torch.cuda.synchronize()
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step_graphs[i % n_step_graphs].replay()
+    torch.cuda.synchronize()
+    _barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(args.steps):
+                step_graphs[i % n_step_graphs].replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        _barrier(world)
+        torch.cuda.synchronize()
+    step_ms = ev0.elapsed_time(ev1) / args.steps
+    step_ms = _max_over_ranks(step_ms, world)
+    kv_step = sum(cases[k][0].kv_bytes_touched() for k in keys)
+    alg_step = sum(cases[k][0].algorithmic_bytes() for k in keys)
+    value = world * kv_step / (step_ms * 1e-3) / 1e9
+    launches = args.steps * len(keys)
+
+    # ---- per case: graphs over the case's replicas -------------------------
+    per_case = []
+    for k in keys:
+        g = torch.cuda.CUDAGraph()
+        n = len(cases[k])
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(n):
+                call(k, r)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+            reps = max(3, min(50, int(2000 / n)))
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * n)
+        c = cases[k][0]
+        kv_gbs = c.kv_bytes_touched() / (us * 1e-6) / 1e9
+        alg_gbs = c.algorithmic_bytes() / (us * 1e-6) / 1e9
+        per_case.append({"M": k[0], "context": k[1], "us": round(us, 3),
+                         "kv_gbs": round(kv_gbs, 1), "pct_hbm": round(100 * alg_gbs / peak, 2),
+                         "replicas": n})
+        del g
+    long_ctx = [c["pct_hbm"] for c in per_case if c["context"] >= 4096]
+
+    # ---- end to end through the C ABI with host buffers --------------------
+    e2e = None
+    if rank == 0 or world > 1:
+        e2e = measure_e2e(pd, cases, outs, scratch, stream, keys, args)
+
+    # ---- the oracle on the host (rank 0 only) -------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cases, keys)
+
+    status = pd.paged_decode_device_status(reset=True)
+    if rank != 0:
+        return
+    workload = WORKLOAD if not args.only else WORKLOAD + f"; restricted to (M, context) {sorted(args.only)}"
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/K/V, random page permutation)",
+        "config": {
+            "workload": workload,
+            "l2": "inputs larger than L2: rotating replicas, >= 2.2x L2 per case",
+            "timing": "CUDA graphs of the calls, CUDA events on the launching stream",
+            "parallelism": f"replicas x{world}",
+        },
+        "gpu_launches": launches,
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(alg_step / (step_ms * 1e-3) / 1e9, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(alg_step / (step_ms * 1e-3) / 1e9 / peak, 4),
+            "traffic": None,
+            "peak_kind": peak_kind,
+        },
+        "median_pct_hbm_4k_32k": round(statistics.median(long_ctx), 2) if long_ctx else None,
+        "cases": per_case,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def measure_e2e(pd, cases, outs, scratch, stream, keys, args):
+    """The same sweep through the C ABI with pinned host buffers: every step
+    copies each case's q, block table and seq_lens host->device, runs the
+    call and copies the output back."""
+    host_in, dev_in, host_out = {}, {}, {}
+    for k in keys:
+        c = cases[k][0]
+        host_in[k] = [t.cpu().pin_memory() for t in (c.q, c.block_table, c.seq_lens)]
+        dev_in[k] = [torch.empty_like(t) for t in (c.q, c.block_table, c.seq_lens)]
+        host_out[k] = torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for k in keys for t in host_in[k])
+    d2h = sum(host_out[k].numel() * host_out[k].element_size() for k in keys)
+    kv_step = sum(cases[k][0].kv_bytes_touched() for k in keys)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for k in keys:
+                for d, h in zip(dev_in[k], host_in[k]):
+                    d.copy_(h, non_blocking=True)
+                c = cases[k][0]
+                pd.paged_decode_attn(dev_in[k][0], c.k_cache, c.v_cache, dev_in[k][1],
+                                     dev_in[k][2], outs[k][0], c.num_q_heads, c.num_kv_heads,
+                                     c.head_size, c.page_size, c.max_query_len, c.window,
+                                     c.scale, c.layout, scratch, stream)
+                host_out[k].copy_(outs[k][0], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    return {"value": round(kv_step / dt / 1e9, 1), "unit": UNIT, "ms_per_step": round(dt * 1e3, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def _oracle_sweep(host_cases, keys, nthreads):
+    import oracle
+
+    t0 = time.perf_counter()
+    for k in keys:
+        oracle.attention(host_cases[k], nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cases, keys):
+    """The fp64 oracle on the host cores over one call of every case."""
+    import oracle
+
+    oracle.build()
+    host = {k: cases[k][0].to("cpu") for k in keys}
+    n = oracle.default_threads()
+    dt = _oracle_sweep(host, keys, n)
+    kv = sum(host[k].kv_bytes_touched() for k in keys)
+    return {"value": round(kv / dt / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": "one call of each of the 20 sweep cases (all heads), fp64 C oracle",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step runs it on the host cores
+    over one call of every sweep case (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    from paged_split_kv_02_gb300 import workloads as W
+
+    oracle.build()
+    keys = [(M, L) for M in MS for L in CONTEXTS]
+    host = {(M, L): W.spec_decode_hnd(M, L, seed=1000 * M) for (M, L) in keys}
+    n = oracle.default_threads()
+    kv = sum(host[k].kv_bytes_touched() for k in keys)
+    for _ in range(args.warmup):
+        _oracle_sweep(host, keys, n)
+    t = 0.0
+    for _ in range(args.steps):
+        t += _oracle_sweep(host, keys, n)
+    dt = t / args.steps
+    value = kv / dt / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/K/V, random page permutation)",
+        "config": {"workload": WORKLOAD, "parallelism": "host threads"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": n, "kind": "oracle",
+                         "sample": "one call of each of the 20 sweep cases per step"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cases", default="",
+                    help="restrict the sweep, e.g. 4:32768,1:4096 (profiling runs only)")
+    args = ap.parse_args()
+    args.only = None
+    if args.cases:
+        args.only = {tuple(int(x) for x in c.split(":")) for c in args.cases.split(",")}
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

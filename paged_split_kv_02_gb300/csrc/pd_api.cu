@@ -203,7 +203,10 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   const int TB = kStageBytes / 2 / (kBlockKeys * D * 2);
   const int fixed = smem_bytes(D, NT, 0);
   const int ns_max = std::min(8, (kSmemLimit - fixed - 16 * 8) / kStageBytes);
-  int KG = o.key_groups > 0 ? o.key_groups : std::max(1, std::min(4, kMaxConsumerWarps / NT));
+  if (ns_max < 1) return PD_EINVAL;
+  // two warp groups with >= 2 stages each keep a group's next stage loading
+  // while it computes on the current one
+  int KG = o.key_groups > 0 ? o.key_groups : std::max(1, std::min(2, kMaxConsumerWarps / NT));
   int NS = 0;
   while (true) {
     NS = o.stages > 0 ? o.stages : (ns_max / KG) * KG;
@@ -400,6 +403,7 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   p.CS = plan.cluster;
   p.max_parts = std::max(plan.max_parts, 1);
   p.status = dev.status;
+  p.epi_floats = epilogue_bytes(head_size, plan.n_tiles, plan.stages) / 4;
   if (plan.max_parts > 0) {
     char *base = static_cast<char *>(scratch->data);
     const int64_t cbytes = (scratch->counter_slots * 4 + 255) / 256 * 256;

@@ -14,6 +14,7 @@ constexpr int kMaxRowGroups = 8;      // counters reserved per (sequence, kv hea
 constexpr int kMaxConsumerWarps = 8;  // warps that compute; one more loads
 constexpr int kMaxThreads = 32 * (kMaxConsumerWarps + 1);
 constexpr int kSmemAlign = 1024;      // the 128-byte TMA swizzle repeats every 1 KiB
+constexpr int kBlockIds = 512;        // page ids of 16-key blocks staged in shared memory
 
 // Everything a launch needs besides the two tensor maps.
 struct Params {
@@ -42,6 +43,7 @@ struct Params {
   float *part_ml;    // [S][Hkv][rg][max_parts][NT*8][2]
   int *counters;     // [S][Hkv][rg]
   unsigned int *status;
+  int64_t epi_floats;  // floats of the epilogue region (dead ring + Q tile)
 };
 
 struct Launch {
@@ -51,9 +53,10 @@ struct Launch {
   int cluster;
 };
 
-// Dynamic shared memory of a launch: ring + Q tile + barriers + flags.
+// Dynamic shared memory of a launch: ring + Q tile + barriers + flags +
+// the staged page ids.
 inline int smem_bytes(int D, int NT, int NS) {
-  return kSmemAlign + NS * kStageBytes + NT * D * 16 + 2 * NS * 8 + 64;
+  return kSmemAlign + NS * kStageBytes + NT * D * 16 + 2 * NS * 8 + 16 + 4 * kBlockIds;
 }
 
 // Bytes of the epilogue region (the ring and the Q tile once they are dead).
@@ -64,9 +67,12 @@ inline int64_t epilogue_bytes(int D, int NT, int NS) {
 // Floats the epilogue needs: combine phase and final-merge phase.
 inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
   const int64_t nt8 = 8LL * NT;
-  const int64_t combine = KG * nt8 * D + 2LL * KG * nt8 + 2 * nt8 + nt8 * (D / CS) + 2 * nt8 +
-                          (int64_t)CS * nt8 + 16;
-  const int64_t final_merge = 2LL * ncl_max * nt8 + nt8 + 16;
+  // the cluster combine (CS > 1) adds a D/CS slice, its (m, l) and weights
+  const int64_t combine = KG * nt8 * D + 2LL * KG * nt8 + 2 * nt8 +
+                          (CS > 1 ? nt8 * (D / CS) + 2 * nt8 + (int64_t)CS * nt8 : 0) + 16;
+  // weights and sums of every part, then a chunk buffer of >= one row chunk
+  // of one part (rows * D/CS <= 16 floats per thread)
+  const int64_t final_merge = 2LL * ncl_max * nt8 + nt8 + 16 + 16LL * kMaxThreads + D;
   return combine > final_merge ? combine : final_merge;
 }
 

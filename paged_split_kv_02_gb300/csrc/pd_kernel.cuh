@@ -103,12 +103,30 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   uint64_t *full = reinterpret_cast<uint64_t *>(qs + NT * D * 16);
   uint64_t *empty = full + NS;
   volatile int *flags = reinterpret_cast<volatile int *>(empty + NS);  // [0] abort, [1] last
+  uint64_t *mbar_merge = reinterpret_cast<uint64_t *>(empty + NS) + 1;   // flags[2..3]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = blockIdx.y;
   const int seg = blockIdx.x % p.max_seg;
   const int hg = blockIdx.x / p.max_seg;
   const int h = hg / p.rg, grow = hg % p.rg;
+
+  // ---- speculative page ids ----------------------------------------------
+  // Without a window, segment `seg` starts at block seg * seg_blocks whenever
+  // the sequence fits the plan; the producer reads those block-table entries
+  // while seq_lens is still in flight.
+  constexpr int kSpec = 256;
+  int spec[kSpec / 32];
+  const int spec_b0 = seg * p.seg_blocks;
+  const int32_t *bt_row = p.block_table + (int64_t)s * p.bt_stride;
+  const int bt_blocks = p.bt_width * (p.P / kBlockKeys);
+  if (warp == p.NT * p.KG && p.window == 0) {
+#pragma unroll
+    for (int k = 0; k < kSpec / 32; ++k) {
+      const int i = lane + 32 * k, b = spec_b0 + i;
+      spec[k] = (i < p.seg_blocks && b < bt_blocks) ? __ldg(bt_row + b / (p.P / kBlockKeys)) : 0;
+    }
+  }
 
   // ---- key ranges --------------------------------------------------------
   int L = __ldg(p.seq_lens + s);
@@ -140,30 +158,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int my_nb = max(0, min(b_first + nb, my_b0 + sb) - my_b0);
   const int ntile = (my_nb + TB - 1) / TB;
 
-  // ---- set-up: barriers and the Q tile --------------------------------------
+  // ---- set-up: barriers (the Q tile is loaded by the consumers) ----------
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(full + i), 1);
       mbar_init(smem_u32(empty + i), NT);
     }
+    mbar_init(smem_u32(mbar_merge), 1);
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init();
-  }
-  {
-    const T *qbase = static_cast<const T *>(p.q);
-    for (int idx = tid; idx < NT8 * (D / 8); idx += blockDim.x) {
-      const int r = idx / (D / 8), c = idx % (D / 8);
-      const int rr = rr0 + r;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < p.rows_cta && rr < p.R) {
-        const int i = rr / p.G, j = rr % p.G;
-        v = __ldg(reinterpret_cast<const uint4 *>(qbase + (int64_t)(s * p.M + i) * p.q_s0 +
-                                                  (int64_t)(h * p.G + j) * p.q_s1 + c * 8));
-      }
-      const int tn = r >> 3, rw = r & 7, box = c >> 3, cc = c & 7;
-      *reinterpret_cast<uint4 *>(qs + (tn * NBOX + box) * 1024 + rw * 128 + ((cc ^ rw) << 4)) = v;
-    }
   }
   __syncthreads();
 
@@ -182,10 +186,34 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
     }
-    const int32_t *bt_row = p.block_table + (int64_t)s * p.bt_stride;
+    // Physical page of every 16-key block of the segment, read from the
+    // block table kBlockIds at a time ahead of the copies that need them, so
+    // no TMA issue waits on a dependent global load.
+    int *pids = const_cast<int *>(flags + 4);
+    int pid_base = 0;
+    const bool spec_ok = p.window == 0 && my_b0 == spec_b0;
+    auto load_pids = [&](int base) {
+      __syncwarp();
+      const int n = min(kBlockIds, my_nb - base);
+      int i0 = 0;
+      if (base == 0 && spec_ok) {
+#pragma unroll
+        for (int k = 0; k < kSpec / 32; ++k)
+          if (lane + 32 * k < n) pids[lane + 32 * k] = spec[k];
+        i0 = kSpec;
+      }
+      for (int i = i0 + lane; i < n; i += 32)
+        pids[i] = __ldg(bt_row + (my_b0 + base + i) / (p.P / kBlockKeys));
+      __syncwarp();
+    };
+    if (my_nb > 0) load_pids(0);
     int issued = 0;
     for (int j = 0; j < ntile; ++j) {
       const int slot = j % NS;
+      if (j * TB >= pid_base + kBlockIds) {
+        pid_base = j * TB;
+        load_pids(pid_base);
+      }
       if (j >= NS) {
         int ok = 1;
         if (lane == 0) ok = mbar_wait_bounded(smem_u32(empty + slot), ((j / NS) - 1) & 1);
@@ -207,10 +235,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const int rem = lane % (nbt * NBOX);
         const int b = rem / NBOX, box = rem % NBOX;
         const int key0 = (my_b0 + j * TB + b) * kBlockKeys;
-        const int page = key0 / p.P, tok = key0 % p.P;
-        int phys = __ldg(bt_row + page);
+        const int tok = key0 % p.P;
+        int phys = pids[j * TB + b - pid_base];
         if ((unsigned)phys >= (unsigned)p.num_pool_blocks) {
-          atomicOr(p.status, 0x2u);
+          atomicOr(p.status, 0x2u);  // a page id outside the pool: report, read page 0
           phys = 0;
         }
         const uint32_t dst =
@@ -241,6 +269,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         lo1 = p.window ? max(0, hi1 - p.window) : 0;
       }
     }
+    {
+      // the Q tile: packed rows of this CTA, 16-byte chunks, 128B-swizzled
+      const T *qbase = static_cast<const T *>(p.q);
+      for (int idx = tid; idx < NT8 * (D / 8); idx += NC * 32) {
+        const int r = idx / (D / 8), c = idx % (D / 8);
+        const int rr = rr0 + r;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < p.rows_cta && rr < p.R) {
+          const int i = rr / p.G, j = rr % p.G;
+          v = __ldg(reinterpret_cast<const uint4 *>(qbase + (int64_t)(s * p.M + i) * p.q_s0 +
+                                                    (int64_t)(h * p.G + j) * p.q_s1 + c * 8));
+        }
+        const int tn = r >> 3, rw = r & 7, box = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4 *>(qs + (tn * NBOX + box) * 1024 + rw * 128 + ((cc ^ rw) << 4)) = v;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
+    }
     const uint32_t qs_u32 = smem_u32(qs) + t_n * NBOX * 1024;
     uint32_t qf[Q_IN_REGS ? KS : 1][2];
     if constexpr (Q_IN_REGS) {
@@ -260,7 +305,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
     for (int j = g_k; j < ntile; j += KG) {
       const int slot = j % NS;
-      if (!mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1)) {
+      // one verdict for the warp, so no lane leaves the shuffles alone
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1))) {
         if (lane == 0) {
           flags[0] = 1;
           atomicOr(p.status, 0x1u);
@@ -492,80 +538,85 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     return;
   }
 
-  // ---- combine the segments of this cluster (cluster size 1: a copy) ----
+  // ---- combine the segments of this cluster ------------------------------
+  // cluster size 1: the CTA partial (cp, swizzled, full D) is the cluster's
   const int CS = p.CS;
   const int DS = D / CS;
   const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
-  float *clp = lfin + NT8;               // [NT8][DS] cluster partial slice
-  float *mcl = clp + NT8 * DS;           // [NT8]
-  float *lcl = mcl + NT8;                // [NT8]
-  float *wts = lcl + NT8;                // [CS][NT8]
-  if (CS > 1) cluster_sync();            // every CTA's partial is in its shared memory
-  for (int r = tid; r < NT8; r += blockDim.x) {
-    float mr[8];
-    float ms = -INFINITY;
-    for (int x = 0; x < CS; ++x) {
-      mr[x] = CS > 1 ? ld_dsmem_f32(mapa(smem_u32(mfin + r), x)) : mfin[r];
-      ms = fmaxf(ms, mr[x]);
+  float *clp = lfin + NT8;               // [NT8][DS] cluster partial slice (CS > 1)
+  float *mcl = CS > 1 ? clp + NT8 * DS : mfin;
+  float *lcl = CS > 1 ? mcl + NT8 : lfin;
+  if (CS > 1) {
+    float *wts = lcl + NT8;  // [CS][NT8]
+    cluster_sync();          // every CTA's partial is in its shared memory
+    for (int r = tid; r < NT8; r += blockDim.x) {
+      float mr[8];
+      float ms = -INFINITY;
+      for (int x = 0; x < CS; ++x) {
+        mr[x] = ld_dsmem_f32(mapa(smem_u32(mfin + r), x));
+        ms = fmaxf(ms, mr[x]);
+      }
+      const float mu = ms == -INFINITY ? 0.f : ms;
+      float lsum = 0.f;
+      for (int x = 0; x < CS; ++x) {
+        const float w = exp2_or_zero(mr[x], mu);
+        lsum += ld_dsmem_f32(mapa(smem_u32(lfin + r), x)) * w;
+        wts[x * NT8 + r] = w;
+      }
+      mcl[r] = ms;
+      lcl[r] = lsum;
     }
-    const float mu = ms == -INFINITY ? 0.f : ms;
-    float lsum = 0.f;
-    for (int x = 0; x < CS; ++x) {
-      const float w = exp2_or_zero(mr[x], mu);
-      const float lx = CS > 1 ? ld_dsmem_f32(mapa(smem_u32(lfin + r), x)) : lfin[r];
-      lsum += lx * w;
-      wts[x * NT8 + r] = w;
-    }
-    mcl[r] = ms;
-    lcl[r] = lsum;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < NT8 * (DS / 4); idx += blockDim.x) {
-    const int r = idx / (DS / 4), d = (int)rank * DS + (idx % (DS / 4)) * 4;
-    const uint32_t local = smem_u32(cp + r * D + psw(d, r));
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int x = 0; x < CS; ++x) {
-      const float w = wts[x * NT8 + r];
-      const float4 b = CS > 1 ? ld_dsmem_f32x4(mapa(local, x))
-                              : *reinterpret_cast<const float4 *>(cp + r * D + psw(d, r));
-      a.x += w * b.x;
-      a.y += w * b.y;
-      a.z += w * b.z;
-      a.w += w * b.w;
-    }
-    *reinterpret_cast<float4 *>(clp + r * DS + (d - (int)rank * DS)) = a;
-  }
-  if (CS > 1)
-    cluster_sync();  // no CTA reads another's shared memory after this
-  else
     __syncthreads();
+    for (int idx = tid; idx < NT8 * (DS / 4); idx += blockDim.x) {
+      const int r = idx / (DS / 4), d = (int)rank * DS + (idx % (DS / 4)) * 4;
+      const uint32_t local = smem_u32(cp + r * D + psw(d, r));
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int x = 0; x < CS; ++x) {
+        const float w = wts[x * NT8 + r];
+        const float4 b = ld_dsmem_f32x4(mapa(local, x));
+        a.x += w * b.x;
+        a.y += w * b.y;
+        a.z += w * b.z;
+        a.w += w * b.w;
+      }
+      *reinterpret_cast<float4 *>(clp + r * DS + (d - (int)rank * DS)) = a;
+    }
+    cluster_sync();  // no CTA reads another's shared memory after this
+  }
+  // element (r, d) of this CTA's slice of the cluster partial
+  auto part4 = [&](int r, int d4) -> float4 {
+    return CS > 1 ? *reinterpret_cast<const float4 *>(clp + r * DS + d4)
+                  : *reinterpret_cast<const float4 *>(cp + r * D + psw(d4, r));
+  };
 
   if (ncl == 1) {
     for (int idx = tid; idx < nrows * (DS / 8); idx += blockDim.x) {
       const int r = idx / (DS / 8), c8 = (idx % (DS / 8)) * 8;
       const float lr = lcl[r];
       const float inv = lr > 0.f ? 1.f / lr : 0.f;
-      const float *src = clp + r * DS + c8;
-      const float v[8] = {src[0] * inv, src[1] * inv, src[2] * inv, src[3] * inv,
-                          src[4] * inv, src[5] * inv, src[6] * inv, src[7] * inv};
+      const float4 a = part4(r, c8), b = part4(r, c8 + 4);
+      const float v[8] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv,
+                          b.x * inv, b.y * inv, b.z * inv, b.w * inv};
       store8<BF16>(out_row(r) + (int)rank * DS + c8, v);
     }
     return;
   }
 
   // ---- several clusters: publish this cluster's partial, count arrivals ----
+  // Global partials of a group: acc [max_parts][CS][NT8][DS] (each CTA's
+  // slice contiguous), (m, l) [max_parts][NT8].
   const int group = (s * p.Hkv + h) * p.rg + grow;
   const int64_t gbase = (int64_t)group * p.max_parts;
+  const int64_t slice_floats = (int64_t)NT8 * DS;
   {
-    float *pa = p.part_acc + (gbase + cl_id) * NT8 * D + (int)rank * DS;
+    float *pa = p.part_acc + ((gbase + cl_id) * CS + rank) * slice_floats;
     for (int idx = tid; idx < NT8 * (DS / 4); idx += blockDim.x) {
       const int r = idx / (DS / 4), d4 = (idx % (DS / 4)) * 4;
-      __stcg(reinterpret_cast<float4 *>(pa + (int64_t)r * D + d4),
-             *reinterpret_cast<const float4 *>(clp + r * DS + d4));
+      __stcg(reinterpret_cast<float4 *>(pa + (int64_t)r * DS + d4), part4(r, d4));
     }
     if (rank == 0) {
-      float *pm = p.part_ml + (gbase + cl_id) * NT8 * 2;
-      for (int r = tid; r < NT8; r += blockDim.x) __stcg(reinterpret_cast<float2 *>(pm) + r, make_float2(mcl[r], lcl[r]));
+      float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
+      for (int r = tid; r < NT8; r += blockDim.x) __stcg(pm + r, make_float2(mcl[r], lcl[r]));
     }
   }
   __threadfence();
@@ -579,7 +630,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (last) atomicExch(p.counters + group, 0);
     __threadfence();
     flags[1] = last;
-    for (int x = 1; x < CS; ++x) st_dsmem_u32(mapa(smem_u32((const void *)(flags + 1)), x), (uint32_t)last);
+    for (int x = 1; x < CS; ++x)
+      st_dsmem_u32(mapa(smem_u32((const void *)(flags + 1)), x), (uint32_t)last);
   }
   if (CS > 1)
     cluster_sync();
@@ -589,9 +641,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   __threadfence();
 
   // ---- the last cluster merges every cluster partial (its own slice) ----
-  float *pm_s = ep;                 // [ncl][NT8] max, then weights
-  float *pl_s = pm_s + ncl * NT8;   // [ncl][NT8] sums
-  float *lall = pl_s + ncl * NT8;   // [NT8]
+  // Weights from every part's (m, l); then, by row chunks that keep at most
+  // four float4 sums per thread, the parts' rows are pulled into shared
+  // memory with bulk copies (a chunk of parts in flight at once) and summed.
+  float *pm_s = ep;                // [ncl][NT8] max, then weights
+  float *pl_s = pm_s + ncl * NT8;  // [ncl][NT8] sums
+  float *lall = pl_s + ncl * NT8;  // [NT8]
+  float *buf = lall + NT8;         // [chunk][RC][DS]
   for (int idx = tid; idx < ncl * NT8; idx += blockDim.x) {
     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + gbase * NT8 * 2) + idx);
     pm_s[idx] = ml.x;
@@ -610,24 +666,65 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
     lall[r] = lsum;
   }
-  __syncthreads();
-  for (int idx = tid; idx < nrows * (DS / 4); idx += blockDim.x) {
-    const int r = idx / (DS / 4), d = (int)rank * DS + (idx % (DS / 4)) * 4;
-    const float *src = p.part_acc + gbase * NT8 * D + (int64_t)r * D + d;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int c = 0; c < ncl; ++c) {
-      const float w = pm_s[c * NT8 + r];
-      const float4 b = __ldcg(reinterpret_cast<const float4 *>(src + (int64_t)c * NT8 * D));
-      a.x += w * b.x;
-      a.y += w * b.y;
-      a.z += w * b.z;
-      a.w += w * b.w;
+  const int nthr = blockDim.x;
+  const int RC = max(1, min(nrows, (16 * nthr) / DS));  // rows per chunk: <= 4 float4 per thread
+  const int PC = max(1, min(ncl, (int)((p.epi_floats - (2 * ncl + 1) * NT8 - 16) / (RC * DS))));
+  const uint32_t mb = smem_u32(mbar_merge);
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int rc0 = 0; rc0 < nrows && ok; rc0 += RC) {
+    const int nr = min(RC, nrows - rc0);
+    const int nitems = nr * (DS / 4);
+    float4 a[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < ncl; p0 += PC) {
+      const int np = min(PC, ncl - p0);
+      __syncthreads();  // the weights are in place; the previous chunk is consumed
+      if (tid == 0) {
+        fence_proxy_async();
+        const uint32_t bytes = (uint32_t)(nr * DS * 4);
+        mbar_arrive_expect_tx(mb, bytes * np);
+        for (int c = 0; c < np; ++c)
+          bulk_load(smem_u32(buf + (int64_t)c * RC * DS),
+                    p.part_acc + ((gbase + p0 + c) * CS + rank) * slice_floats + (int64_t)rc0 * DS,
+                    bytes, mb);
+      }
+      // one verdict for the whole CTA, so no thread leaves a barrier alone
+      if (!__syncthreads_and(mbar_wait_bounded(mb, phase))) {
+        if (tid == 0) atomicOr(p.status, 0x1u);
+        ok = false;
+        break;
+      }
+      phase ^= 1;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int it = tid + k * nthr;
+        if (it < nitems) {
+          const int rl = it / (DS / 4), d4 = (it % (DS / 4)) * 4;
+          for (int c = 0; c < np; ++c) {
+            const float w = pm_s[(p0 + c) * NT8 + rc0 + rl];
+            const float4 b = *reinterpret_cast<const float4 *>(buf + ((int64_t)c * RC + rl) * DS + d4);
+            a[k].x += w * b.x;
+            a[k].y += w * b.y;
+            a[k].z += w * b.z;
+            a[k].w += w * b.w;
+          }
+        }
+      }
     }
-    const float lr = lall[r];
-    const float inv = lr > 0.f ? 1.f / lr : 0.f;
-    const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
-    store4<BF16>(out_row(r) + d, v);
+    if (!ok) break;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int it = tid + k * nthr;
+      if (it < nitems) {
+        const int rl = it / (DS / 4), d4 = (it % (DS / 4)) * 4;
+        const float lr = lall[rc0 + rl];
+        const float inv = lr > 0.f ? 1.f / lr : 0.f;
+        const float v[4] = {a[k].x * inv, a[k].y * inv, a[k].z * inv, a[k].w * inv};
+        store4<BF16>(out_row(rc0 + rl) + (int)rank * DS + d4, v);
+      }
+    }
   }
 }
 

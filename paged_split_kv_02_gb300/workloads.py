@@ -163,6 +163,7 @@ def make_case(
     packed: bool = False,
     poison: bool = True,
     device: str = "cpu",
+    gen_device: str = "cpu",
 ) -> DecodeCase:
     """Build one call's inputs.
 
@@ -171,7 +172,9 @@ def make_case(
     mapped to a random permutation of the pool.  ``window_pages_only`` keeps
     only the pages a sliding window reaches in the block table; entries
     before the window's first page point at a NaN page, as in a block table
-    that holds only the blocks the window reaches.
+    that holds only the blocks the window reaches.  ``gen_device="cuda"``
+    draws q, K and V with a seeded CUDA generator (fast for large pools;
+    other values than the CPU streams of the same seed).
     """
     D, P = head_size, page_size
     S, M = len(seq_lens), max_query_len
@@ -221,19 +224,19 @@ def make_case(
         k_cache = torch.full(shape_pool, fill, dtype=dtype, device=device)
         v_cache = torch.full(shape_pool, fill, dtype=dtype, device=device)
 
-    g_q, g_k, g_v = _gen(seed, _STREAM_Q), _gen(seed, _STREAM_K), _gen(seed, _STREAM_V)
-    q = _rounded_normal((S * M, num_q_heads, D), std, 0.0, dtype, g_q)
+    g_q, g_k, g_v = (_gen(seed, st, gen_device) for st in (_STREAM_Q, _STREAM_K, _STREAM_V))
+    q = _rounded_normal((S * M, num_q_heads, D), std, 0.0, dtype, g_q, gen_device)
     for s in range(S):
         L = lens[s]
         lo_pos = first_page[s] * P
         n = L - lo_pos
         if n <= 0:
             continue
-        kvals = _rounded_normal((n, num_kv_heads, D), std, 0.0, dtype, g_k)
-        vvals = _rounded_normal((n, num_kv_heads, D), std, v_mean, dtype, g_v)
+        kvals = _rounded_normal((n, num_kv_heads, D), std, 0.0, dtype, g_k, gen_device)
+        vvals = _rounded_normal((n, num_kv_heads, D), std, v_mean, dtype, g_v, gen_device)
         pos = torch.arange(lo_pos, L)
-        phys = block_table[s, (pos // P)].long()
-        tok = (pos % P).long()
+        phys = block_table[s, (pos // P)].long().to(device)
+        tok = (pos % P).long().to(device)
         if layout == NHD:
             k_cache[phys, tok] = kvals.to(device)
             v_cache[phys, tok] = vvals.to(device)
@@ -280,13 +283,14 @@ def single_seq_nhd(seed: int = 0, device: str = "cpu") -> DecodeCase:
     )
 
 
-def spec_decode_hnd(M: int, L: int, seed: int = 0, device: str = "cpu") -> DecodeCase:
+def spec_decode_hnd(M: int, L: int, seed: int = 0, device: str = "cpu",
+                    gen_device: str = "cpu") -> DecodeCase:
     """bf16, D=128, 32 q / 8 kv heads, P=16, HND, batch 1, M in 1..4."""
     return make_case(
         f"spec_decode_hnd_bf16_d128_M{M}_L{L}",
         seed=seed, dtype=torch.bfloat16, head_size=128, num_q_heads=32,
         num_kv_heads=8, page_size=16, max_query_len=M, seq_lens=[L],
-        layout=HND, device=device,
+        layout=HND, device=device, gen_device=gen_device,
     )
 
 
@@ -303,13 +307,14 @@ def sliding_window(dtype: torch.dtype, M: int, L: int, seed: int = 0,
     )
 
 
-def wide_head(M: int, L: int, seed: int = 0, device: str = "cpu") -> DecodeCase:
+def wide_head(M: int, L: int, seed: int = 0, device: str = "cpu",
+              gen_device: str = "cpu") -> DecodeCase:
     """fp16, D=512, 8 q / 1 kv head, full causal, P=16, values N(0, 0.5)."""
     return make_case(
         f"wide_head_fp16_d512_M{M}_L{L}",
         seed=seed, dtype=torch.float16, head_size=512, num_q_heads=8,
         num_kv_heads=1, page_size=16, max_query_len=M, seq_lens=[L],
-        layout=HND, std=0.5, device=device,
+        layout=HND, std=0.5, device=device, gen_device=gen_device,
     )
 
 
