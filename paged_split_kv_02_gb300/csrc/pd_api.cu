@@ -8,7 +8,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/paged_decode.h"
+#include "paged_decode.h"
 #include "pd_internal.h"
 
 namespace pd {
@@ -88,8 +88,13 @@ MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 std::mutex g_map_mu;
 
-// Box: 64 head-dim elements (128 bytes, one swizzle row) x 16 tokens of one
-// kv head of one page.
+// One copy moves one 16-token block of one kv head of one page, all D dims:
+// dims (innermost first) = d within a 128-byte row (64), token, 128-byte row
+// of the head dim (D/64, stride 128 B), kv head, page.  The copy lands as
+// [D/64][16 tokens][128 B] with the 128-byte swizzle, the layout the
+// consumers' ldmatrix reads.  A TMA copy has a fixed per-copy cost (2 KiB
+// boxes stream at ~33 GB/s per SM on GB300); one copy per block is 32*D
+// bytes (4 KiB at D = 128, 16 KiB at D = 512).
 int encode_cache_map(const pd_tensor *t, int layout, CUtensorMap *out) {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
@@ -104,39 +109,30 @@ int encode_cache_map(const pd_tensor *t, int layout, CUtensorMap *out) {
   if (!g_encode) return PD_ECUDA;
   int dev = 0;
   cudaGetDevice(&dev);
-  // logical dims (innermost first): d, then the two middle dims, then block
+  // NHD [NB, P, Hkv, D]; HND [NB, Hkv, P, D]
+  const int ti = layout == PD_NHD ? 1 : 2, hi = layout == PD_NHD ? 2 : 1;
   MapKey key{};
   key.ptr = t->data;
   key.layout = layout;
-  // tensor shape: NHD [NB, P, Hkv, D]; HND [NB, Hkv, P, D]
-  key.dims[0] = t->shape[3];
-  key.dims[1] = t->shape[2];
-  key.dims[2] = t->shape[1];
-  key.dims[3] = t->shape[0];
-  key.strides[0] = t->stride[2];
-  key.strides[1] = t->stride[1];
-  key.strides[2] = t->stride[0];
+  for (int i = 0; i < 4; ++i) key.dims[i] = t->shape[i];
+  for (int i = 0; i < 3; ++i) key.strides[i] = t->stride[i];
   std::lock_guard<std::mutex> lock(g_map_mu);
   for (auto &e : g_maps)
     if (e.dev == dev && e.key == key) {
       *out = e.map;
       return PD_OK;
     }
-  cuuint64_t dims[4];
-  cuuint64_t strides[3];
-  for (int i = 0; i < 4; ++i) dims[i] = (cuuint64_t)key.dims[i];
-  for (int i = 0; i < 3; ++i) strides[i] = (cuuint64_t)key.strides[i] * 2;  // bytes
-  cuuint32_t box[4] = {64, 1, 1, 1};
-  // the token dim is dims[1] for HND ([.., P, D]) and dims[2] for NHD
-  if (layout == PD_HND)
-    box[1] = kBlockKeys;
-  else
-    box[2] = kBlockKeys;
-  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const int64_t D = t->shape[3];
+  cuuint64_t dims[5] = {64, (cuuint64_t)t->shape[ti], (cuuint64_t)(D / 64),
+                        (cuuint64_t)t->shape[hi], (cuuint64_t)t->shape[0]};
+  cuuint64_t strides[4] = {(cuuint64_t)t->stride[ti] * 2, 128, (cuuint64_t)t->stride[hi] * 2,
+                           (cuuint64_t)t->stride[0] * 2};  // bytes
+  cuuint32_t box[5] = {64, (cuuint32_t)kBlockKeys, (cuuint32_t)(D / 64), 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUtensorMap m;
-  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, t->data, dims, strides, box, estr,
+  CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, t->data, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return PD_EALIGN;
   MapEntry &e = g_maps[g_map_next];
   g_map_next = (g_map_next + 1) % kMapCache;
@@ -204,9 +200,10 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   const int fixed = smem_bytes(D, NT, 0);
   const int ns_max = std::min(8, (kSmemLimit - fixed - 16 * 8) / kStageBytes);
   if (ns_max < 1) return PD_EINVAL;
-  // two warp groups with >= 2 stages each keep a group's next stage loading
-  // while it computes on the current one
-  int KG = o.key_groups > 0 ? o.key_groups : std::max(1, std::min(2, kMaxConsumerWarps / NT));
+  // warp groups take alternate stages; with >= 2 stages each, a group's next
+  // stage loads while it computes on the current one (3 groups measured
+  // fastest for up to 16 packed rows)
+  int KG = o.key_groups > 0 ? o.key_groups : (NT <= 2 ? 3 : std::max(1, kMaxConsumerWarps / NT));
   int NS = 0;
   while (true) {
     NS = o.stages > 0 ? o.stages : (ns_max / KG) * KG;

@@ -230,22 +230,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       const int nbt = min(TB, my_nb - j * TB);
       if (lane == 0) mbar_arrive_expect_tx(smem_u32(full + slot), nbt * 2 * BLOCK_BYTES);
       __syncwarp();
-      if (lane < nbt * NBOX * 2) {
-        const int kv = lane / (nbt * NBOX);
-        const int rem = lane % (nbt * NBOX);
-        const int b = rem / NBOX, box = rem % NBOX;
+      if (lane < 2 * nbt) {
+        // one copy per 16-key block of K or V (all D/64 swizzle rows at once)
+        const int kv = lane / nbt, b = lane % nbt;
         const int key0 = (my_b0 + j * TB + b) * kBlockKeys;
-        const int tok = key0 % p.P;
         int phys = pids[j * TB + b - pid_base];
         if ((unsigned)phys >= (unsigned)p.num_pool_blocks) {
           atomicOr(p.status, 0x2u);  // a page id outside the pool: report, read page 0
           phys = 0;
         }
         const uint32_t dst =
-            smem_u32(ring + slot * kStageBytes + kv * (TB * BLOCK_BYTES) + (b * NBOX + box) * 2048);
-        const int c1 = p.layout == 1 ? tok : h;
-        const int c2 = p.layout == 1 ? h : tok;
-        tma_load_4d(dst, kv ? &tmV : &tmK, smem_u32(full + slot), box * 64, c1, c2, phys, pol);
+            smem_u32(ring + slot * kStageBytes + kv * (TB * BLOCK_BYTES) + b * BLOCK_BYTES);
+        tma_load_5d(dst, kv ? &tmV : &tmK, smem_u32(full + slot), 0, key0 % p.P, 0, h, phys, pol);
       }
       issued = j + 1;
     }
@@ -604,31 +600,33 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   // ---- several clusters: publish this cluster's partial, count arrivals ----
   // Global partials of a group: acc [max_parts][CS][NT8][DS] (each CTA's
-  // slice contiguous), (m, l) [max_parts][NT8].
+  // slice contiguous, valid rows only), (m, l) [max_parts][NT8].
   const int group = (s * p.Hkv + h) * p.rg + grow;
   const int64_t gbase = (int64_t)group * p.max_parts;
   const int64_t slice_floats = (int64_t)NT8 * DS;
   {
     float *pa = p.part_acc + ((gbase + cl_id) * CS + rank) * slice_floats;
-    for (int idx = tid; idx < NT8 * (DS / 4); idx += blockDim.x) {
+    for (int idx = tid; idx < nrows * (DS / 4); idx += blockDim.x) {
       const int r = idx / (DS / 4), d4 = (idx % (DS / 4)) * 4;
       __stcg(reinterpret_cast<float4 *>(pa + (int64_t)r * DS + d4), part4(r, d4));
     }
     if (rank == 0) {
       float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
-      for (int r = tid; r < NT8; r += blockDim.x) __stcg(pm + r, make_float2(mcl[r], lcl[r]));
+      for (int r = tid; r < nrows; r += blockDim.x) __stcg(pm + r, make_float2(mcl[r], lcl[r]));
     }
   }
-  __threadfence();
+  // The barrier orders every thread's stores before thread 0's release
+  // (acq_rel) increment of the counter; the last arriver's acquire then
+  // orders every cluster's partial before its reads (the split-K semaphore
+  // pattern: stores, barrier, one release by one thread).
   if (CS > 1)
     cluster_sync();
   else
     __syncthreads();
   if (rank == 0 && tid == 0) {
-    const int old = atomicAdd(p.counters + group, 1);
+    const int old = atomic_add_acq_rel_gpu(p.counters + group, 1);
     const int last = old == ncl - 1;
     if (last) atomicExch(p.counters + group, 0);
-    __threadfence();
     flags[1] = last;
     for (int x = 1; x < CS; ++x)
       st_dsmem_u32(mapa(smem_u32((const void *)(flags + 1)), x), (uint32_t)last);
@@ -638,23 +636,40 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   else
     __syncthreads();
   if (!flags[1]) return;
-  __threadfence();
 
   // ---- the last cluster merges every cluster partial (its own slice) ----
-  // Weights from every part's (m, l); then, by row chunks that keep at most
-  // four float4 sums per thread, the parts' rows are pulled into shared
-  // memory with bulk copies (a chunk of parts in flight at once) and summed.
+  // By row chunks that keep at most four float4 sums per thread, the parts'
+  // rows are pulled into shared memory with bulk copies (a chunk of parts in
+  // flight at once); the first chunk is requested before the parts' (m, l)
+  // are read, so both round trips overlap.
   float *pm_s = ep;                // [ncl][NT8] max, then weights
   float *pl_s = pm_s + ncl * NT8;  // [ncl][NT8] sums
   float *lall = pl_s + ncl * NT8;  // [NT8]
   float *buf = lall + NT8;         // [chunk][RC][DS]
+  const int nthr = blockDim.x;
+  const int RC = max(1, min(nrows, (16 * nthr) / DS));  // rows per chunk: <= 4 float4 per thread
+  const int PC = max(1, min(ncl, (int)((p.epi_floats - (2 * ncl + 1) * NT8 - 16) / (RC * DS))));
+  const uint32_t mb = smem_u32(mbar_merge);
+  auto request = [&](int rc0, int p0) {
+    if (tid == 0) {
+      const int nr = min(RC, nrows - rc0), np = min(PC, ncl - p0);
+      fence_proxy_async();
+      const uint32_t bytes = (uint32_t)(nr * DS * 4);
+      mbar_arrive_expect_tx(mb, bytes * np);
+      for (int c = 0; c < np; ++c)
+        bulk_load(smem_u32(buf + (int64_t)c * RC * DS),
+                  p.part_acc + ((gbase + p0 + c) * CS + rank) * slice_floats + (int64_t)rc0 * DS,
+                  bytes, mb);
+    }
+  };
+  if (nrows > 0) request(0, 0);
   for (int idx = tid; idx < ncl * NT8; idx += blockDim.x) {
     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + gbase * NT8 * 2) + idx);
     pm_s[idx] = ml.x;
     pl_s[idx] = ml.y;
   }
   __syncthreads();
-  for (int r = tid; r < NT8; r += blockDim.x) {
+  for (int r = tid; r < nrows; r += blockDim.x) {
     float ms = -INFINITY;
     for (int c = 0; c < ncl; ++c) ms = fmaxf(ms, pm_s[c * NT8 + r]);
     const float mu = ms == -INFINITY ? 0.f : ms;
@@ -666,12 +681,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
     lall[r] = lsum;
   }
-  const int nthr = blockDim.x;
-  const int RC = max(1, min(nrows, (16 * nthr) / DS));  // rows per chunk: <= 4 float4 per thread
-  const int PC = max(1, min(ncl, (int)((p.epi_floats - (2 * ncl + 1) * NT8 - 16) / (RC * DS))));
-  const uint32_t mb = smem_u32(mbar_merge);
   uint32_t phase = 0;
-  bool ok = true;
+  bool ok = true, first = true;
   for (int rc0 = 0; rc0 < nrows && ok; rc0 += RC) {
     const int nr = min(RC, nrows - rc0);
     const int nitems = nr * (DS / 4);
@@ -681,15 +692,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     for (int p0 = 0; p0 < ncl; p0 += PC) {
       const int np = min(PC, ncl - p0);
       __syncthreads();  // the weights are in place; the previous chunk is consumed
-      if (tid == 0) {
-        fence_proxy_async();
-        const uint32_t bytes = (uint32_t)(nr * DS * 4);
-        mbar_arrive_expect_tx(mb, bytes * np);
-        for (int c = 0; c < np; ++c)
-          bulk_load(smem_u32(buf + (int64_t)c * RC * DS),
-                    p.part_acc + ((gbase + p0 + c) * CS + rank) * slice_floats + (int64_t)rc0 * DS,
-                    bytes, mb);
-      }
+      if (!first) request(rc0, p0);
+      first = false;
       // one verdict for the whole CTA, so no thread leaves a barrier alone
       if (!__syncthreads_and(mbar_wait_bounded(mb, phase))) {
         if (tid == 0) atomicOr(p.status, 0x1u);
