@@ -177,6 +177,37 @@ PD_API int paged_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, in
                       int num_sms, const pd_scratch *scratch, const pd_options *opts,
                       pd_plan *plan);
 
+/* Size of the scratch array compiled into the library for
+ * paged_decode_attn_static, and the part of it kept for counters. */
+#define PD_STATIC_SCRATCH_BYTES (16u << 20)
+#define PD_STATIC_COUNTER_BYTES (256u << 10)
+
+/* The decode call without caller scratch.  Not from the paper: it has no
+ * counterpart there.  For callers that cannot allocate device memory (a host
+ * framework that owns all device allocation, a runtime that forbids
+ * allocation after start-up, an integration that only hands over inputs and
+ * outputs), the split-KV scratch is a fixed array of
+ * PD_STATIC_SCRATCH_BYTES inside the library, present on every GPU that
+ * loads the library until the process exits.  Arguments, layouts and
+ * results are those of paged_decode_attn; the split is fitted to the array,
+ * so long or large calls may use fewer segments than with a larger caller
+ * buffer.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Each call clears its counters with cudaMemsetAsync on `stream` and
+ *     allocates nothing (no cudaMalloc, no cudaFree, no allocating library).
+ *   - Every call shares the one array: calls that overlap on the GPU (on two
+ *     streams, or two host threads) race on it.  Serialise them.
+ *   - A call whose sequences x kv heads need more than
+ *     PD_STATIC_COUNTER_BYTES of counters (8 int32 per pair, i.e. more than
+ *     8192 pairs) returns PD_ESCRATCH. */
+PD_API int paged_decode_attn_static(const pd_tensor *q, const pd_tensor *k_cache,
+                                    const pd_tensor *v_cache, const pd_tensor *block_table,
+                                    const pd_tensor *seq_lens, pd_tensor *out, int num_q_heads,
+                                    int num_kv_heads, int head_size, int page_size,
+                                    int max_query_len, int window, float scale, int layout,
+                                    void *stream);
+
 /* Read the device status word (PD_DEV_* bits) of the current device after
  * synchronising `stream`; reset it to 0 when `reset` is non-zero. */
 PD_API int paged_decode_device_status(unsigned int *status, int reset, void *stream);

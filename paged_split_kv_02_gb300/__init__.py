@@ -110,6 +110,8 @@ def lib():
         L.paged_decode_attn.restype = i32
         L.paged_decode_attn_opts.argtypes = attn_args + [ctypes.POINTER(PdOptions)]
         L.paged_decode_attn_opts.restype = i32
+        L.paged_decode_attn_static.argtypes = attn_args[:14] + [vp]
+        L.paged_decode_attn_static.restype = i32
         L.paged_decode_plan.argtypes = [i32] * 9 + [ctypes.POINTER(PdScratch),
                                                     ctypes.POINTER(PdOptions),
                                                     ctypes.POINTER(PdPlan)]
@@ -219,6 +221,24 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, out, num_q_hea
         rc = L.paged_decode_attn_opts(*args, ctypes.byref(opts))
     if check and rc != PD_OK:
         raise PagedDecodeError(rc, "paged_decode_attn")
+    return rc
+
+
+def paged_decode_attn_static(q, k_cache, v_cache, block_table, seq_lens, out, num_q_heads,
+                             num_kv_heads, head_size, page_size, max_query_len, window, scale,
+                             layout, stream=None, check: bool = True) -> int:
+    """The decode call with the library's own fixed scratch array, for
+    callers that cannot allocate device memory (see the C header).  Calls
+    share that array, so do not overlap them on the GPU; make the first call
+    on a device before any stream capture."""
+    L = lib()
+    descs = [tensor_desc(t) for t in (q, k_cache, v_cache, block_table, seq_lens, out)]
+    rc = L.paged_decode_attn_static(*[ctypes.byref(d) for d in descs], int(num_q_heads),
+                                    int(num_kv_heads), int(head_size), int(page_size),
+                                    int(max_query_len), int(window), float(scale), int(layout),
+                                    _stream_handle(stream))
+    if check and rc != PD_OK:
+        raise PagedDecodeError(rc, "paged_decode_attn_static")
     return rc
 
 
