@@ -148,6 +148,9 @@ typedef struct pd_options {
   int cluster;       /* thread-block cluster size of the merge (1, 2, 4, 8)   */
   int path;          /* 0 = auto, 1 = tensor-core (mma.sync), 2 = warp dot     */
   int max_ctas_hint; /* CTAs the split aims for (0 = the SM count)            */
+  int merge;         /* split-KV merge: 0 = auto, 1 = the last-arriving CTA,
+                        2 = the last K arrivals of a co-resident (cooperative)
+                        grid, one D/K slice each                                */
 } pd_options;
 
 /* paged_decode_attn with explicit knobs (opts may be NULL). */
@@ -161,6 +164,8 @@ PD_API int paged_decode_attn_opts(const pd_tensor *q, const pd_tensor *k_cache, 
  * device access), for inspection and tests. */
 typedef struct pd_plan {
   int path;          /* 1 = mma, 2 = dot                                       */
+  int merge;         /* 0 = none, 1 = last arriver, 2 = cooperative mergers    */
+  int mergers;       /* K of the cooperative merge                             */
   int rows;          /* packed rows per kv head, G * M                         */
   int row_groups, rows_per_cta, n_tiles, key_groups, stages;
   int seg_blocks;    /* 16-key blocks per segment                              */

@@ -60,12 +60,12 @@ class PdScratch(ctypes.Structure):
 class PdOptions(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("segments", "row_groups", "key_groups", "stages", "cluster", "path",
-                 "max_ctas_hint")]
+                 "max_ctas_hint", "merge")]
 
 
 class PdPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
-                ("path", "rows", "row_groups", "rows_per_cta", "n_tiles", "key_groups", "stages",
+                ("path", "merge", "mergers", "rows", "row_groups", "rows_per_cta", "n_tiles", "key_groups", "stages",
                  "seg_blocks", "max_segments", "cluster", "max_parts", "grid_x", "grid_y",
                  "block_threads", "smem_bytes")] + [("scratch_needed", ctypes.c_int64)]
 

@@ -255,7 +255,7 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   int64_t max_parts = nseg > CS ? nseg / CS : 0;  // partial slots per group (0: none)
 
   // Scratch: counters for every group, partials for every cluster.
-  const int64_t counter_need = units;
+  const int64_t counter_need = 2 * units;  // arrivals and finished mergers per group
   auto partial_bytes = [&](int64_t parts) -> int64_t {
     const int64_t acc = ((units * parts * part_floats * 4) + 255) / 256 * 256;
     const int64_t ml = ((units * parts * 8LL * NT * 2 * 4) + 255) / 256 * 256;
@@ -303,9 +303,30 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   }
   if (epilogue_floats(D, NT, KG, CS, 1) * 4 > epilogue_bytes(D, NT, NS)) return PD_EINVAL;
   const int64_t seg_blocks = cdiv(nb_max, nseg);
+  // Merge.  A grid that fits on the GPU at once (one CTA per SM) can be
+  // launched cooperatively; then the last K arrivals of a group each merge
+  // one D/K slice instead of the last arrival merging all of it alone.
+  if (o.merge < 0 || o.merge > 2) return PD_EINVAL;
+  const int64_t nt8 = 8LL * NT;
+  // a merger's shared memory: (m, l) of every part, and its share of every
+  // part (K >= half the parts when there are <= 8)
+  const int64_t coop_floats = 2 * max_parts * nt8 + nt8 + 64 +
+                              std::max<int64_t>(2 * nt8 * D, cdiv(max_parts * nt8 * D, 8));
+  const bool coop_ok = max_parts > 1 && CS == 1 && (int64_t)S * Hkv * rg * nseg <= num_sms &&
+                       coop_floats * 4 <= epilogue_bytes(D, NT, NS);
+  int merge = max_parts > 1 ? 1 : 0, mergers = 0;
+  if (coop_ok && o.merge != 1) {
+    merge = 2;
+    mergers = 1;  // a power of two <= min(8, parts): D / mergers stays a multiple of 8
+    while (2 * mergers <= std::min<int64_t>(8, max_parts)) mergers *= 2;
+  } else if (o.merge == 2 && max_parts > 1) {
+    return PD_EINVAL;  // the grid does not fit at once, or a cluster was asked for
+  }
   if ((int64_t)Hkv * rg * nseg > INT32_MAX || S > 65535) return PD_EINVAL;
 
   plan->path = 1;
+  plan->merge = merge;
+  plan->mergers = mergers;
   plan->rows = R;
   plan->row_groups = rg;
   plan->rows_per_cta = rows_cta;
@@ -400,6 +421,8 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   p.CS = plan.cluster;
   p.max_parts = std::max(plan.max_parts, 1);
   p.status = dev.status;
+  p.coop = plan.merge == 2 ? 1 : 0;
+  p.mergers = plan.mergers > 0 ? plan.mergers : 1;
   p.epi_floats = epilogue_bytes(head_size, plan.n_tiles, plan.stages) / 4;
   if (plan.max_parts > 0) {
     char *base = static_cast<char *>(scratch->data);
@@ -417,6 +440,7 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   l.block = dim3(plan.block_threads, 1, 1);
   l.smem = plan.smem_bytes;
   l.cluster = plan.cluster;
+  l.cooperative = plan.merge == 2 ? 1 : 0;
   cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, tk, tv, p, l,
                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {

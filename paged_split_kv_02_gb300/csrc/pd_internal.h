@@ -41,9 +41,11 @@ struct Params {
   int max_parts;     // partial slots per group, max_seg / CS
   float *part_acc;   // [S][Hkv][rg][max_parts][NT*8][D]
   float *part_ml;    // [S][Hkv][rg][max_parts][NT*8][2]
-  int *counters;     // [S][Hkv][rg]
+  int *counters;     // [S][Hkv][rg][2]: arrivals, finished mergers
   unsigned int *status;
   int64_t epi_floats;  // floats of the epilogue region (dead ring + Q tile)
+  int coop;            // 1: co-resident grid, the last `mergers` arrivals merge
+  int mergers;         // K_max of the cooperative merge (a power of two)
 };
 
 struct Launch {
@@ -51,6 +53,7 @@ struct Launch {
   dim3 block;
   int smem;
   int cluster;
+  int cooperative;
 };
 
 // Dynamic shared memory of a launch: ring + Q tile + barriers + flags +

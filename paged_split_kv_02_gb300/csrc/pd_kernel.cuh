@@ -604,12 +604,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int group = (s * p.Hkv + h) * p.rg + grow;
   const int64_t gbase = (int64_t)group * p.max_parts;
   const int64_t slice_floats = (int64_t)NT8 * DS;
-  {
+  if (p.coop) {
+    // layout [part][K_max][NT8][D/K_max]: a merger's slice is one block
+    const int DKm = D / p.mergers;
+    float *pa = p.part_acc + (gbase + cl_id) * (int64_t)NT8 * D;
+    for (int idx = tid; idx < nrows * (D / 4); idx += blockDim.x) {
+      const int r = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
+      const int k = d4 / DKm, dk = d4 % DKm;
+      __stcg(reinterpret_cast<float4 *>(pa + ((int64_t)k * NT8 + r) * DKm + dk), part4(r, d4));
+    }
+  } else {
     float *pa = p.part_acc + ((gbase + cl_id) * CS + rank) * slice_floats;
     for (int idx = tid; idx < nrows * (DS / 4); idx += blockDim.x) {
       const int r = idx / (DS / 4), d4 = (idx % (DS / 4)) * 4;
       __stcg(reinterpret_cast<float4 *>(pa + (int64_t)r * DS + d4), part4(r, d4));
     }
+  }
+  {
     if (rank == 0) {
       float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
       for (int r = tid; r < nrows; r += blockDim.x) __stcg(pm + r, make_float2(mcl[r], lcl[r]));
@@ -623,10 +634,106 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     cluster_sync();
   else
     __syncthreads();
+
+  if (p.coop) {
+    // ---- co-resident grid: the last K arrivals merge one D/K slice each ----
+    // Every CTA of a cooperative launch is resident, so a merger waiting for
+    // the remaining arrivals waits on CTAs that are running (bounded).
+    // K = the largest power of two <= min(K_max, arrivals of this group).
+    int K = 1;
+    while (2 * K <= min(p.mergers, ncl)) K *= 2;
+    if (tid == 0) flags[1] = atomic_add_acq_rel_gpu(p.counters + 2 * group, 1) - (ncl - K);
+    __syncthreads();
+    const int mi = flags[1];
+    if (mi < 0) return;  // not one of the last K arrivals
+    if (tid == 0) {
+      int ok = 1;
+      if (ld_acquire_gpu(p.counters + 2 * group) < ncl) {
+        const unsigned long long t0 = global_timer_ns();
+        while (ld_acquire_gpu(p.counters + 2 * group) < ncl) {
+          __nanosleep(64);
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            ok = 0;
+            atomicOr(p.status, 0x1u);
+            break;
+          }
+        }
+      }
+      flags[2] = ok;
+    }
+    __syncthreads();
+    if (!flags[2]) return;
+    // this merger's layout slices: [mi * q, (mi + 1) * q) of the K_max slices
+    const int DKm = D / p.mergers, q = p.mergers / K, DK = q * DKm;
+    const int64_t part_floats = (int64_t)NT8 * D;
+    const int slab = q * NT8 * DKm;  // floats of one part's share
+    float *w_s = ep;                 // [ncl][NT8] max, then weights
+    float *l_s = w_s + ncl * NT8;    // [ncl][NT8] sums; row r of part 0 then the merged sum
+    float *buf = l_s + ncl * NT8;    // [ncl][q][NT8][DKm]
+    const uint32_t mb = smem_u32(mbar_merge);
+    if (tid == 0) {
+      fence_proxy_async();
+      mbar_arrive_expect_tx(mb, (uint32_t)(ncl * slab * 4));
+      for (int c = 0; c < ncl; ++c)
+        bulk_load(smem_u32(buf + (int64_t)c * slab),
+                  p.part_acc + (gbase + c) * part_floats + (int64_t)mi * slab, (uint32_t)(slab * 4),
+                  mb);
+    }
+    for (int idx = tid; idx < ncl * NT8; idx += blockDim.x) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + gbase * NT8 * 2) + idx);
+      w_s[idx] = ml.x;
+      l_s[idx] = ml.y;
+    }
+    __syncthreads();
+    for (int r = tid; r < nrows; r += blockDim.x) {
+      float ms = -INFINITY;
+      for (int c = 0; c < ncl; ++c) ms = fmaxf(ms, w_s[c * NT8 + r]);
+      const float mu = ms == -INFINITY ? 0.f : ms;
+      float lsum = 0.f;
+      for (int c = 0; c < ncl; ++c) {
+        const float w = exp2_or_zero(w_s[c * NT8 + r], mu);
+        w_s[c * NT8 + r] = w;
+        lsum += l_s[c * NT8 + r] * w;
+      }
+      l_s[r] = lsum;
+    }
+    if (!__syncthreads_and(mbar_wait_bounded(mb, 0))) {
+      if (tid == 0) atomicOr(p.status, 0x1u);
+      return;
+    }
+    for (int idx = tid; idx < nrows * (DK / 4); idx += blockDim.x) {
+      const int r = idx / (DK / 4), dd = (idx % (DK / 4)) * 4;
+      const int kk = dd / DKm, dk = dd % DKm;
+      const float *src = buf + ((int64_t)kk * NT8 + r) * DKm + dk;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < ncl; ++c) {
+        const float w = w_s[c * NT8 + r];
+        const float4 b = *reinterpret_cast<const float4 *>(src + (int64_t)c * slab);
+        a.x += w * b.x;
+        a.y += w * b.y;
+        a.z += w * b.z;
+        a.w += w * b.w;
+      }
+      const float lr = l_s[r];
+      const float inv = lr > 0.f ? 1.f / lr : 0.f;
+      const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
+      store4<BF16>(out_row(r) + mi * DK + dd, v);
+    }
+    if (tid == 0) {
+      // the last merger to finish resets both counters: every merger has
+      // passed its wait by then and every arrival has been counted
+      if (atomicAdd(p.counters + 2 * group + 1, 1) == K - 1) {
+        atomicExch(p.counters + 2 * group, 0);
+        atomicExch(p.counters + 2 * group + 1, 0);
+      }
+    }
+    return;
+  }
+
   if (rank == 0 && tid == 0) {
-    const int old = atomic_add_acq_rel_gpu(p.counters + group, 1);
+    const int old = atomic_add_acq_rel_gpu(p.counters + 2 * group, 1);
     const int last = old == ncl - 1;
-    if (last) atomicExch(p.counters + group, 0);
+    if (last) atomicExch(p.counters + 2 * group, 0);
     flags[1] = last;
     for (int x = 1; x < CS; ++x)
       st_dsmem_u32(mapa(smem_u32((const void *)(flags + 1)), x), (uint32_t)last);
@@ -750,15 +857,22 @@ cudaError_t launch_mma_t(const CUtensorMap &tk, const CUtensorMap &tv, const Par
   cfg.blockDim = l.block;
   cfg.dynamicSmemBytes = l.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int na = 0;
   if (l.cluster > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = l.cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = l.cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  if (l.cooperative) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 

@@ -143,6 +143,12 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
   return old;
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int *addr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

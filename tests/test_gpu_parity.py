@@ -66,7 +66,38 @@ def test_forced_splits_agree(segments, cluster):
     out, _ = _parity(case, opts=pd.options(segments=segments, cluster=cluster))
 
 
-@pytest.mark.parametrize("kg,ns", [(1, 2), (1, 5), (2, 2), (2, 6), (4, 4)])
+@pytest.mark.parametrize("merge", [1, 2])
+@pytest.mark.parametrize("M,L,seg", [(1, 4096, 19), (4, 4096, 5), (4, 16384, 19), (2, 1024, 16),
+                                     (3, 2048, 3)])
+def test_merge_modes(merge, M, L, seg):
+    """Last-arriving CTA vs the last K arrivals of a cooperative grid."""
+    _parity(W.spec_decode_hnd(M, L, seed=14), opts=pd.options(segments=seg, merge=merge))
+
+
+def test_cooperative_merge_refused_when_grid_does_not_fit():
+    case = W.spec_decode_hnd(2, 1024, seed=15)
+    g = case.to("cuda")
+    rc = pd.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens,
+                              torch.empty_like(g.q), g.num_q_heads, g.num_kv_heads,
+                              g.head_size, g.page_size, g.max_query_len, g.window, g.scale,
+                              g.layout, scratch_for(case), opts=pd.options(segments=64, merge=2),
+                              check=False)
+    assert rc == -1
+
+
+@pytest.mark.parametrize("merge", [1, 2])
+def test_batched_uneven_segments(merge):
+    """A batch whose sequences split into different numbers of segments (some
+    fewer than the cooperative mergers, some unsplit, one empty)."""
+    case = W.make_case("uneven", seed=16, dtype=torch.bfloat16, head_size=128, num_q_heads=16,
+                       num_kv_heads=2, page_size=16, max_query_len=3,
+                       seq_lens=[3000, 200, 40, 0, 1, 1100, 600], layout=W.HND)
+    # 7 sequences x 2 kv heads x 10 segments = 140 CTAs: one wave, so the
+    # cooperative merge is allowed
+    _parity(case, opts=pd.options(segments=10, merge=merge))
+
+
+@pytest.mark.parametrize("kg,ns", [(1, 2), (1, 5), (2, 2), (2, 6), (3, 6), (4, 4)])
 def test_warp_groups_and_stages(kg, ns):
     _parity(W.spec_decode_hnd(2, 1024, seed=4), opts=pd.options(key_groups=kg, stages=ns))
 
