@@ -310,7 +310,7 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   const int64_t nt8 = 8LL * NT;
   // a merger's shared memory: (m, l) of every part, and its share of every
   // part (K >= half the parts when there are <= 8)
-  const int64_t coop_floats = 2 * max_parts * nt8 + nt8 + 64 +
+  const int64_t coop_floats = 3 * max_parts * nt8 + nt8 + 64 +
                               std::max<int64_t>(2 * nt8 * D, cdiv(max_parts * nt8 * D, 8));
   const bool coop_ok = max_parts > 1 && CS == 1 && (int64_t)S * Hkv * rg * nseg <= num_sms &&
                        coop_floats * 4 <= epilogue_bytes(D, NT, NS);

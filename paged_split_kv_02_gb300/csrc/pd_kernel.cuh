@@ -111,6 +111,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int hg = blockIdx.x / p.max_seg;
   const int h = hg / p.rg, grow = hg % p.rg;
 
+  // Launched with programmatic stream serialisation: wait here until the
+  // previous grid on the stream (which may have written q, the caches, the
+  // block table or the scratch) has completed, before reading any of them.
+  grid_dependency_wait();
+
   // ---- speculative page ids ----------------------------------------------
   // Without a window, segment `seg` starts at block seg * seg_blocks whenever
   // the sequence fits the plan; the producer reads those block-table entries
@@ -453,6 +458,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
 
   // ================= epilogue ==============================================
+  // The next grid on the stream may start launching now (its CTAs wait at
+  // their own grid_dependency_wait until this grid has completed).
+  grid_dependents_launch();
   __syncthreads();  // ring and Q tile are dead from here on
   float *ep = reinterpret_cast<float *>(smem);
   float *cp = ep;                          // [KG][NT8][D] (swizzled columns)
@@ -461,12 +469,97 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   float *mfin = lrow + KG * NT8;  // [NT8]
   float *lfin = mfin + NT8;
 
+  T *obase = static_cast<T *>(p.out);
+  auto out_row = [&](int r) -> T * {
+    const int rr = rr0 + r;
+    const int i = rr / p.G, j = rr % p.G;
+    return obase + (int64_t)(s * p.M + i) * p.o_s0 + (int64_t)(h * p.G + j) * p.o_s1;
+  };
+  const int nrows = max(0, rr1 - rr0);  // valid rows of this CTA
+
+  const int CS = p.CS;
+  const int DS = D / CS;
+  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
+  const int group = (s * p.Hkv + h) * p.rg + grow;
+  const int64_t gbase = (int64_t)group * p.max_parts;
+  const int64_t slice_floats = (int64_t)NT8 * DS;
+
   if (warp < NC && lane < 4) {
     mrow[g_k * NT8 + r0] = m0;
     mrow[g_k * NT8 + r1] = m1;
     lrow[g_k * NT8 + r0] = l0;
     lrow[g_k * NT8 + r1] = l1;
   }
+  if (CS == 1) {
+    // ---- no cluster: one pass over the warp groups' partials -------------
+    // Once every group's (m, l) is in shared memory, each warp scales its own
+    // rows by exp2(m_g - m*) as it stores them and the rows' (m*, L) are
+    // formed alongside; the pass that writes the output (one segment) or
+    // publishes the partial (several) then only sums the groups.
+    __syncthreads();
+    if (warp < NC) {
+      float ms0 = -INFINITY, ms1 = -INFINITY;
+      for (int gg = 0; gg < KG; ++gg) {
+        ms0 = fmaxf(ms0, mrow[gg * NT8 + r0]);
+        ms1 = fmaxf(ms1, mrow[gg * NT8 + r1]);
+      }
+      const float f0 = exp2_or_zero(m0, ms0 == -INFINITY ? 0.f : ms0);
+      const float f1 = exp2_or_zero(m1, ms1 == -INFINITY ? 0.f : ms1);
+      float *dst = cp + (size_t)g_k * NT8 * D;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int d = mt * 16 + (lane >> 2);
+        dst[r0 * D + psw(d, r0)] = acc[mt][0] * f0;
+        dst[r1 * D + psw(d, r1)] = acc[mt][1] * f1;
+        dst[r0 * D + psw(d + 8, r0)] = acc[mt][2] * f0;
+        dst[r1 * D + psw(d + 8, r1)] = acc[mt][3] * f1;
+      }
+    } else {
+      for (int r = lane + 32 * (warp - NC); r < NT8; r += 32 * (blockDim.x / 32 - NC)) {
+        float ms = -INFINITY;
+        for (int gg = 0; gg < KG; ++gg) ms = fmaxf(ms, mrow[gg * NT8 + r]);
+        const float mu = ms == -INFINITY ? 0.f : ms;
+        float lsum = 0.f;
+        for (int gg = 0; gg < KG; ++gg) lsum += lrow[gg * NT8 + r] * exp2_or_zero(mrow[gg * NT8 + r], mu);
+        mfin[r] = ms;
+        lfin[r] = lsum;
+      }
+    }
+    __syncthreads();
+    auto sum4 = [&](int r, int d4) -> float4 {
+      float4 a = *reinterpret_cast<const float4 *>(cp + (size_t)r * D + psw(d4, r));
+      for (int gg = 1; gg < KG; ++gg) {
+        const float4 b = *reinterpret_cast<const float4 *>(cp + ((size_t)gg * NT8 + r) * D + psw(d4, r));
+        a.x += b.x;
+        a.y += b.y;
+        a.z += b.z;
+        a.w += b.w;
+      }
+      return a;
+    };
+    if (nseg == 1) {
+      for (int idx = tid; idx < nrows * (D / 8); idx += blockDim.x) {
+        const int r = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
+        const float lr = lfin[r];
+        const float inv = lr > 0.f ? 1.f / lr : 0.f;
+        const float4 a = sum4(r, c8), b = sum4(r, c8 + 4);
+        const float v[8] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv,
+                            b.x * inv, b.y * inv, b.z * inv, b.w * inv};
+        store8<BF16>(out_row(r) + c8, v);
+      }
+      return;
+    }
+    // several segments: publish (in the layout of the merge that reads it)
+    const int DKm = p.coop ? D / p.mergers : D;
+    float *pa = p.part_acc + (gbase + cl_id) * (int64_t)NT8 * D;
+    for (int idx = tid; idx < nrows * (D / 4); idx += blockDim.x) {
+      const int r = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
+      const int k = d4 / DKm, dk = d4 % DKm;
+      __stcg(reinterpret_cast<float4 *>(pa + ((int64_t)k * NT8 + r) * DKm + dk), sum4(r, d4));
+    }
+    float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
+    for (int r = tid; r < nrows; r += blockDim.x) __stcg(pm + r, make_float2(mfin[r], lfin[r]));
+  } else {
   __syncthreads();
   if (warp < NC) {
     float ms0 = -INFINITY, ms1 = -INFINITY;
@@ -511,14 +604,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
   __syncthreads();
 
-  T *obase = static_cast<T *>(p.out);
-  auto out_row = [&](int r) -> T * {
-    const int rr = rr0 + r;
-    const int i = rr / p.G, j = rr % p.G;
-    return obase + (int64_t)(s * p.M + i) * p.o_s0 + (int64_t)(h * p.G + j) * p.o_s1;
-  };
-  const int nrows = max(0, rr1 - rr0);  // valid rows of this CTA
-
   if (nseg == 1) {
     // one segment: normalise and store
     for (int idx = tid; idx < nrows * (D / 8); idx += blockDim.x) {
@@ -536,9 +621,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   // ---- combine the segments of this cluster ------------------------------
   // cluster size 1: the CTA partial (cp, swizzled, full D) is the cluster's
-  const int CS = p.CS;
-  const int DS = D / CS;
-  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
   float *clp = lfin + NT8;               // [NT8][DS] cluster partial slice (CS > 1)
   float *mcl = CS > 1 ? clp + NT8 * DS : mfin;
   float *lcl = CS > 1 ? mcl + NT8 : lfin;
@@ -601,9 +683,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   // ---- several clusters: publish this cluster's partial, count arrivals ----
   // Global partials of a group: acc [max_parts][CS][NT8][DS] (each CTA's
   // slice contiguous, valid rows only), (m, l) [max_parts][NT8].
-  const int group = (s * p.Hkv + h) * p.rg + grow;
-  const int64_t gbase = (int64_t)group * p.max_parts;
-  const int64_t slice_floats = (int64_t)NT8 * DS;
   if (p.coop) {
     // layout [part][K_max][NT8][D/K_max]: a merger's slice is one block
     const int DKm = D / p.mergers;
@@ -625,6 +704,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
       for (int r = tid; r < nrows; r += blockDim.x) __stcg(pm + r, make_float2(mcl[r], lcl[r]));
     }
+  }
   }
   // The barrier orders every thread's stores before thread 0's release
   // (acq_rel) increment of the counter; the last arriver's acquire then
@@ -667,40 +747,44 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const int DKm = D / p.mergers, q = p.mergers / K, DK = q * DKm;
     const int64_t part_floats = (int64_t)NT8 * D;
     const int slab = q * NT8 * DKm;  // floats of one part's share
-    float *w_s = ep;                 // [ncl][NT8] max, then weights
-    float *l_s = w_s + ncl * NT8;    // [ncl][NT8] sums; row r of part 0 then the merged sum
-    float *buf = l_s + ncl * NT8;    // [ncl][q][NT8][DKm]
+    float *ml_s = ep;                   // [ncl][NT8][2] (m, l) of every part
+    float *w_s = ml_s + 2 * ncl * NT8;  // [ncl][NT8] weights
+    float *l_s = w_s + ncl * NT8;       // [NT8] merged sums
+    float *buf = l_s + NT8;             // [ncl][q][NT8][DKm]
     const uint32_t mb = smem_u32(mbar_merge);
     if (tid == 0) {
+      // one batch of bulk copies: every part's (m, l) and this merger's share
       fence_proxy_async();
-      mbar_arrive_expect_tx(mb, (uint32_t)(ncl * slab * 4));
+      const uint32_t ml_bytes = (uint32_t)(ncl * NT8 * 8);
+      mbar_arrive_expect_tx(mb, (uint32_t)(ncl * slab * 4) + ml_bytes);
+      bulk_load(smem_u32(ml_s), p.part_ml + gbase * NT8 * 2, ml_bytes, mb);
       for (int c = 0; c < ncl; ++c)
         bulk_load(smem_u32(buf + (int64_t)c * slab),
                   p.part_acc + (gbase + c) * part_floats + (int64_t)mi * slab, (uint32_t)(slab * 4),
                   mb);
     }
-    for (int idx = tid; idx < ncl * NT8; idx += blockDim.x) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + gbase * NT8 * 2) + idx);
-      w_s[idx] = ml.x;
-      l_s[idx] = ml.y;
-    }
-    __syncthreads();
-    for (int r = tid; r < nrows; r += blockDim.x) {
-      float ms = -INFINITY;
-      for (int c = 0; c < ncl; ++c) ms = fmaxf(ms, w_s[c * NT8 + r]);
-      const float mu = ms == -INFINITY ? 0.f : ms;
-      float lsum = 0.f;
-      for (int c = 0; c < ncl; ++c) {
-        const float w = exp2_or_zero(w_s[c * NT8 + r], mu);
-        w_s[c * NT8 + r] = w;
-        lsum += l_s[c * NT8 + r] * w;
-      }
-      l_s[r] = lsum;
-    }
     if (!__syncthreads_and(mbar_wait_bounded(mb, 0))) {
       if (tid == 0) atomicOr(p.status, 0x1u);
       return;
     }
+    // weights: one warp per row, one lane per part
+    for (int r = warp; r < nrows; r += blockDim.x >> 5) {
+      float ms = -INFINITY;
+      for (int c = lane; c < ncl; c += 32) ms = fmaxf(ms, ml_s[(c * NT8 + r) * 2]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, o));
+      const float mu = ms == -INFINITY ? 0.f : ms;
+      float lsum = 0.f;
+      for (int c = lane; c < ncl; c += 32) {
+        const float w = exp2_or_zero(ml_s[(c * NT8 + r) * 2], mu);
+        w_s[c * NT8 + r] = w;
+        lsum += ml_s[(c * NT8 + r) * 2 + 1] * w;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+      if (lane == 0) l_s[r] = lsum;
+    }
+    __syncthreads();
     for (int idx = tid; idx < nrows * (DK / 4); idx += blockDim.x) {
       const int r = idx / (DK / 4), dd = (idx % (DK / 4)) * 4;
       const int kk = dd / DKm, dk = dd % DKm;
@@ -857,8 +941,11 @@ cudaError_t launch_mma_t(const CUtensorMap &tk, const CUtensorMap &tv, const Par
   cfg.blockDim = l.block;
   cfg.dynamicSmemBytes = l.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
   if (l.cluster > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = l.cluster;

@@ -149,6 +149,15 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *addr) {
   return v;
 }
 
+// Programmatic dependent launch: wait for the prerequisite grid to complete
+// (and its writes to be visible); allow the dependent grid to launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
