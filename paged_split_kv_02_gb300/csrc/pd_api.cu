@@ -317,8 +317,8 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   int merge = max_parts > 1 ? 1 : 0, mergers = 0;
   if (coop_ok && o.merge != 1) {
     merge = 2;
-    mergers = 1;  // a power of two <= min(8, parts): D / mergers stays a multiple of 8
-    while (2 * mergers <= std::min<int64_t>(8, max_parts)) mergers *= 2;
+    mergers = 1;  // a power of two <= min(16, parts): D / mergers stays a multiple of 4
+    while (2 * mergers <= std::min<int64_t>(16, max_parts)) mergers *= 2;
   } else if (o.merge == 2 && max_parts > 1) {
     return PD_EINVAL;  // the grid does not fit at once, or a cluster was asked for
   }

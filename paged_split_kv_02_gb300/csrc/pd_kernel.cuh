@@ -76,6 +76,14 @@ __device__ __forceinline__ void store4(void *dst, const float (&v)[4]) {
   *reinterpret_cast<uint2 *>(dst) = w;
 }
 
+template <typename T>
+__device__ __forceinline__ T to_t(float x) {
+  if constexpr (std::is_same_v<T, __nv_bfloat16>)
+    return __float2bfloat16_rn(x);
+  else
+    return __float2half_rn(x);
+}
+
 __device__ __forceinline__ float exp2_or_zero(float x, float m) {
   // e^(x - m) in exp2 form; 0 for an empty row (x = -inf)
   return x == -INFINITY ? 0.f : exp2f(x - m);
@@ -94,8 +102,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   constexpr bool Q_IN_REGS = D <= 256;
 
   extern __shared__ unsigned char smem_raw[];
-  unsigned char *smem = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + kSmemAlign - 1) & ~uintptr_t(kSmemAlign - 1));
+  // aligned by pointer arithmetic on the shared array (not through an
+  // integer), so every pointer derived from it stays in the shared space
+  unsigned char *smem =
+      smem_raw + ((kSmemAlign - (smem_u32(smem_raw) & (kSmemAlign - 1))) & (kSmemAlign - 1));
   const int NS = p.NS, NT = p.NT, KG = p.KG, NC = NT * KG;
   const int NT8 = NT * 8;
   unsigned char *ring = smem;
@@ -491,78 +501,68 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     lrow[g_k * NT8 + r1] = l1;
   }
   if (CS == 1) {
-    // ---- no cluster: one pass over the warp groups' partials -------------
-    // Once every group's (m, l) is in shared memory, each warp scales its own
-    // rows by exp2(m_g - m*) as it stores them and the rows' (m*, L) are
-    // formed alongside; the pass that writes the output (one segment) or
-    // publishes the partial (several) then only sums the groups.
-    __syncthreads();
+    // ---- no cluster: one pass over the warp groups' raw accumulators -------
+    // Each warp stores its fragment unscaled (rows of D fp32, columns
+    // swizzled) next to its rows' (m, l), so one barrier separates the
+    // stores from the pass that forms every (row, 4 columns) item of the
+    // CTA's partial: sum over the groups of acc_g * exp2(m_g - m*), then
+    // normalised (one segment) or published (several).
     if (warp < NC) {
-      float ms0 = -INFINITY, ms1 = -INFINITY;
-      for (int gg = 0; gg < KG; ++gg) {
-        ms0 = fmaxf(ms0, mrow[gg * NT8 + r0]);
-        ms1 = fmaxf(ms1, mrow[gg * NT8 + r1]);
-      }
-      const float f0 = exp2_or_zero(m0, ms0 == -INFINITY ? 0.f : ms0);
-      const float f1 = exp2_or_zero(m1, ms1 == -INFINITY ? 0.f : ms1);
       float *dst = cp + (size_t)g_k * NT8 * D;
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
         const int d = mt * 16 + (lane >> 2);
-        dst[r0 * D + psw(d, r0)] = acc[mt][0] * f0;
-        dst[r1 * D + psw(d, r1)] = acc[mt][1] * f1;
-        dst[r0 * D + psw(d + 8, r0)] = acc[mt][2] * f0;
-        dst[r1 * D + psw(d + 8, r1)] = acc[mt][3] * f1;
-      }
-    } else {
-      for (int r = lane + 32 * (warp - NC); r < NT8; r += 32 * (blockDim.x / 32 - NC)) {
-        float ms = -INFINITY;
-        for (int gg = 0; gg < KG; ++gg) ms = fmaxf(ms, mrow[gg * NT8 + r]);
-        const float mu = ms == -INFINITY ? 0.f : ms;
-        float lsum = 0.f;
-        for (int gg = 0; gg < KG; ++gg) lsum += lrow[gg * NT8 + r] * exp2_or_zero(mrow[gg * NT8 + r], mu);
-        mfin[r] = ms;
-        lfin[r] = lsum;
+        dst[r0 * D + psw(d, r0)] = acc[mt][0];
+        dst[r1 * D + psw(d, r1)] = acc[mt][1];
+        dst[r0 * D + psw(d + 8, r0)] = acc[mt][2];
+        dst[r1 * D + psw(d + 8, r1)] = acc[mt][3];
       }
     }
     __syncthreads();
-    auto sum4 = [&](int r, int d4) -> float4 {
-      float4 a = *reinterpret_cast<const float4 *>(cp + (size_t)r * D + psw(d4, r));
-      for (int gg = 1; gg < KG; ++gg) {
-        const float4 b = *reinterpret_cast<const float4 *>(cp + ((size_t)gg * NT8 + r) * D + psw(d4, r));
-        a.x += b.x;
-        a.y += b.y;
-        a.z += b.z;
-        a.w += b.w;
-      }
-      return a;
-    };
-    if (nseg == 1) {
-      for (int idx = tid; idx < nrows * (D / 8); idx += blockDim.x) {
-        const int r = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
-        const float lr = lfin[r];
-        const float inv = lr > 0.f ? 1.f / lr : 0.f;
-        const float4 a = sum4(r, c8), b = sum4(r, c8 + 4);
-        const float v[8] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv,
-                            b.x * inv, b.y * inv, b.z * inv, b.w * inv};
-        store8<BF16>(out_row(r) + c8, v);
-      }
-      return;
-    }
-    // several segments: publish (in the layout of the merge that reads it)
     const int DKm = p.coop ? D / p.mergers : D;
     float *pa = p.part_acc + (gbase + cl_id) * (int64_t)NT8 * D;
+    float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
+#pragma unroll 1
     for (int idx = tid; idx < nrows * (D / 4); idx += blockDim.x) {
       const int r = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
-      const int k = d4 / DKm, dk = d4 % DKm;
-      __stcg(reinterpret_cast<float4 *>(pa + ((int64_t)k * NT8 + r) * DKm + dk), sum4(r, d4));
+      float mg[kMaxConsumerWarps];
+      float ms = -INFINITY;
+#pragma unroll
+      for (int gg = 0; gg < kMaxConsumerWarps; ++gg) {
+        mg[gg] = gg < KG ? mrow[gg * NT8 + r] : -INFINITY;
+        ms = fmaxf(ms, mg[gg]);
+      }
+      const float mu = ms == -INFINITY ? 0.f : ms;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      float lsum = 0.f;
+#pragma unroll
+      for (int gg = 0; gg < kMaxConsumerWarps; ++gg) {
+        if (gg < KG) {
+          const float w = exp2_or_zero(mg[gg], mu);
+          const float4 b = *reinterpret_cast<const float4 *>(cp + ((size_t)gg * NT8 + r) * D + psw(d4, r));
+          lsum += w * lrow[gg * NT8 + r];
+          a.x += w * b.x;
+          a.y += w * b.y;
+          a.z += w * b.z;
+          a.w += w * b.w;
+        }
+      }
+      if (nseg == 1) {
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
+        store4<BF16>(out_row(r) + d4, v);
+      } else {
+        const int k = d4 / DKm, dk = d4 % DKm;
+        __stcg(reinterpret_cast<float4 *>(pa + ((int64_t)k * NT8 + r) * DKm + dk), a);
+        if (d4 == 0) __stcg(pm + r, make_float2(ms, lsum));
+      }
     }
-    float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
-    for (int r = tid; r < nrows; r += blockDim.x) __stcg(pm + r, make_float2(mfin[r], lfin[r]));
+    if (nseg == 1) return;
   } else {
   __syncthreads();
   if (warp < NC) {
     float ms0 = -INFINITY, ms1 = -INFINITY;
+#pragma unroll 1
     for (int gg = 0; gg < KG; ++gg) {
       ms0 = fmaxf(ms0, mrow[gg * NT8 + r0]);
       ms1 = fmaxf(ms1, mrow[gg * NT8 + r1]);
@@ -581,8 +581,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
   __syncthreads();
   if (KG > 1) {
+#pragma unroll 1
     for (int idx = tid; idx < NT8 * D / 4; idx += blockDim.x) {
       float4 a = reinterpret_cast<float4 *>(cp)[idx];
+#pragma unroll 1
       for (int gg = 1; gg < KG; ++gg) {
         const float4 b = reinterpret_cast<float4 *>(cp + (size_t)gg * NT8 * D)[idx];
         a.x += b.x;
@@ -593,11 +595,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       reinterpret_cast<float4 *>(cp)[idx] = a;
     }
   }
+#pragma unroll 1
   for (int r = tid; r < NT8; r += blockDim.x) {
     float ms = -INFINITY;
+#pragma unroll 1
     for (int gg = 0; gg < KG; ++gg) ms = fmaxf(ms, mrow[gg * NT8 + r]);
     const float mu = ms == -INFINITY ? 0.f : ms;
     float lsum = 0.f;
+#pragma unroll 1
     for (int gg = 0; gg < KG; ++gg) lsum += lrow[gg * NT8 + r] * exp2_or_zero(mrow[gg * NT8 + r], mu);
     mfin[r] = ms;
     lfin[r] = lsum;
@@ -606,6 +611,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
   if (nseg == 1) {
     // one segment: normalise and store
+#pragma unroll 1
     for (int idx = tid; idx < nrows * (D / 8); idx += blockDim.x) {
       const int r = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
       const float lr = lfin[r];
@@ -627,15 +633,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   if (CS > 1) {
     float *wts = lcl + NT8;  // [CS][NT8]
     cluster_sync();          // every CTA's partial is in its shared memory
+#pragma unroll 1
     for (int r = tid; r < NT8; r += blockDim.x) {
       float mr[8];
       float ms = -INFINITY;
+#pragma unroll 1
       for (int x = 0; x < CS; ++x) {
         mr[x] = ld_dsmem_f32(mapa(smem_u32(mfin + r), x));
         ms = fmaxf(ms, mr[x]);
       }
       const float mu = ms == -INFINITY ? 0.f : ms;
       float lsum = 0.f;
+#pragma unroll 1
       for (int x = 0; x < CS; ++x) {
         const float w = exp2_or_zero(mr[x], mu);
         lsum += ld_dsmem_f32(mapa(smem_u32(lfin + r), x)) * w;
@@ -645,10 +654,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       lcl[r] = lsum;
     }
     __syncthreads();
+#pragma unroll 1
     for (int idx = tid; idx < NT8 * (DS / 4); idx += blockDim.x) {
       const int r = idx / (DS / 4), d = (int)rank * DS + (idx % (DS / 4)) * 4;
       const uint32_t local = smem_u32(cp + r * D + psw(d, r));
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
       for (int x = 0; x < CS; ++x) {
         const float w = wts[x * NT8 + r];
         const float4 b = ld_dsmem_f32x4(mapa(local, x));
@@ -668,6 +679,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   };
 
   if (ncl == 1) {
+#pragma unroll 1
     for (int idx = tid; idx < nrows * (DS / 8); idx += blockDim.x) {
       const int r = idx / (DS / 8), c8 = (idx % (DS / 8)) * 8;
       const float lr = lcl[r];
@@ -687,6 +699,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     // layout [part][K_max][NT8][D/K_max]: a merger's slice is one block
     const int DKm = D / p.mergers;
     float *pa = p.part_acc + (gbase + cl_id) * (int64_t)NT8 * D;
+#pragma unroll 1
     for (int idx = tid; idx < nrows * (D / 4); idx += blockDim.x) {
       const int r = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
       const int k = d4 / DKm, dk = d4 % DKm;
@@ -694,6 +707,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
   } else {
     float *pa = p.part_acc + ((gbase + cl_id) * CS + rank) * slice_floats;
+#pragma unroll 1
     for (int idx = tid; idx < nrows * (DS / 4); idx += blockDim.x) {
       const int r = idx / (DS / 4), d4 = (idx % (DS / 4)) * 4;
       __stcg(reinterpret_cast<float4 *>(pa + (int64_t)r * DS + d4), part4(r, d4));
@@ -702,6 +716,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   {
     if (rank == 0) {
       float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
+#pragma unroll 1
       for (int r = tid; r < nrows; r += blockDim.x) __stcg(pm + r, make_float2(mcl[r], lcl[r]));
     }
   }
@@ -743,73 +758,93 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
     __syncthreads();
     if (!flags[2]) return;
+    // count this merger past its wait now; the answer is needed only at the
+    // end, so the round trip overlaps the merge
+    const int fin_old = tid == 0 ? atomicAdd(p.counters + 2 * group + 1, 1) : 0;
     // this merger's layout slices: [mi * q, (mi + 1) * q) of the K_max slices
     const int DKm = D / p.mergers, q = p.mergers / K, DK = q * DKm;
     const int64_t part_floats = (int64_t)NT8 * D;
-    const int slab = q * NT8 * DKm;  // floats of one part's share
-    float *ml_s = ep;                   // [ncl][NT8][2] (m, l) of every part
-    float *w_s = ml_s + 2 * ncl * NT8;  // [ncl][NT8] weights
-    float *l_s = w_s + ncl * NT8;       // [NT8] merged sums
-    float *buf = l_s + NT8;             // [ncl][q][NT8][DKm]
-    const uint32_t mb = smem_u32(mbar_merge);
-    if (tid == 0) {
-      // one batch of bulk copies: every part's (m, l) and this merger's share
-      fence_proxy_async();
-      const uint32_t ml_bytes = (uint32_t)(ncl * NT8 * 8);
-      mbar_arrive_expect_tx(mb, (uint32_t)(ncl * slab * 4) + ml_bytes);
-      bulk_load(smem_u32(ml_s), p.part_ml + gbase * NT8 * 2, ml_bytes, mb);
-      for (int c = 0; c < ncl; ++c)
-        bulk_load(smem_u32(buf + (int64_t)c * slab),
-                  p.part_acc + (gbase + c) * part_floats + (int64_t)mi * slab, (uint32_t)(slab * 4),
-                  mb);
-    }
-    if (!__syncthreads_and(mbar_wait_bounded(mb, 0))) {
-      if (tid == 0) atomicOr(p.status, 0x1u);
-      return;
-    }
-    // weights: one warp per row, one lane per part
-    for (int r = warp; r < nrows; r += blockDim.x >> 5) {
-      float ms = -INFINITY;
-      for (int c = lane; c < ncl; c += 32) ms = fmaxf(ms, ml_s[(c * NT8 + r) * 2]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, o));
-      const float mu = ms == -INFINITY ? 0.f : ms;
-      float lsum = 0.f;
-      for (int c = lane; c < ncl; c += 32) {
-        const float w = exp2_or_zero(ml_s[(c * NT8 + r) * 2], mu);
-        w_s[c * NT8 + r] = w;
-        lsum += ml_s[(c * NT8 + r) * 2 + 1] * w;
+    const int slab = q * NT8 * DKm;      // floats of one part's share
+    float *ml_s = ep;                    // [ncl][NT8][2] (m, l) of every part
+    float *buf = ml_s + 2 * ncl * NT8;   // [ncl][q][NT8][DKm]
+    // Every part's (m, l) and this merger's share of every part, brought into
+    // shared memory by 16-byte asynchronous copies from every thread, all in
+    // flight at once (one L2 round trip).
+    {
+      const int slab4 = slab / 4, n_ml4 = ncl * NT8 / 2;
+      const int64_t part4 = part_floats / 4;
+      const float4 *ml_g = reinterpret_cast<const float4 *>(p.part_ml + gbase * NT8 * 2);
+      const float4 *acc_g = reinterpret_cast<const float4 *>(p.part_acc + gbase * part_floats) +
+                            (int64_t)mi * slab4;
+      const int nwarps = blockDim.x >> 5;
+#pragma unroll 1
+      for (int i = tid; i < n_ml4; i += blockDim.x) cp_async16(ml_s + 4 * i, ml_g + i);
+#pragma unroll 1
+      for (int c = warp; c < ncl; c += nwarps) {
+#pragma unroll 1
+        for (int j = lane; j < slab4; j += 32)
+          cp_async16(buf + ((int64_t)c * slab4 + j) * 4, acc_g + c * part4 + j);
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-      if (lane == 0) l_s[r] = lsum;
+      cp_async_wait_all();
     }
     __syncthreads();
-    for (int idx = tid; idx < nrows * (DK / 4); idx += blockDim.x) {
-      const int r = idx / (DK / 4), dd = (idx % (DK / 4)) * 4;
-      const int kk = dd / DKm, dk = dd % DKm;
-      const float *src = buf + ((int64_t)kk * NT8 + r) * DKm + dk;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 0; c < ncl; ++c) {
-        const float w = w_s[c * NT8 + r];
-        const float4 b = *reinterpret_cast<const float4 *>(src + (int64_t)c * slab);
-        a.x += w * b.x;
-        a.y += w * b.y;
-        a.z += w * b.z;
-        a.w += w * b.w;
+    // T threads (a power of two, adjacent lanes) per (row, 4 columns) item of
+    // the slice, each over every T-th part, two parts at a time: the row's
+    // largest m, then the weighted sums of l and of the accumulators,
+    // combined across the T threads by shuffles.
+    const int n_items = nrows * (DK / 4);
+    int lgT = 0;
+    while (lgT < 5 && (2 << lgT) * n_items <= (int)blockDim.x) ++lgT;
+    const int T = 1 << lgT;
+#pragma unroll 1
+    for (int base = 0; base < n_items * T; base += blockDim.x) {
+      const int item = (base + tid) >> lgT, sub = (base + tid) & (T - 1);
+      const bool active = item < n_items;
+      const int r = active ? item / (DK / 4) : 0, dd = active ? (item % (DK / 4)) * 4 : 0;
+      const float2 *mlr = reinterpret_cast<const float2 *>(ml_s) + r;
+      float ms = -INFINITY;
+#pragma unroll 1
+      for (int c = active ? sub : ncl; c < ncl; c += T) ms = fmaxf(ms, mlr[c * NT8].x);
+#pragma unroll 1
+      for (int o = 1; o < T; o <<= 1) ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, o));
+      const float mu = ms == -INFINITY ? 0.f : ms;
+      const float *src = buf + ((int64_t)(dd / DKm) * NT8 + r) * DKm + dd % DKm;
+      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+      float l0s = 0.f, l1s = 0.f;
+#pragma unroll 1
+      for (int c = active ? sub : ncl; c < ncl; c += 2 * T) {
+        const int c1 = c + T < ncl ? c + T : c;
+        const float2 m0v = mlr[c * NT8], m1v = mlr[c1 * NT8];
+        const float4 b0 = *reinterpret_cast<const float4 *>(src + (int64_t)c * slab);
+        const float4 b1 = *reinterpret_cast<const float4 *>(src + (int64_t)c1 * slab);
+        const float w0 = exp2_or_zero(m0v.x, mu);
+        const float w1 = c1 != c ? exp2_or_zero(m1v.x, mu) : 0.f;
+        l0s += m0v.y * w0;
+        l1s += m1v.y * w1;
+        a0.x += w0 * b0.x; a0.y += w0 * b0.y; a0.z += w0 * b0.z; a0.w += w0 * b0.w;
+        a1.x += w1 * b1.x; a1.y += w1 * b1.y; a1.z += w1 * b1.z; a1.w += w1 * b1.w;
       }
-      const float lr = l_s[r];
-      const float inv = lr > 0.f ? 1.f / lr : 0.f;
-      const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
-      store4<BF16>(out_row(r) + mi * DK + dd, v);
+      float lr = l0s + l1s;
+      float4 a = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
+#pragma unroll 1
+      for (int o = 1; o < T; o <<= 1) {
+        lr += __shfl_xor_sync(0xffffffffu, lr, o);
+        a.x += __shfl_xor_sync(0xffffffffu, a.x, o);
+        a.y += __shfl_xor_sync(0xffffffffu, a.y, o);
+        a.z += __shfl_xor_sync(0xffffffffu, a.z, o);
+        a.w += __shfl_xor_sync(0xffffffffu, a.w, o);
+      }
+      if (active && sub == 0) {
+        const float inv = lr > 0.f ? 1.f / lr : 0.f;
+        const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
+        store4<BF16>(out_row(r) + mi * DK + dd, v);
+      }
     }
-    if (tid == 0) {
-      // the last merger to finish resets both counters: every merger has
-      // passed its wait by then and every arrival has been counted
-      if (atomicAdd(p.counters + 2 * group + 1, 1) == K - 1) {
-        atomicExch(p.counters + 2 * group, 0);
-        atomicExch(p.counters + 2 * group + 1, 0);
-      }
+    if (tid == 0 && fin_old == K - 1) {
+      // the last merger past its wait resets both counters: every merger
+      // has passed its wait by then and every arrival has been counted
+      atomicExch(p.counters + 2 * group, 0);
+      atomicExch(p.counters + 2 * group + 1, 0);
     }
     return;
   }
@@ -819,6 +854,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const int last = old == ncl - 1;
     if (last) atomicExch(p.counters + 2 * group, 0);
     flags[1] = last;
+#pragma unroll 1
     for (int x = 1; x < CS; ++x)
       st_dsmem_u32(mapa(smem_u32((const void *)(flags + 1)), x), (uint32_t)last);
   }
@@ -847,6 +883,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       fence_proxy_async();
       const uint32_t bytes = (uint32_t)(nr * DS * 4);
       mbar_arrive_expect_tx(mb, bytes * np);
+#pragma unroll 1
       for (int c = 0; c < np; ++c)
         bulk_load(smem_u32(buf + (int64_t)c * RC * DS),
                   p.part_acc + ((gbase + p0 + c) * CS + rank) * slice_floats + (int64_t)rc0 * DS,
@@ -854,17 +891,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
   };
   if (nrows > 0) request(0, 0);
+#pragma unroll 1
   for (int idx = tid; idx < ncl * NT8; idx += blockDim.x) {
     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + gbase * NT8 * 2) + idx);
     pm_s[idx] = ml.x;
     pl_s[idx] = ml.y;
   }
   __syncthreads();
+#pragma unroll 1
   for (int r = tid; r < nrows; r += blockDim.x) {
     float ms = -INFINITY;
+#pragma unroll 1
     for (int c = 0; c < ncl; ++c) ms = fmaxf(ms, pm_s[c * NT8 + r]);
     const float mu = ms == -INFINITY ? 0.f : ms;
     float lsum = 0.f;
+#pragma unroll 1
     for (int c = 0; c < ncl; ++c) {
       const float w = exp2_or_zero(pm_s[c * NT8 + r], mu);
       pm_s[c * NT8 + r] = w;
@@ -874,12 +915,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
   uint32_t phase = 0;
   bool ok = true, first = true;
+#pragma unroll 1
   for (int rc0 = 0; rc0 < nrows && ok; rc0 += RC) {
     const int nr = min(RC, nrows - rc0);
     const int nitems = nr * (DS / 4);
     float4 a[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
     for (int p0 = 0; p0 < ncl; p0 += PC) {
       const int np = min(PC, ncl - p0);
       __syncthreads();  // the weights are in place; the previous chunk is consumed
@@ -897,6 +940,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const int it = tid + k * nthr;
         if (it < nitems) {
           const int rl = it / (DS / 4), d4 = (it % (DS / 4)) * 4;
+#pragma unroll 1
           for (int c = 0; c < np; ++c) {
             const float w = pm_s[(p0 + c) * NT8 + rc0 + rl];
             const float4 b = *reinterpret_cast<const float4 *>(buf + ((int64_t)c * RC + rl) * DS + d4);

@@ -93,6 +93,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and the wait for
+// all of this thread's outstanding ones.
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Order this thread's earlier generic-proxy accesses before its later
 // async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async() {
