@@ -76,14 +76,6 @@ __device__ __forceinline__ void store4(void *dst, const float (&v)[4]) {
   *reinterpret_cast<uint2 *>(dst) = w;
 }
 
-template <typename T>
-__device__ __forceinline__ T to_t(float x) {
-  if constexpr (std::is_same_v<T, __nv_bfloat16>)
-    return __float2bfloat16_rn(x);
-  else
-    return __float2half_rn(x);
-}
-
 __device__ __forceinline__ float exp2_or_zero(float x, float m) {
   // e^(x - m) in exp2 form; 0 for an empty row (x = -inf)
   return x == -INFINITY ? 0.f : exp2f(x - m);
@@ -480,9 +472,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   float *lfin = mfin + NT8;
 
   T *obase = static_cast<T *>(p.out);
+  const int lg_g = (p.G & (p.G - 1)) == 0 ? __ffs(p.G) - 1 : -1;  // G a power of two
   auto out_row = [&](int r) -> T * {
     const int rr = rr0 + r;
-    const int i = rr / p.G, j = rr % p.G;
+    const int i = lg_g >= 0 ? rr >> lg_g : rr / p.G;
+    const int j = rr - i * p.G;
     return obase + (int64_t)(s * p.M + i) * p.o_s0 + (int64_t)(h * p.G + j) * p.o_s1;
   };
   const int nrows = max(0, rr1 - rr0);  // valid rows of this CTA
@@ -520,6 +514,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
     __syncthreads();
     const int DKm = p.coop ? D / p.mergers : D;
+    const int lg_dkm = __ffs(DKm) - 1;
     float *pa = p.part_acc + (gbase + cl_id) * (int64_t)NT8 * D;
     float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
 #pragma unroll 1
@@ -552,7 +547,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
         store4<BF16>(out_row(r) + d4, v);
       } else {
-        const int k = d4 / DKm, dk = d4 % DKm;
+        // DKm is a power of two
+        const int k = d4 >> lg_dkm, dk = d4 & (DKm - 1);
         __stcg(reinterpret_cast<float4 *>(pa + ((int64_t)k * NT8 + r) * DKm + dk), a);
         if (d4 == 0) __stcg(pm + r, make_float2(ms, lsum));
       }
@@ -788,46 +784,67 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       cp_async_wait_all();
     }
     __syncthreads();
-    // T threads (a power of two, adjacent lanes) per (row, 4 columns) item of
-    // the slice, each over every T-th part, two parts at a time: the row's
-    // largest m, then the weighted sums of l and of the accumulators,
-    // combined across the T threads by shuffles.
-    const int n_items = nrows * (DK / 4);
+    // TPI threads (a power of two, adjacent lanes) per (row, 4 columns) item
+    // of the slice.  Parts are taken 8 * TPI at a time: each thread loads its
+    // eight (m, l) and accumulator rows at once, the chunk's largest m is
+    // shared by shuffles, and the running sums are rescaled when it grows
+    // (online softmax over the parts); the TPI threads' sums are then added
+    // by shuffles.  DKm and DK / 4 are powers of two.
+    const int lg_dkm = __ffs(DKm) - 1, lg_i = __ffs(DK / 4) - 1;
+    const int n_items = nrows << lg_i;
     int lgT = 0;
     while (lgT < 5 && (2 << lgT) * n_items <= (int)blockDim.x) ++lgT;
-    const int T = 1 << lgT;
+    const int TPI = 1 << lgT;  // threads per item
+    constexpr int kChunk = 8;
 #pragma unroll 1
-    for (int base = 0; base < n_items * T; base += blockDim.x) {
-      const int item = (base + tid) >> lgT, sub = (base + tid) & (T - 1);
+    for (int base = 0; base < n_items * TPI; base += blockDim.x) {
+      const int item = (base + tid) >> lgT, sub = (base + tid) & (TPI - 1);
       const bool active = item < n_items;
-      const int r = active ? item / (DK / 4) : 0, dd = active ? (item % (DK / 4)) * 4 : 0;
+      const int r = active ? item >> lg_i : 0, dd = active ? (item & ((DK >> 2) - 1)) * 4 : 0;
       const float2 *mlr = reinterpret_cast<const float2 *>(ml_s) + r;
-      float ms = -INFINITY;
+      const float *src = buf + ((int64_t)(dd >> lg_dkm) * NT8 + r) * DKm + (dd & (DKm - 1));
+      float M = -INFINITY, lr = 0.f;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-      for (int c = active ? sub : ncl; c < ncl; c += T) ms = fmaxf(ms, mlr[c * NT8].x);
+      for (int c0 = 0; c0 < ncl; c0 += kChunk * TPI) {
+        float2 mv[kChunk];
+        float4 bv[kChunk];
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) {
+          const int c = c0 + sub + u * TPI;
+          if (active && c < ncl) {
+            mv[u] = mlr[c * NT8];
+            bv[u] = *reinterpret_cast<const float4 *>(src + (int64_t)c * slab);
+          } else {
+            mv[u] = make_float2(-INFINITY, 0.f);
+            bv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+        float cm = M;
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) cm = fmaxf(cm, mv[u].x);
 #pragma unroll 1
-      for (int o = 1; o < T; o <<= 1) ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, o));
-      const float mu = ms == -INFINITY ? 0.f : ms;
-      const float *src = buf + ((int64_t)(dd / DKm) * NT8 + r) * DKm + dd % DKm;
-      float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-      float l0s = 0.f, l1s = 0.f;
-#pragma unroll 1
-      for (int c = active ? sub : ncl; c < ncl; c += 2 * T) {
-        const int c1 = c + T < ncl ? c + T : c;
-        const float2 m0v = mlr[c * NT8], m1v = mlr[c1 * NT8];
-        const float4 b0 = *reinterpret_cast<const float4 *>(src + (int64_t)c * slab);
-        const float4 b1 = *reinterpret_cast<const float4 *>(src + (int64_t)c1 * slab);
-        const float w0 = exp2_or_zero(m0v.x, mu);
-        const float w1 = c1 != c ? exp2_or_zero(m1v.x, mu) : 0.f;
-        l0s += m0v.y * w0;
-        l1s += m1v.y * w1;
-        a0.x += w0 * b0.x; a0.y += w0 * b0.y; a0.z += w0 * b0.z; a0.w += w0 * b0.w;
-        a1.x += w1 * b1.x; a1.y += w1 * b1.y; a1.z += w1 * b1.z; a1.w += w1 * b1.w;
+        for (int o = 1; o < TPI; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+        const float mu = cm == -INFINITY ? 0.f : cm;
+        const float sc = exp2_or_zero(M, mu);
+        lr *= sc;
+        a.x *= sc;
+        a.y *= sc;
+        a.z *= sc;
+        a.w *= sc;
+#pragma unroll
+        for (int u = 0; u < kChunk; ++u) {
+          const float w = exp2_or_zero(mv[u].x, mu);
+          lr += w * mv[u].y;
+          a.x += w * bv[u].x;
+          a.y += w * bv[u].y;
+          a.z += w * bv[u].z;
+          a.w += w * bv[u].w;
+        }
+        M = cm;
       }
-      float lr = l0s + l1s;
-      float4 a = make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
 #pragma unroll 1
-      for (int o = 1; o < T; o <<= 1) {
+      for (int o = 1; o < TPI; o <<= 1) {
         lr += __shfl_xor_sync(0xffffffffu, lr, o);
         a.x += __shfl_xor_sync(0xffffffffu, a.x, o);
         a.y += __shfl_xor_sync(0xffffffffu, a.y, o);
