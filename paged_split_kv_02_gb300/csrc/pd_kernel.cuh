@@ -89,7 +89,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
   constexpr int NBOX = D / 64;                  // 128-byte boxes across the head dim
   constexpr int BLOCK_BYTES = kBlockKeys * D * 2;
-  constexpr int TB = kStageBytes / 2 / BLOCK_BYTES;  // 16-key blocks per stage
+  constexpr int STAGE = kStageBytes;
+  constexpr int TB = STAGE / 2 / BLOCK_BYTES;  // 16-key blocks per stage
   constexpr int KS = D / 16;                    // mma k-steps over d, and m-tiles of O^T
   constexpr bool Q_IN_REGS = D <= 256;
 
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int NS = p.NS, NT = p.NT, KG = p.KG, NC = NT * KG;
   const int NT8 = NT * 8;
   unsigned char *ring = smem;
-  unsigned char *qs = ring + NS * kStageBytes;
+  unsigned char *qs = ring + NS * STAGE;
   uint64_t *full = reinterpret_cast<uint64_t *>(qs + NT * D * 16);
   uint64_t *empty = full + NS;
   volatile int *flags = reinterpret_cast<volatile int *>(empty + NS);  // [0] abort, [1] last
@@ -112,6 +113,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int seg = blockIdx.x % p.max_seg;
   const int hg = blockIdx.x / p.max_seg;
   const int h = hg / p.rg, grow = hg % p.rg;
+
+  // ---- set-up that reads no global memory (it overlaps the previous grid's
+  // tail): barriers, the tensor-map prefetch (the Q tile is loaded by the
+  // consumers later) ----
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(full + i), 1);
+      mbar_init(smem_u32(empty + i), NT);
+    }
+    mbar_init(smem_u32(mbar_merge), 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == NC && lane == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  __syncthreads();
 
   // Launched with programmatic stream serialisation: wait here until the
   // previous grid on the stream (which may have written q, the caches, the
@@ -127,7 +147,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int spec_b0 = seg * p.seg_blocks;
   const int32_t *bt_row = p.block_table + (int64_t)s * p.bt_stride;
   const int bt_blocks = p.bt_width * (p.P / kBlockKeys);
-  if (warp == p.NT * p.KG && p.window == 0) {
+  if (warp == NC && p.window == 0) {
 #pragma unroll
     for (int k = 0; k < kSpec / 32; ++k) {
       const int i = lane + 32 * k, b = spec_b0 + i;
@@ -165,18 +185,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int my_nb = max(0, min(b_first + nb, my_b0 + sb) - my_b0);
   const int ntile = (my_nb + TB - 1) / TB;
 
-  // ---- set-up: barriers (the Q tile is loaded by the consumers) ----------
-  if (tid == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(smem_u32(full + i), 1);
-      mbar_init(smem_u32(empty + i), NT);
-    }
-    mbar_init(smem_u32(mbar_merge), 1);
-    flags[0] = 0;
-    flags[1] = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
 
   // Consumer state (kept in registers across the main loop).
   float acc[KS][4];
@@ -189,10 +197,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   if (warp == NC) {
     // ================= producer: the page gather ===========================
     const uint64_t pol = policy_evict_first();
-    if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-    }
     // Physical page of every 16-key block of the segment, read from the
     // block table kBlockIds at a time ahead of the copies that need them, so
     // no TMA issue waits on a dependent global load.
@@ -247,7 +251,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           phys = 0;
         }
         const uint32_t dst =
-            smem_u32(ring + slot * kStageBytes + kv * (TB * BLOCK_BYTES) + b * BLOCK_BYTES);
+            smem_u32(ring + slot * STAGE + kv * (TB * BLOCK_BYTES) + b * BLOCK_BYTES);
         tma_load_5d(dst, kv ? &tmV : &tmK, smem_u32(full + slot), 0, key0 % p.P, 0, h, phys, pol);
       }
       issued = j + 1;
@@ -317,7 +321,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         break;
       }
       const int nbt = min(TB, my_nb - j * TB);
-      const uint32_t kbase = smem_u32(ring + slot * kStageBytes);
+      const uint32_t kbase = smem_u32(ring + slot * STAGE);
       const uint32_t vbase = kbase + TB * BLOCK_BYTES;
       const int key_t0 = (my_b0 + j * TB) * kBlockKeys;
 
@@ -517,42 +521,79 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const int lg_dkm = __ffs(DKm) - 1;
     float *pa = p.part_acc + (gbase + cl_id) * (int64_t)NT8 * D;
     float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
+    // one item = (row, kCols columns), every load of an item issued at once;
+    // 4 columns when that gives every thread at most one item, else 16
+    auto items_pass = [&](auto cols) {
+    constexpr int kCols = decltype(cols)::value, kItemsPerRow = D / kCols;
 #pragma unroll 1
-    for (int idx = tid; idx < nrows * (D / 4); idx += blockDim.x) {
-      const int r = idx / (D / 4), d4 = (idx % (D / 4)) * 4;
-      float mg[kMaxConsumerWarps];
+    for (int idx = tid; idx < nrows * kItemsPerRow; idx += blockDim.x) {
+      const int r = idx / kItemsPerRow, d16 = (idx % kItemsPerRow) * kCols;
       float ms = -INFINITY;
 #pragma unroll
-      for (int gg = 0; gg < kMaxConsumerWarps; ++gg) {
-        mg[gg] = gg < KG ? mrow[gg * NT8 + r] : -INFINITY;
-        ms = fmaxf(ms, mg[gg]);
-      }
+      for (int gg = 0; gg < kMaxConsumerWarps; ++gg)
+        if (gg < KG) ms = fmaxf(ms, mrow[gg * NT8 + r]);
       const float mu = ms == -INFINITY ? 0.f : ms;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      float lsum = 0.f;
+      float4 a[kCols / 4];
 #pragma unroll
-      for (int gg = 0; gg < kMaxConsumerWarps; ++gg) {
-        if (gg < KG) {
-          const float w = exp2_or_zero(mg[gg], mu);
-          const float4 b = *reinterpret_cast<const float4 *>(cp + ((size_t)gg * NT8 + r) * D + psw(d4, r));
-          lsum += w * lrow[gg * NT8 + r];
-          a.x += w * b.x;
-          a.y += w * b.y;
-          a.z += w * b.z;
-          a.w += w * b.w;
+      for (int v = 0; v < kCols / 4; ++v) a[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      float lsum = 0.f;
+      constexpr int kGroupChunk = 4;  // warp groups whose loads are in flight at once
+#pragma unroll 1
+      for (int g0 = 0; g0 < KG; g0 += kGroupChunk) {
+        float mg[kGroupChunk], lg[kGroupChunk];
+        float4 b[kGroupChunk][kCols / 4];
+#pragma unroll
+        for (int u = 0; u < kGroupChunk; ++u) {
+          const int gg = g0 + u;
+          if (gg < KG) {
+            mg[u] = mrow[gg * NT8 + r];
+            lg[u] = lrow[gg * NT8 + r];
+#pragma unroll
+            for (int v = 0; v < kCols / 4; ++v)
+              b[u][v] = *reinterpret_cast<const float4 *>(cp + ((size_t)gg * NT8 + r) * D +
+                                                          psw(d16 + 4 * v, r));
+          } else {
+            mg[u] = -INFINITY;
+            lg[u] = 0.f;
+#pragma unroll
+            for (int v = 0; v < kCols / 4; ++v) b[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kGroupChunk; ++u) {
+          const float w = exp2_or_zero(mg[u], mu);
+          lsum += w * lg[u];
+#pragma unroll
+          for (int v = 0; v < kCols / 4; ++v) {
+            a[v].x += w * b[u][v].x;
+            a[v].y += w * b[u][v].y;
+            a[v].z += w * b[u][v].z;
+            a[v].w += w * b[u][v].w;
+          }
         }
       }
       if (nseg == 1) {
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-        const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
-        store4<BF16>(out_row(r) + d4, v);
+#pragma unroll
+        for (int v = 0; v < kCols / 4; ++v) {
+          const float o[4] = {a[v].x * inv, a[v].y * inv, a[v].z * inv, a[v].w * inv};
+          store4<BF16>(out_row(r) + d16 + 4 * v, o);
+        }
       } else {
-        // DKm is a power of two
-        const int k = d4 >> lg_dkm, dk = d4 & (DKm - 1);
-        __stcg(reinterpret_cast<float4 *>(pa + ((int64_t)k * NT8 + r) * DKm + dk), a);
-        if (d4 == 0) __stcg(pm + r, make_float2(ms, lsum));
+        // DKm is a power of two (>= 4)
+#pragma unroll
+        for (int v = 0; v < kCols / 4; ++v) {
+          const int d4 = d16 + 4 * v, k = d4 >> lg_dkm, dk = d4 & (DKm - 1);
+          __stcg(reinterpret_cast<float4 *>(pa + ((int64_t)k * NT8 + r) * DKm + dk), a[v]);
+        }
+        if (d16 == 0) __stcg(pm + r, make_float2(ms, lsum));
       }
     }
+    };
+    if (nrows * (D / 4) <= (int)blockDim.x)
+      items_pass(std::integral_constant<int, 4>{});
+    else
+      items_pass(std::integral_constant<int, 16>{});
     if (nseg == 1) return;
   } else {
   __syncthreads();
