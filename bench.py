@@ -44,6 +44,27 @@ WORKLOAD = ("spec-decode sweep: bf16, head_size 128, 32 q / 8 kv heads, page_siz
             "per case")
 
 
+# DRAM bytes (read + write) over algorithmic bytes of the decode kernel, from
+# the ncu capture summarised in profiles/pd_decode_mma_d128_bf16_spec_decode_
+# M4_L32768.md (M=4, 32768 keys).  It holds for the kernel sources the
+# capture was taken on only: with any other sources `traffic` is null.
+TRAFFIC_CAPTURE = {"sources": "2bb4f5c993c74904", "dram_over_algorithmic": 1.0229}
+
+
+def _kernel_sources_digest() -> str:
+    import glob
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_split_kv_02_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
+                    glob.glob(os.path.join(csrc, "*.h"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -206,7 +227,7 @@ def run_ours(args, world, rank, local):
     _barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
+        with torch.cuda.stream(stream), torch.cuda.nvtx.range("bench_timed_steps"):
             ev0.record(stream)
             for i in range(args.steps):
                 step_graphs[i % n_step_graphs].replay()
@@ -249,6 +270,11 @@ def run_ours(args, world, rank, local):
                          "replicas": n})
         del g
     long_ctx = [c["pct_hbm"] for c in per_case if c["context"] >= 4096]
+    traffic, traffic_basis = None, "no ncu capture of these kernel sources"
+    if _kernel_sources_digest() == TRAFFIC_CAPTURE["sources"]:
+        traffic = round(TRAFFIC_CAPTURE["dram_over_algorithmic"] * alg_step / len(keys))
+        traffic_basis = ("bytes per launch, averaged over the step's calls: the DRAM/algorithmic "
+                         "ratio of one ncu capture (M=4, 32768 keys) x the algorithmic bytes")
 
     # ---- end to end through the C ABI with host buffers --------------------
     e2e = None
@@ -290,7 +316,8 @@ def run_ours(args, world, rank, local):
             "peak": peak,
             "unit": "GB/s",
             "frac": round(alg_step / (step_ms * 1e-3) / 1e9 / peak, 4),
-            "traffic": None,
+            "traffic": traffic,
+            "traffic_basis": traffic_basis,
             "peak_kind": peak_kind,
         },
         "median_pct_hbm_4k_32k": round(statistics.median(long_ctx), 2) if long_ctx else None,
