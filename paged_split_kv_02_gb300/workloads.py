@@ -295,7 +295,7 @@ def spec_decode_hnd(M: int, L: int, seed: int = 0, device: str = "cpu",
 
 
 def sliding_window(dtype: torch.dtype, M: int, L: int, seed: int = 0,
-                   device: str = "cpu") -> DecodeCase:
+                   device: str = "cpu", gen_device: str = "cpu") -> DecodeCase:
     """D=256, 8 q / 1 kv head, window 512, P=32; the block table holds only
     the pages the window reaches (earlier entries point at a NaN page)."""
     tag = "fp16" if dtype == torch.float16 else "bf16"
@@ -303,7 +303,7 @@ def sliding_window(dtype: torch.dtype, M: int, L: int, seed: int = 0,
         f"sliding_window_{tag}_d256_w512_M{M}_L{L}",
         seed=seed, dtype=dtype, head_size=256, num_q_heads=8, num_kv_heads=1,
         page_size=32, max_query_len=M, seq_lens=[L], layout=HND, window=512,
-        window_pages_only=True, device=device,
+        window_pages_only=True, device=device, gen_device=gen_device,
     )
 
 
@@ -319,7 +319,7 @@ def wide_head(M: int, L: int, seed: int = 0, device: str = "cpu",
 
 
 def batched_hybrid_pages(seed: int = 0, num_seqs: int = 64, max_len: int = 16384,
-                         device: str = "cpu") -> DecodeCase:
+                         device: str = "cpu", gen_device: str = "cpu") -> DecodeCase:
     """bf16, D=256, 16 q / 2 kv heads, P=1056, M=4, 64 sequences with lengths
     uniform in [1, max_len] and one empty (padded) slot; a shared pool with
     10 % slack pages, randomly permuted."""
@@ -333,7 +333,7 @@ def batched_hybrid_pages(seed: int = 0, num_seqs: int = 64, max_len: int = 16384
         seed=seed, dtype=torch.bfloat16, head_size=256, num_q_heads=16,
         num_kv_heads=2, page_size=P, max_query_len=4, seq_lens=lens,
         layout=HND, pool_pages=used + max(1, used // 10),
-        table_width=(max_len + P - 1) // P, device=device,
+        table_width=(max_len + P - 1) // P, device=device, gen_device=gen_device,
     )
 
 

@@ -1,0 +1,71 @@
+"""The five decode configurations at their full sizes, run the way bench.py
+runs them (the library's own plan: segments, warp groups, cooperative
+merge), checked on sampled output rows that the oracle computes one by one,
+plus properties that hold at any size (finite outputs, a clean device
+status word, counters left at zero).
+
+Inputs are drawn on the device with the seeded CUDA generator (the sizes
+reach 1 GB of K/V) and copied to the host for the oracle."""
+
+import pytest
+import torch
+
+import paged_split_kv_02_gb300 as pd
+from paged_split_kv_02_gb300 import workloads as W
+from gpu_helpers import check, run, sample_rows, scratch_for
+
+pytestmark = pytest.mark.gpu
+
+N_ROWS = 48
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    pd.build()
+    yield
+    assert pd.paged_decode_device_status(reset=True) == 0
+
+
+def _full_size(case_gpu, seed):
+    sc = scratch_for(case_gpu)
+    out = run(case_gpu, scratch=sc)
+    assert torch.isfinite(out.float()).all()
+    assert int(sc.counters().abs().sum()) == 0, "counters not left at zero"
+    assert pd.paged_decode_device_status(reset=True) == 0
+    case_cpu = case_gpu.to("cpu")
+    rows = sample_rows(case_cpu, N_ROWS, seed=seed)
+    check(case_cpu, out, rows=rows)
+    return out
+
+
+@pytest.mark.parametrize("L", [4096, 16384, 32768])
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+def test_spec_decode_full(M, L):
+    """bf16, D=128, 32/8 heads, P=16, HND, batch 1 (the bench sweep)."""
+    _full_size(W.spec_decode_hnd(M, L, seed=100 + M, device="cuda", gen_device="cuda"), seed=M)
+
+
+@pytest.mark.parametrize("L", [1024, 4096, 16384, 32768])
+@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_sliding_window_full(dtype, M, L):
+    """D=256, 8/1 heads, window 512, P=32, block table of the window's pages."""
+    _full_size(W.sliding_window(dtype, M, L, seed=200 + M, device="cuda", gen_device="cuda"),
+               seed=M)
+
+
+@pytest.mark.parametrize("L", [4096, 32768])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_wide_head_full(M, L):
+    """fp16, D=512, 8/1 heads, full causal, P=16, N(0, 0.5): the heavy split."""
+    _full_size(W.wide_head(M, L, seed=300 + M, device="cuda", gen_device="cuda"), seed=M)
+
+
+def test_batched_hybrid_pages_full():
+    """bf16, D=256, 16/2 heads, P=1056, 64 sequences U[1, 16384] with an
+    empty slot, M=4: every sequence's first and last rows are sampled."""
+    case = W.batched_hybrid_pages(seed=400, device="cuda", gen_device="cuda")
+    out = _full_size(case, seed=5)
+    empty = [s for s, L in enumerate(case.seq_lens_host) if L == 0]
+    for s in empty:
+        assert torch.all(out[s * 4:(s + 1) * 4] == 0)
