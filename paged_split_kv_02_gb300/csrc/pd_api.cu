@@ -241,9 +241,17 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, nb_max));
   const int64_t part_floats = 8LL * NT * D;  // one partial's acc
   int CS = o.cluster > 0 ? o.cluster : 1;
-  // clusters only in the one-wave regime: a batch runs several waves, where
-  // the last-arriving CTA's merge overlaps other CTAs' work
-  if (o.cluster == 0 && S <= 1 && nseg >= 8 && nseg * part_floats * 4 > (256 << 10)) CS = 8;
+  // A cooperative merger needs room for one part's (m, l) and share at least
+  // (it pulls the parts a window at a time; K >= 2 mergers).
+  const int64_t coop_floats = 16LL * NT + 8LL * NT * D / 2 + 64;
+  const bool coop_possible = o.merge != 1 && (int64_t)S * Hkv * rg * nseg <= num_sms &&
+                             coop_floats * 4 <= epilogue_bytes(D, NT, NS);
+  // Clusters only in the one-wave regime (a batch runs several waves, where
+  // the last-arriving CTA's merge overlaps other CTAs' work) and only when
+  // the cooperative merge is not possible (it measured faster).
+  if (o.cluster == 0 && S <= 1 && nseg >= 8 && nseg * part_floats * 4 > (256 << 10) &&
+      !coop_possible)
+    CS = 8;
   if (CS != 1 && CS != 2 && CS != 4 && CS != 8) return PD_EINVAL;
   if (CS > 1) {
     if (o.segments > 0) {
@@ -307,11 +315,6 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   // launched cooperatively; then the last K arrivals of a group each merge
   // one D/K slice instead of the last arrival merging all of it alone.
   if (o.merge < 0 || o.merge > 2) return PD_EINVAL;
-  const int64_t nt8 = 8LL * NT;
-  // a merger's shared memory: (m, l) of every part, and its share of every
-  // part (K >= half the parts when there are <= 8)
-  const int64_t coop_floats = 3 * max_parts * nt8 + nt8 + 64 +
-                              std::max<int64_t>(2 * nt8 * D, cdiv(max_parts * nt8 * D, 8));
   const bool coop_ok = max_parts > 1 && CS == 1 && (int64_t)S * Hkv * rg * nseg <= num_sms &&
                        coop_floats * 4 <= epilogue_bytes(D, NT, NS);
   int merge = max_parts > 1 ? 1 : 0, mergers = 0;

@@ -801,7 +801,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     // this merger's layout slices: [mi * q, (mi + 1) * q) of the K_max slices
     const int DKm = D / p.mergers, q = p.mergers / K, DK = q * DKm;
     const int64_t part_floats = (int64_t)NT8 * D;
-    const int slab = q * NT8 * DKm;      // floats of one part's share
+    const int slab = q * NT8 * DKm;  // floats of one part's share
+    if (ncl * (2 * NT8 + slab) + 64 <= p.epi_floats &&
+        nrows * (DK / 4) <= (int)blockDim.x) {
+    // every part fits in shared memory at once and each thread has at most
+    // one item: one round of copies, one pass
     float *ml_s = ep;                    // [ncl][NT8][2] (m, l) of every part
     float *buf = ml_s + 2 * ncl * NT8;   // [ncl][q][NT8][DKm]
     // Every part's (m, l) and this merger's share of every part, brought into
@@ -897,6 +901,138 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
         store4<BF16>(out_row(r) + mi * DK + dd, v);
       }
+    }
+    } else {
+    // Parts are pulled into shared memory a window at a time ([win][NT8][2]
+    // (m, l), then [win][q][NT8][DKm] shares), as many as the dead ring holds.
+    const int win = max(1, min(ncl, (int)((p.epi_floats - 64) / (2 * NT8 + slab))));
+    float *ml_s = ep;
+    float *buf = ml_s + 2 * win * NT8;
+    // TPI threads (a power of two, adjacent lanes) per (row, 4 columns) item
+    // of the slice, up to kMaxRounds items per thread.  Parts are taken
+    // 8 * TPI at a time: each thread loads its eight (m, l) and accumulator
+    // rows at once, the chunk's largest m is shared by shuffles, and the
+    // running sums are rescaled when it grows (online softmax over the
+    // parts); the TPI threads' sums are added by shuffles at the end.  DKm
+    // and DK / 4 are powers of two.
+    const int lg_dkm = __ffs(DKm) - 1, lg_i = __ffs(DK / 4) - 1;
+    const int n_items = nrows << lg_i;
+    int lgT = 0;
+    while (lgT < 5 && (2 << lgT) * n_items <= (int)blockDim.x) ++lgT;
+    const int TPI = 1 << lgT;  // threads per item
+    constexpr int kChunk = 8, kMaxRounds = 4;
+    const int slab4 = slab / 4;
+    const int64_t part4 = part_floats / 4;
+    const float4 *ml_g = reinterpret_cast<const float4 *>(p.part_ml + gbase * NT8 * 2);
+    const float4 *acc_g =
+        reinterpret_cast<const float4 *>(p.part_acc + gbase * part_floats) + (int64_t)mi * slab4;
+    const int nwarps = blockDim.x >> 5;
+    // items beyond kMaxRounds per thread (a large slice) go in further
+    // batches, each over all the windows again
+#pragma unroll 1
+    for (int ib = 0; ib < n_items * TPI; ib += kMaxRounds * blockDim.x) {
+    const int rounds = min(kMaxRounds, (n_items * TPI - ib + blockDim.x - 1) / blockDim.x);
+    float Ms[kMaxRounds], Ls[kMaxRounds];
+    float4 As[kMaxRounds];
+#pragma unroll
+    for (int ri = 0; ri < kMaxRounds; ++ri) {
+      Ms[ri] = -INFINITY;
+      Ls[ri] = 0.f;
+      As[ri] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll 1
+    for (int w0 = 0; w0 < ncl; w0 += win) {
+      const int nw = min(win, ncl - w0);
+      if (w0 > 0 || ib > 0) __syncthreads();  // the previous window is consumed
+      // the window's (m, l) and shares: 16-byte asynchronous copies from
+      // every thread, all in flight at once (one L2 round trip)
+#pragma unroll 1
+      for (int i = tid; i < nw * NT8 / 2; i += blockDim.x)
+        cp_async16(ml_s + 4 * i, ml_g + (int64_t)w0 * NT8 / 2 + i);
+#pragma unroll 1
+      for (int c = warp; c < nw; c += nwarps) {
+#pragma unroll 1
+        for (int j = lane; j < slab4; j += 32)
+          cp_async16(buf + ((int64_t)c * slab4 + j) * 4, acc_g + (int64_t)(w0 + c) * part4 + j);
+      }
+      cp_async_wait_all();
+      __syncthreads();
+#pragma unroll
+      for (int ri = 0; ri < kMaxRounds; ++ri) {
+        if (ri >= rounds) break;
+        const int gi = ib + ri * blockDim.x + tid;
+        const int item = gi >> lgT, sub = gi & (TPI - 1);
+        const bool active = item < n_items;
+        const int r = active ? item >> lg_i : 0, dd = active ? (item & ((DK >> 2) - 1)) * 4 : 0;
+        const float2 *mlr = reinterpret_cast<const float2 *>(ml_s) + r;
+        const float *src = buf + ((int64_t)(dd >> lg_dkm) * NT8 + r) * DKm + (dd & (DKm - 1));
+#pragma unroll 1
+        for (int c0 = 0; c0 < nw; c0 += kChunk * TPI) {
+          float2 mv[kChunk];
+          float4 bv[kChunk];
+#pragma unroll
+          for (int u = 0; u < kChunk; ++u) {
+            const int c = c0 + sub + u * TPI;
+            if (active && c < nw) {
+              mv[u] = mlr[c * NT8];
+              bv[u] = *reinterpret_cast<const float4 *>(src + (int64_t)c * slab);
+            } else {
+              mv[u] = make_float2(-INFINITY, 0.f);
+              bv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+          float cm = Ms[ri];
+#pragma unroll
+          for (int u = 0; u < kChunk; ++u) cm = fmaxf(cm, mv[u].x);
+#pragma unroll 1
+          for (int o = 1; o < TPI; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+          const float mu = cm == -INFINITY ? 0.f : cm;
+          const float sc = exp2_or_zero(Ms[ri], mu);
+          float lr = Ls[ri] * sc;
+          float4 a = As[ri];
+          a.x *= sc;
+          a.y *= sc;
+          a.z *= sc;
+          a.w *= sc;
+#pragma unroll
+          for (int u = 0; u < kChunk; ++u) {
+            const float w = exp2_or_zero(mv[u].x, mu);
+            lr += w * mv[u].y;
+            a.x += w * bv[u].x;
+            a.y += w * bv[u].y;
+            a.z += w * bv[u].z;
+            a.w += w * bv[u].w;
+          }
+          Ms[ri] = cm;
+          Ls[ri] = lr;
+          As[ri] = a;
+        }
+      }
+    }
+#pragma unroll
+    for (int ri = 0; ri < kMaxRounds; ++ri) {
+      if (ri >= rounds) break;
+      const int gi = ib + ri * blockDim.x + tid;
+      const int item = gi >> lgT, sub = gi & (TPI - 1);
+      const bool active = item < n_items;
+      float lr = Ls[ri];
+      float4 a = As[ri];
+#pragma unroll 1
+      for (int o = 1; o < TPI; o <<= 1) {
+        lr += __shfl_xor_sync(0xffffffffu, lr, o);
+        a.x += __shfl_xor_sync(0xffffffffu, a.x, o);
+        a.y += __shfl_xor_sync(0xffffffffu, a.y, o);
+        a.z += __shfl_xor_sync(0xffffffffu, a.z, o);
+        a.w += __shfl_xor_sync(0xffffffffu, a.w, o);
+      }
+      if (active && sub == 0) {
+        const int r = item >> lg_i, dd = (item & ((DK >> 2) - 1)) * 4;
+        const float inv = lr > 0.f ? 1.f / lr : 0.f;
+        const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
+        store4<BF16>(out_row(r) + mi * DK + dd, v);
+      }
+    }
+    }
     }
     if (tid == 0 && fin_old == K - 1) {
       // the last merger past its wait resets both counters: every merger
