@@ -92,9 +92,9 @@ def test_batched_uneven_segments(merge):
     case = W.make_case("uneven", seed=16, dtype=torch.bfloat16, head_size=128, num_q_heads=16,
                        num_kv_heads=2, page_size=16, max_query_len=3,
                        seq_lens=[3000, 200, 40, 0, 1, 1100, 600], layout=W.HND)
-    # 7 sequences x 2 kv heads x 10 segments = 140 CTAs: one wave, so the
-    # cooperative merge is allowed
-    _parity(case, opts=pd.options(segments=10, merge=merge))
+    # 7 sequences x 2 kv heads x 1 row group x 10 segments = 140 CTAs: one
+    # wave, so the cooperative merge is allowed
+    _parity(case, opts=pd.options(segments=10, merge=merge, row_groups=1))
 
 
 @pytest.mark.parametrize("kg,ns", [(1, 2), (1, 5), (2, 2), (2, 6), (3, 6), (4, 4)])
