@@ -232,9 +232,10 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   if (window > 0) nb_max = std::min<int64_t>(nb_max, cdiv(window + M - 1, kBlockKeys) + 1);
   const int64_t units = (int64_t)S * Hkv * rg;
   const int64_t target = o.max_ctas_hint > 0 ? o.max_ctas_hint : num_sms;
-  // a segment reads at least one stage per warp group, and at least four
-  // keys per packed row so its partial stays small next to the keys it read
-  const int64_t min_seg_blocks = std::max<int64_t>({4, (int64_t)TB * KG, 2LL * NT});
+  // a segment reads at least one and a half stages (~10 segments of 1k keys
+  // measured best at D=128: 9.9 -> 9.4 us), and at least four keys per
+  // packed row so its partial stays small next to the keys it read
+  const int64_t min_seg_blocks = std::max<int64_t>({4, (3LL * TB) / 2, 2LL * NT});
   int64_t nseg;
   if (o.segments > 0) {
     nseg = o.segments;
@@ -242,12 +243,13 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
     nseg = std::max<int64_t>(1, target / std::max<int64_t>(units, 1));
     nseg = std::min(nseg, std::max<int64_t>(1, nb_max / min_seg_blocks));
   } else {
-    // a batch: lengths are only known on the device; aim at ~2 waves of
+    // a batch: lengths are only known on the device; aim at ~1.5 waves of
     // equal segments assuming an average length of half the table width
-    // (fewer, longer segments measured faster than ~4 waves: 301 -> 289 us
-    // for 64 sequences of U[1, 16384] keys at D=256)
+    // (fewer, longer segments measured faster than ~4 waves: 300 -> 288 us
+    // for 64 sequences of U[1, 16384] keys at D=256; the last-arriver merge
+    // of a (sequence, kv head) then reads fewer parts)
     const int64_t est = std::max<int64_t>(1, units * nb_max / 2);
-    int64_t sb = std::max(min_seg_blocks, cdiv(est, 2 * target));
+    int64_t sb = std::max(min_seg_blocks, cdiv(2 * est, 3 * target));
     nseg = cdiv(nb_max, sb);
   }
   nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, nb_max));
