@@ -146,7 +146,9 @@ typedef struct pd_options {
   int key_groups;    /* warp groups of a CTA that take alternate KV tiles     */
   int stages;        /* shared-memory ring stages (32 KiB each)               */
   int cluster;       /* thread-block cluster size of the merge (1, 2, 4, 8)   */
-  int path;          /* 0 = auto, 1 = tensor-core (mma.sync), 2 = warp dot     */
+  int path;          /* 0 = auto (= 1), 1 = mma.sync, 2 = warp dot (not built:
+                        PD_EINVAL), 3 = tcgen05 MMAs with tensor memory
+                        (D <= 256, 16 packed rows per CTA)                     */
   int max_ctas_hint; /* CTAs the split aims for (0 = the SM count)            */
   int merge;         /* split-KV merge: 0 = auto, 1 = the last-arriving CTA,
                         2 = the last K arrivals of a co-resident (cooperative)
@@ -163,7 +165,7 @@ PD_API int paged_decode_attn_opts(const pd_tensor *q, const pd_tensor *k_cache, 
 /* The launch plan chosen for a call shape, computed on the host only (no
  * device access), for inspection and tests. */
 typedef struct pd_plan {
-  int path;          /* 1 = mma, 2 = dot                                       */
+  int path;          /* 1 = mma.sync, 3 = tcgen05 / tensor memory             */
   int merge;         /* 0 = none, 1 = last arriver, 2 = cooperative mergers    */
   int mergers;       /* K of the cooperative merge                             */
   int rows;          /* packed rows per kv head, G * M                         */

@@ -189,7 +189,12 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
     return PD_EINVAL;
   if (D != 64 && D != 128 && D != 256 && D != 512) return PD_EHEAD;
   if (M < 1 || M > 8) return PD_EQLEN;
-  if (o.path == 2) return PD_EINVAL;  // the warp-dot path is not part of this build
+  // path: 0 = auto (mma.sync), 1 = mma.sync, 3 = tcgen05 with tensor memory
+  // (D <= 256); the warp-dot path (2) is not part of this build
+  if (o.path < 0 || o.path > 3 || o.path == 2) return PD_EINVAL;
+  const bool tc = o.path == 3;
+  if (tc && D > 256) return PD_EINVAL;
+  if (tc && o.cluster > 1) return PD_EINVAL;
   const int G = Hq / Hkv, R = G * M;
   // One sequence: at most 16 packed rows per CTA.  Every n-tile warp of a
   // warp group reads the whole stage from shared memory, so more rows per
@@ -198,7 +203,8 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   // the same time (mostly L2 hits).  Measured at D=512, 64 rows, 32k keys:
   // 81 -> 52 us.  A batch runs several waves and is bound by HBM, where a
   // second read of the pages costs more than it saves: up to 64 rows.
-  const int64_t rows_max = S <= 1 ? 16 : 64;
+  // (the tensor-memory path takes 16 rows per CTA, four copies of them)
+  const int64_t rows_max = (S <= 1 || tc) ? 16 : 64;
   int rg = o.row_groups > 0
                ? o.row_groups
                : (int)std::min<int64_t>(kMaxRowGroups, std::max<int64_t>(1, cdiv(R, rows_max)));
@@ -207,25 +213,30 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   const int NT = (int)cdiv(rows_cta, 8);
   if (NT > kMaxConsumerWarps) return PD_EINVAL;
   const int TB = kStageBytes / 2 / (kBlockKeys * D * 2);
-  const int fixed = smem_bytes(D, NT, 0);
+  const int fixed = tc ? smem_bytes_tc(D, 0) : smem_bytes(D, NT, 0);
   const int ns_max = std::min(8, (kSmemLimit - fixed - 16 * 8) / kStageBytes);
+  // dead ring (+ Q and P tiles) available to the epilogue with NS stages
+  auto epi_bytes = [&](int ns) { return tc ? epilogue_bytes_tc(D, ns) : epilogue_bytes(D, NT, ns); };
   if (ns_max < 1) return PD_EINVAL;
   // warp groups take alternate stages; with >= 2 stages each, a group's next
   // stage loads while it computes on the current one (3 groups measured
   // fastest for up to 16 packed rows)
   int KG = o.key_groups > 0 ? o.key_groups : (NT <= 2 ? 3 : std::max(1, kMaxConsumerWarps / NT));
+  if (tc) KG = 4;  // four copies of the rows, each over a quarter of the keys
   int NS = 0;
   while (true) {
-    NS = o.stages > 0 ? o.stages : (ns_max / KG) * KG;
+    // (the tensor-memory path's copies share every stage: any count)
+    NS = o.stages > 0 ? o.stages : (tc ? ns_max : (ns_max / KG) * KG);
     // the warp groups' partials (KG copies of NT*8 x D fp32) must fit in the
     // dead ring at the end; fewer groups when they do not
     if (o.key_groups > 0 || KG == 1 || NS < 1 ||
-        epilogue_floats(D, NT, KG, 1, 1) * 4 <= epilogue_bytes(D, NT, NS))
+        epilogue_floats(D, NT, KG, 1, 1) * 4 <= epi_bytes(NS))
       break;
     KG /= 2;
   }
-  if (NT * KG > kMaxConsumerWarps) return PD_EINVAL;
-  if (NS < 1 || NS > ns_max || NS % KG != 0 || (NS < 2 && o.stages == 0)) return PD_EINVAL;
+  if (!tc && NT * KG > kMaxConsumerWarps) return PD_EINVAL;
+  if (NS < 1 || NS > ns_max || (!tc && NS % KG != 0) || (NS < 2 && o.stages == 0))
+    return PD_EINVAL;
 
   // KV blocks (16 keys) a (sequence, kv head, row group) can span at most.
   int64_t nb_max = cdiv((int64_t)bt_width * P, kBlockKeys);
@@ -259,11 +270,11 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   // (it pulls the parts a window at a time; K >= 2 mergers).
   const int64_t coop_floats = 16LL * NT + 8LL * NT * D / 2 + 64;
   const bool coop_possible = o.merge != 1 && (int64_t)S * Hkv * rg * nseg <= num_sms &&
-                             coop_floats * 4 <= epilogue_bytes(D, NT, NS);
+                             coop_floats * 4 <= epi_bytes(NS);
   // Clusters only in the one-wave regime (a batch runs several waves, where
   // the last-arriving CTA's merge overlaps other CTAs' work) and only when
   // the cooperative merge is not possible (it measured faster).
-  if (o.cluster == 0 && S <= 1 && nseg >= 8 && nseg * part_floats * 4 > (256 << 10) &&
+  if (o.cluster == 0 && !tc && S <= 1 && nseg >= 8 && nseg * part_floats * 4 > (256 << 10) &&
       !coop_possible)
     CS = 8;
   if (CS != 1 && CS != 2 && CS != 4 && CS != 8) return PD_EINVAL;
@@ -317,20 +328,20 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   }
   // The epilogue must fit in the ring + Q region.
   while (max_parts > 0 &&
-         epilogue_floats(D, NT, KG, CS, (int)max_parts) * 4 > epilogue_bytes(D, NT, NS)) {
+         epilogue_floats(D, NT, KG, CS, (int)max_parts) * 4 > epi_bytes(NS)) {
     if (o.segments > 0) return PD_EINVAL;
     max_parts = max_parts - 1;
     nseg = max_parts > 1 ? max_parts * CS : CS;
     if (max_parts <= 1) max_parts = 0;
   }
-  if (epilogue_floats(D, NT, KG, CS, 1) * 4 > epilogue_bytes(D, NT, NS)) return PD_EINVAL;
+  if (epilogue_floats(D, NT, KG, CS, 1) * 4 > epi_bytes(NS)) return PD_EINVAL;
   const int64_t seg_blocks = cdiv(nb_max, nseg);
   // Merge.  A grid that fits on the GPU at once (one CTA per SM) can be
   // launched cooperatively; then the last K arrivals of a group each merge
   // one D/K slice instead of the last arrival merging all of it alone.
   if (o.merge < 0 || o.merge > 2) return PD_EINVAL;
   const bool coop_ok = max_parts > 1 && CS == 1 && (int64_t)S * Hkv * rg * nseg <= num_sms &&
-                       coop_floats * 4 <= epilogue_bytes(D, NT, NS);
+                       coop_floats * 4 <= epi_bytes(NS);
   int merge = max_parts > 1 ? 1 : 0, mergers = 0;
   if (coop_ok && o.merge != 1) {
     merge = 2;
@@ -343,7 +354,7 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   }
   if ((int64_t)Hkv * rg * nseg > INT32_MAX || S > 65535) return PD_EINVAL;
 
-  plan->path = 1;
+  plan->path = tc ? 3 : 1;
   plan->merge = merge;
   plan->mergers = mergers;
   plan->rows = R;
@@ -358,8 +369,8 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   plan->max_parts = (int)max_parts;
   plan->grid_x = (int)(Hkv * rg * nseg);
   plan->grid_y = S;
-  plan->block_threads = 32 * (NT * KG + 1);
-  plan->smem_bytes = smem_bytes(D, NT, NS);
+  plan->block_threads = tc ? kTcThreads : 32 * (NT * KG + 1);
+  plan->smem_bytes = tc ? smem_bytes_tc(D, NS) : smem_bytes(D, NT, NS);
   plan->scratch_needed = max_parts > 0 ? partial_bytes(max_parts) : 0;
   return PD_OK;
 }
@@ -442,7 +453,8 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   p.status = dev.status;
   p.coop = plan.merge == 2 ? 1 : 0;
   p.mergers = plan.mergers > 0 ? plan.mergers : 1;
-  p.epi_floats = epilogue_bytes(head_size, plan.n_tiles, plan.stages) / 4;
+  p.epi_floats = (plan.path == 3 ? epilogue_bytes_tc(head_size, plan.stages)
+                                  : epilogue_bytes(head_size, plan.n_tiles, plan.stages)) / 4;
   if (plan.max_parts > 0) {
     char *base = static_cast<char *>(scratch->data);
     const int64_t cbytes = (scratch->counter_slots * 4 + 255) / 256 * 256;
@@ -460,7 +472,7 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   l.smem = plan.smem_bytes;
   l.cluster = plan.cluster;
   l.cooperative = plan.merge == 2 ? 1 : 0;
-  cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, tk, tv, p, l,
+  cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, plan.path == 3, tk, tv, p, l,
                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();

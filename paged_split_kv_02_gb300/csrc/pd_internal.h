@@ -15,6 +15,13 @@ constexpr int kMaxConsumerWarps = 8;  // warps that compute; one more loads
 constexpr int kMaxThreads = 32 * (kMaxConsumerWarps + 1);
 constexpr int kSmemAlign = 1024;      // the 128-byte TMA swizzle repeats every 1 KiB
 constexpr int kBlockIds = 512;        // page ids of 16-key blocks staged in shared memory
+// Tensor-memory path: 4 softmax warps (one per tensor-memory sub-partition)
+// and one warp that issues the tcgen05 MMAs, plus the producer warp; the
+// packed rows (<= 64) are the M = 64 side of every MMA.
+constexpr int kTcConsumerWarps = 5;
+constexpr int kTcThreads = 32 * (kTcConsumerWarps + 1);
+constexpr int kTcRows = 64;
+constexpr int kTcBarriers = 9;  // S full/free, P full, PV done (x2 each), all MMAs done
 
 // Everything a launch needs besides the two tensor maps.
 struct Params {
@@ -67,6 +74,30 @@ inline int64_t epilogue_bytes(int D, int NT, int NS) {
   return (int64_t)NS * kStageBytes + (int64_t)NT * D * 16;
 }
 
+// Tensor-memory path: keys per stage, bytes of one P tile (64 rows of
+// 128-byte swizzled rows per 64 keys), tensor-memory columns (two S buffers
+// and O, rounded up to a power of two).
+constexpr int tc_stage_keys(int D) { return kStageBytes / 2 / (kBlockKeys * D * 2) * kBlockKeys; }
+constexpr int tc_p_tile_bytes(int D) {
+  return kTcRows * (tc_stage_keys(D) > 64 ? tc_stage_keys(D) : 64) * 2;
+}
+constexpr int tc_tmem_cols(int D) {
+  return 2 * tc_stage_keys(D) + D <= 32    ? 32
+         : 2 * tc_stage_keys(D) + D <= 64  ? 64
+         : 2 * tc_stage_keys(D) + D <= 128 ? 128
+         : 2 * tc_stage_keys(D) + D <= 256 ? 256
+                                            : 512;
+}
+// Dynamic shared memory of a tensor-memory launch: ring + 64-row Q tile +
+// two P tiles + barriers + flags + staged page ids + tensor-memory address.
+inline int smem_bytes_tc(int D, int NS) {
+  return kSmemAlign + NS * kStageBytes + kTcRows * D * 2 + 2 * tc_p_tile_bytes(D) + 2 * NS * 8 +
+         kTcBarriers * 8 + 16 + 4 * kBlockIds + 16;
+}
+inline int64_t epilogue_bytes_tc(int D, int NS) {
+  return (int64_t)NS * kStageBytes + (int64_t)kTcRows * D * 2 + 2LL * tc_p_tile_bytes(D);
+}
+
 // Floats the epilogue needs: combine phase and final-merge phase.
 inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
   const int64_t nt8 = 8LL * NT;
@@ -79,7 +110,7 @@ inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
   return combine > final_merge ? combine : final_merge;
 }
 
-cudaError_t launch_mma(int D, bool bf16, const CUtensorMap &tk, const CUtensorMap &tv,
+cudaError_t launch_mma(int D, bool bf16, bool tc, const CUtensorMap &tk, const CUtensorMap &tv,
                        const Params &p, const Launch &l, cudaStream_t stream);
 
 unsigned int *device_status_ptr();

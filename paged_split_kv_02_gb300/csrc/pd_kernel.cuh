@@ -81,8 +81,8 @@ __device__ __forceinline__ float exp2_or_zero(float x, float m) {
   return x == -INFINITY ? 0.f : exp2f(x - m);
 }
 
-template <int D, bool BF16>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+template <int D, bool BF16, bool TC>
+__global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     pd_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ Params p) {
   using tag = std::integral_constant<bool, BF16>;
@@ -99,14 +99,26 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   // integer), so every pointer derived from it stays in the shared space
   unsigned char *smem =
       smem_raw + ((kSmemAlign - (smem_u32(smem_raw) & (kSmemAlign - 1))) & (kSmemAlign - 1));
-  const int NS = p.NS, NT = p.NT, KG = p.KG, NC = NT * KG;
+  // Tensor-memory path (TC): keys per stage, P tile bytes, TMEM columns.
+  constexpr int SC = TB * kBlockKeys;
+  constexpr int PTILE = tc_p_tile_bytes(D);
+  constexpr int TMEM_COLS = tc_tmem_cols(D);
+  const int NS = p.NS, NT = p.NT, KG = p.KG, NC = TC ? kTcConsumerWarps : NT * KG;
   const int NT8 = NT * 8;
+  const int NTQ = TC ? kTcRows / 8 : NT;  // 8-row groups of the Q tile
   unsigned char *ring = smem;
   unsigned char *qs = ring + NS * STAGE;
-  uint64_t *full = reinterpret_cast<uint64_t *>(qs + NT * D * 16);
+  unsigned char *pts = qs + NTQ * D * 16;  // TC: two P tiles
+  uint64_t *full = reinterpret_cast<uint64_t *>(pts + (TC ? 2 * PTILE : 0));
   uint64_t *empty = full + NS;
-  volatile int *flags = reinterpret_cast<volatile int *>(empty + NS);  // [0] abort, [1] last
-  uint64_t *mbar_merge = reinterpret_cast<uint64_t *>(empty + NS) + 1;   // flags[2..3]
+  // TC barriers: [0,1] S full, [2,3] S read, [4,5] P written, [6,7] PV done,
+  // [8] every MMA done
+  uint64_t *tcb = empty + NS;
+  uint64_t *fl64 = tcb + (TC ? kTcBarriers : 0);
+  volatile int *flags = reinterpret_cast<volatile int *>(fl64);  // [0] abort, [1] last
+  uint64_t *mbar_merge = fl64 + 1;                               // flags[2..3]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fl64) + 4 + kBlockIds;  // after the page ids
+  uint32_t tmem_base = 0;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = blockIdx.y;
@@ -120,7 +132,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(full + i), 1);
-      mbar_init(smem_u32(empty + i), NT);
+      mbar_init(smem_u32(empty + i), TC ? 1 : NT);  // TC: freed by the PV MMAs' commit
+    }
+    if constexpr (TC) {
+      for (int i = 0; i < kTcBarriers; ++i)
+        mbar_init(smem_u32(tcb + i), (i == 2 || i == 3 || i == 4 || i == 5) ? 4 : 1);
     }
     mbar_init(smem_u32(mbar_merge), 1);
     flags[0] = 0;
@@ -184,6 +200,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int my_b0 = b_first + seg * sb;
   const int my_nb = max(0, min(b_first + nb, my_b0 + sb) - my_b0);
   const int ntile = (my_nb + TB - 1) / TB;
+  if constexpr (TC) {
+    // tensor memory for the two S buffers and O; freed once the epilogue has
+    // read O (every path of the CTA reaches that point)
+    if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+  }
 
 
   // Consumer state (kept in registers across the main loop).
@@ -262,6 +287,230 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         if (!mbar_wait_bounded(smem_u32(full + j % NS), (j / NS) & 1)) atomicOr(p.status, 0x1u);
     }
   } else {
+    if constexpr (TC) {
+    // ================= tensor-memory consumers ============================
+    // The CTA's packed rows (<= 16) are copied four times into the 64 rows
+    // of the Q tile (row 16 q + r = packed row r), so the M = 64 MMAs give
+    // four copies of every score row, one per tensor-memory sub-partition
+    // (lanes 0-15).  Softmax warp q takes its copy and a quarter of every
+    // stage's keys, one row per thread (lanes < 16), and keeps its own
+    // running (m, l) and O rows: four independent online softmaxes over
+    // disjoint keys, merged in the epilogue like warp groups.  Warp 4
+    // issues the MMAs from one thread:
+    //   S[64 x stage keys] = Q[64 x D] . K^T   (one MMA per 16-key block and
+    //                                          16-dim step, K-major operands)
+    //   O[64 x D]         += P[64 x keys] . V  (one MMA per 16-key block, V
+    //                                          MN-major as the copies land)
+    // S has two tensor-memory buffers so the MMAs of stage j + 1 overlap
+    // the softmax of stage j; P has two shared-memory tiles (row 16 q + r
+    // holds copy q's keys only, the rest stays zero).  O is rescaled in
+    // tensor memory only when a stage's max exceeds a row's reference max by
+    // more than 8 (so P <= 2^8).
+    constexpr int KPC = SC / 4;  // keys of a stage per copy
+    {
+      // the Q tile: 64 rows = 4 copies of the 16 packed rows (others zero);
+      // both P tiles zeroed (each thread later writes its own keys only)
+      const T *qbase = static_cast<const T *>(p.q);
+      for (int idx = tid; idx < kTcRows * (D / 8); idx += NC * 32) {
+        const int r = idx / (D / 8), c = idx % (D / 8);
+        const int rp = r & 15, rr = rr0 + rp;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (rp < p.rows_cta && rr < p.R) {
+          const int i = rr / p.G, jq = rr % p.G;
+          v = __ldg(reinterpret_cast<const uint4 *>(qbase + (int64_t)(s * p.M + i) * p.q_s0 +
+                                                    (int64_t)(h * p.G + jq) * p.q_s1 + c * 8));
+        }
+        const int tn = r >> 3, rw = r & 7, box = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4 *>(qs + (tn * NBOX + box) * 1024 + rw * 128 + ((cc ^ rw) << 4)) = v;
+      }
+      for (int idx = tid; idx < 2 * PTILE / 16; idx += NC * 32)
+        reinterpret_cast<uint4 *>(pts)[idx] = make_uint4(0, 0, 0, 0);
+      fence_proxy_async_smem();  // the tensor core reads both tiles
+      asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
+    }
+    const uint32_t tS = tmem_base, tO = tmem_base + 2 * SC;
+    if (warp == kTcConsumerWarps - 1) {
+      if (lane == 0) {
+        // ---- MMA issue (one thread) ----
+        const uint32_t idS = umma_idesc_f16(kTcRows, kBlockKeys, BF16, 0, 0);
+        const uint32_t idO = umma_idesc_f16(kTcRows, D, BF16, 0, 1);
+        const uint32_t q_u = smem_u32(qs), p_u = smem_u32(pts), ring_u = smem_u32(ring);
+        const uint64_t dq = umma_desc_sw128(q_u, 16, NBOX * 1024);
+        bool ok = true;
+        for (int j = 0; j <= ntile; ++j) {
+          if (j < ntile) {
+            const int slot = j % NS;
+            ok = mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1);
+            if (ok && j >= 2) ok = mbar_wait_bounded(smem_u32(tcb + 2 + (j & 1)), ((j - 2) >> 1) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const int nbt = min(TB, my_nb - j * TB);
+            // descriptors of the stage's first K block; the start-address
+            // field (bits 0-13, 16-byte units) advances with the operand
+            const uint64_t dk = umma_desc_sw128(ring_u + slot * STAGE, 16, 1024);
+            for (int b = 0; b < nbt; ++b) {
+              const uint64_t dkb = dk + (uint64_t)(b * BLOCK_BYTES / 16);
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks)
+                umma_f16(tS + (j & 1) * SC + kBlockKeys * b,
+                         dq + (uint64_t)(((ks >> 2) * 1024 + (ks & 3) * 32) / 16),
+                         dkb + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) / 16), idS,
+                         ks > 0 ? 1u : 0u);
+            }
+            umma_commit(smem_u32(tcb + (j & 1)));  // S of stage j is ready
+          }
+          if (j >= 1) {
+            const int jj = j - 1, slot = jj % NS;
+            ok = mbar_wait_bounded(smem_u32(tcb + 4 + (jj & 1)), (jj >> 1) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const int nbt = min(TB, my_nb - jj * TB);
+            const uint64_t dv = umma_desc_sw128(ring_u + slot * STAGE + TB * BLOCK_BYTES, 2048, 1024);
+            const uint64_t dp = umma_desc_sw128(p_u + (jj & 1) * PTILE, 16, 1024);
+            for (int b = 0; b < nbt; ++b)
+              umma_f16(tO, dp + (uint64_t)(((b >> 2) * 8192 + (b & 3) * 32) / 16),
+                       dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (jj > 0 || b > 0) ? 1u : 0u);
+            umma_commit(smem_u32(empty + slot));       // the stage may be refilled
+            umma_commit(smem_u32(tcb + 6 + (jj & 1)));  // P tile jj & 1 is free, O is current
+          }
+        }
+        if (!ok) {
+          flags[0] = 1;
+          atomicOr(p.status, 0x1u);
+        }
+        umma_commit(smem_u32(tcb + 8));  // every MMA issued above has completed
+      }
+      __syncwarp();
+    } else {
+      // ---- softmax (warp q = copy q, keys [q KPC, (q + 1) KPC) of a stage) ----
+      const int r = lane & 15, prow = 16 * warp + r;  // packed row, P / MMA row
+      const bool live = lane < 16 && r < p.rows_cta && rr0 + r < p.R;
+      int lo = 0, hi = 0;
+      if (live) {
+        hi = max(L - p.M + (rr0 + r) / p.G + 1, 0);
+        lo = p.window ? max(0, hi - p.window) : 0;
+      }
+      const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+      const int c_first = KPC * warp;  // this copy's first key of a stage
+      float m_used = -INFINITY, lsum_all = 0.f;
+      for (int j = 0; j < ntile; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + (j & 1)), (j >> 1) & 1))) {
+          if (lane == 0) {
+            flags[0] = 1;
+            atomicOr(p.status, 0x1u);
+          }
+          break;
+        }
+        tc_fence_after();
+        float sv[KPC];
+#pragma unroll
+        for (int c0 = 0; c0 < KPC; c0 += 8) {
+          uint32_t rr[8];
+          tmem_ld8(tS + lane_base + (j & 1) * SC + c_first + c0, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) sv[c0 + i] = __uint_as_float(rr[i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(tcb + 2 + (j & 1)));  // S buffer read
+        const int nbt = min(TB, my_nb - j * TB);
+        const int key_t0 = (my_b0 + j * TB) * kBlockKeys;
+        const int slot = j % NS;
+        const bool fast = nbt == TB && key_t0 >= v_lo && key_t0 + SC <= v_hi;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < KPC; ++c) {
+          float x = sv[c] * p.scale_log2;
+          const int cs = c_first + c, k = key_t0 + cs;
+          if (!live || (!fast && !(cs < nbt * kBlockKeys && k >= lo && k < hi))) x = -INFINITY;
+          sv[c] = x;
+          mx = fmaxf(mx, x);
+        }
+        const float m_new = fmaxf(m_used, mx);
+        const bool need = m_used != -INFINITY && m_new > m_used + 8.f;
+        bool ok = true;
+        if (__any_sync(0xffffffffu, need)) {
+          // O must be current: the PV MMAs of stage j - 1 have completed
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_bounded(smem_u32(tcb + 6 + ((j - 1) & 1)), ((j - 1) >> 1) & 1));
+          if (ok) {
+            tc_fence_after();
+            const float alpha = need ? exp2f(m_used - m_new) : 1.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32(tO + lane_base + c0, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + lane_base + c0, o);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            if (need) {
+              lsum_all *= alpha;
+              m_used = m_new;
+            }
+          }
+        }
+        if (m_used == -INFINITY) m_used = m_new;
+        // P tile j & 1 is free once the PV MMAs of stage j - 2 have completed
+        if (ok && j >= 2)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_bounded(smem_u32(tcb + 6 + (j & 1)), ((j - 2) >> 1) & 1));
+        if (!ok) {
+          if (lane == 0) {
+            flags[0] = 1;
+            atomicOr(p.status, 0x1u);
+          }
+          break;
+        }
+        {
+          const float mu = m_used == -INFINITY ? 0.f : m_used;
+          unsigned char *pt = pts + (j & 1) * PTILE;
+          float ls = 0.f;
+#pragma unroll
+          for (int u = 0; u < KPC / 8; ++u) {
+            float pv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              pv[e] = exp2_or_zero(sv[8 * u + e], mu);
+              ls += pv[e];
+            }
+            uint4 w;
+            w.x = pack2(pv[0], pv[1], tag{});
+            w.y = pack2(pv[2], pv[3], tag{});
+            w.z = pack2(pv[4], pv[5], tag{});
+            w.w = pack2(pv[6], pv[7], tag{});
+            const int key = c_first + 8 * u;           // first key of the 16-byte unit
+            const int kc = key >> 6, uu = (key >> 3) & 7;  // 64-key chunk, unit of the row
+            if (lane < 16)
+              *reinterpret_cast<uint4 *>(pt + kc * 8192 + prow * 128 + ((uu ^ (prow & 7)) << 4)) = w;
+          }
+          lsum_all += ls;
+        }
+        // zero V of keys no row sees (outside the union, stale or NaN slots)
+        if (!(nbt == TB && key_t0 >= u_lo && key_t0 + SC <= u_hi)) {
+          unsigned char *vb = ring + slot * STAGE + TB * BLOCK_BYTES;
+          for (int c = 32 * warp + lane; c < nbt * kBlockKeys; c += 128) {
+            const int k = key_t0 + c;
+            if (k < u_lo || k >= u_hi) {
+#pragma unroll 1
+              for (int x = 0; x < NBOX * 8; ++x)
+                *reinterpret_cast<uint4 *>(vb + (c >> 4) * BLOCK_BYTES + (x >> 3) * 2048 +
+                                           (c & 15) * 128 + (x & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+        fence_proxy_async_smem();  // P and the zeroed V reach the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(tcb + 4 + (j & 1)));  // P of stage j written
+      }
+      m0 = m_used;
+      l0 = lsum_all;
+    }
+    } else {
     // ================= consumers ==========================================
     // Visible key range of this thread's two rows (empty for padding rows).
     int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
@@ -461,6 +710,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
+    }
   }
 
   // ================= epilogue ==============================================
@@ -492,7 +742,41 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int64_t gbase = (int64_t)group * p.max_parts;
   const int64_t slice_floats = (int64_t)NT8 * DS;
 
-  if (warp < NC && lane < 4) {
+  if constexpr (TC) {
+    // O (tensor memory) -> the CTA's partial in shared memory (one warp group,
+    // KG = 1), one row per thread, once every MMA has completed
+    if (warp < kTcConsumerWarps - 1) {
+      const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8), 0));
+      tc_fence_after();
+      // copy q = warp q is warp group q of the partial pass (KG = 4)
+      const int r = lane & 15;
+      const bool keep = lane < 16 && r < NT8;
+      const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+      float *dst = cp + ((size_t)warp * NT8 + r) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem_base + 2 * SC + lane_base + c0, o);
+        tmem_wait_ld();
+        if (keep) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 v = (ntile > 0 && done)
+                                 ? make_float4(__uint_as_float(o[i]), __uint_as_float(o[i + 1]),
+                                               __uint_as_float(o[i + 2]), __uint_as_float(o[i + 3]))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4 *>(dst + psw(c0 + i, r)) = v;
+          }
+        }
+      }
+      if (keep) {
+        mrow[warp * NT8 + r] = (ntile > 0 && done) ? m0 : -INFINITY;
+        lrow[warp * NT8 + r] = (ntile > 0 && done) ? l0 : 0.f;
+      }
+      if (!done && lane == 0) atomicOr(p.status, 0x1u);
+    }
+    tc_fence_before();
+  } else if (warp < NC && lane < 4) {
     mrow[g_k * NT8 + r0] = m0;
     mrow[g_k * NT8 + r1] = m1;
     lrow[g_k * NT8 + r0] = l0;
@@ -505,7 +789,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     // stores from the pass that forms every (row, 4 columns) item of the
     // CTA's partial: sum over the groups of acc_g * exp2(m_g - m*), then
     // normalised (one segment) or published (several).
-    if (warp < NC) {
+    if (!TC && warp < NC) {
       float *dst = cp + (size_t)g_k * NT8 * D;
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
@@ -517,6 +801,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
     }
     __syncthreads();
+    if constexpr (TC) {
+      // every read of tensor memory is done
+      if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+      }
+    }
     const int DKm = p.coop ? D / p.mergers : D;
     const int lg_dkm = __ffs(DKm) - 1;
     float *pa = p.part_acc + (gbase + cl_id) * (int64_t)NT8 * D;
@@ -597,7 +888,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (nseg == 1) return;
   } else {
   __syncthreads();
-  if (warp < NC) {
+  if constexpr (TC) {
+    // (clusters are not planned on the tensor-memory path; free it anyway)
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+  }
+  if (!TC && warp < NC) {
     float ms0 = -INFINITY, ms1 = -INFINITY;
 #pragma unroll 1
     for (int gg = 0; gg < KG; ++gg) {
@@ -1161,10 +1459,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool TC>
 cudaError_t launch_mma_t(const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
                          const Launch &l, cudaStream_t stream) {
-  auto kern = pd_decode_mma<D, BF16>;
+  auto kern = pd_decode_mma<D, BF16, TC>;
   // largest dynamic shared memory opted into so far, per device
   static int configured_smem[64] = {};
   int dev = 0;

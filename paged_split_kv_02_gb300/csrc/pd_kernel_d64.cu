@@ -3,10 +3,13 @@
 
 namespace pd {
 
-cudaError_t launch_mma_d64(bool bf16, const CUtensorMap &tk, const CUtensorMap &tv,
+cudaError_t launch_mma_d64(bool bf16, bool tc, const CUtensorMap &tk, const CUtensorMap &tv,
                            const Params &p, const Launch &l, cudaStream_t stream) {
-  return bf16 ? launch_mma_t<64, true>(tk, tv, p, l, stream)
-              : launch_mma_t<64, false>(tk, tv, p, l, stream);
+  if (tc)
+    return bf16 ? launch_mma_t<64, true, true>(tk, tv, p, l, stream)
+                : launch_mma_t<64, false, true>(tk, tv, p, l, stream);
+  return bf16 ? launch_mma_t<64, true, false>(tk, tv, p, l, stream)
+              : launch_mma_t<64, false, false>(tk, tv, p, l, stream);
 }
 
 }  // namespace pd

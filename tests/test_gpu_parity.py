@@ -171,3 +171,39 @@ def test_negative_control_detects_a_wrong_scale():
     out = run(g, scratch=scratch_for(case))
     with pytest.raises(AssertionError):
         check(case, out)
+
+
+@pytest.mark.parametrize("M,L,D,layout,dtype,window,seqs", [
+    (1, 40, 128, W.HND, torch.bfloat16, 0, None),
+    (4, 300, 128, W.HND, torch.bfloat16, 0, None),
+    (4, 4100, 128, W.HND, torch.bfloat16, 0, None),
+    (2, 1037, 128, W.NHD, torch.float16, 0, None),
+    (3, 2048, 64, W.HND, torch.float16, 300, None),
+    (4, 2000, 256, W.HND, torch.float16, 512, None),
+    (2, 700, 256, W.NHD, torch.bfloat16, 0, None),
+    (3, 0, 128, W.HND, torch.bfloat16, 0, [900, 0, 17, 2500, 1]),
+])
+def test_tensor_memory_path(M, L, D, layout, dtype, window, seqs):
+    """The tcgen05 / tensor-memory consumer (path 3) against the oracle."""
+    case = W.make_case("tensor_memory", seed=60 + M, dtype=dtype, head_size=D, num_q_heads=16,
+                       num_kv_heads=4, page_size=16, max_query_len=M,
+                       seq_lens=seqs if seqs else [L], layout=layout, window=window,
+                       window_pages_only=bool(window))
+    _parity(case, opts=pd.options(path=3))
+
+
+@pytest.mark.parametrize("seg,merge", [(1, 0), (5, 1), (19, 2), (16, 1)])
+def test_tensor_memory_path_splits(seg, merge):
+    case = W.spec_decode_hnd(4, 8192, seed=70)
+    _parity(case, opts=pd.options(path=3, segments=seg, merge=merge))
+
+
+def test_tensor_memory_path_refused_for_d512():
+    case = W.make_case("tm_d512", seed=71, dtype=torch.float16, head_size=512, num_q_heads=8,
+                       num_kv_heads=1, page_size=16, max_query_len=1, seq_lens=[100], layout=W.HND)
+    g = case.to("cuda")
+    rc = pd.paged_decode_attn(g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens,
+                              torch.empty_like(g.q), g.num_q_heads, g.num_kv_heads,
+                              g.head_size, g.page_size, g.max_query_len, g.window, g.scale,
+                              g.layout, scratch_for(case), opts=pd.options(path=3), check=False)
+    assert rc == -1
