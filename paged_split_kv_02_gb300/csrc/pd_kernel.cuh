@@ -76,6 +76,14 @@ __device__ __forceinline__ void store4(void *dst, const float (&v)[4]) {
   *reinterpret_cast<uint2 *>(dst) = w;
 }
 
+// 2^x by the SFU (ex2.approx.ftz: relative error ~2^-22, -inf -> +0); the
+// main-loop probabilities are rounded to 16 bits right after.
+__device__ __forceinline__ float sfu_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float exp2_or_zero(float x, float m) {
   // e^(x - m) in exp2 form; 0 for an empty row (x = -inf)
   return x == -INFINITY ? 0.f : exp2f(x - m);
@@ -475,7 +483,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
             float pv[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              pv[e] = exp2_or_zero(sv[8 * u + e], mu);
+              pv[e] = sfu_exp2(sv[8 * u + e] - mu);
               ls += pv[e];
             }
             uint4 w;
@@ -648,7 +656,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
       const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
       const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = exp2_or_zero(m0, mu0), al1 = exp2_or_zero(m1, mu1);
+      const float al0 = sfu_exp2(m0 - mu0), al1 = sfu_exp2(m1 - mu1);  // m = -inf -> 0
       m0 = mn0;
       m1 = mn1;
       if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
@@ -667,8 +675,8 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
 #pragma unroll
       for (int b = 0; b < TB; ++b) {
         if (b < nbt) {
-          const float p0 = exp2_or_zero(sc[b][0], mu0), p1 = exp2_or_zero(sc[b][1], mu1);
-          const float p2 = exp2_or_zero(sc[b][2], mu0), p3 = exp2_or_zero(sc[b][3], mu1);
+          const float p0 = sfu_exp2(sc[b][0] - mu0), p1 = sfu_exp2(sc[b][1] - mu1);
+          const float p2 = sfu_exp2(sc[b][2] - mu0), p3 = sfu_exp2(sc[b][3] - mu1);
           l0 += p0 + p2;
           l1 += p1 + p3;
           const uint32_t pb0 = movmatrix_trans(pack2(p0, p1, tag{}));
