@@ -207,3 +207,12 @@ def test_tensor_memory_path_refused_for_d512():
                               g.head_size, g.page_size, g.max_query_len, g.window, g.scale,
                               g.layout, scratch_for(case), opts=pd.options(path=3), check=False)
     assert rc == -1
+
+
+@pytest.mark.parametrize("scale", [-0.09, 0.0, 0.3])
+def test_scales_of_any_sign(scale):
+    """The scale is as passed: zero (uniform weights), negative, or larger."""
+    case = W.make_case("scales", seed=80, dtype=torch.bfloat16, head_size=128, num_q_heads=16,
+                       num_kv_heads=4, page_size=16, max_query_len=3, seq_lens=[1500, 40],
+                       layout=W.HND, scale=scale)
+    _parity(case)
