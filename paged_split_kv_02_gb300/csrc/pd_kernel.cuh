@@ -85,8 +85,9 @@ __device__ __forceinline__ float sfu_exp2(float x) {
 }
 
 __device__ __forceinline__ float exp2_or_zero(float x, float m) {
-  // e^(x - m) in exp2 form; 0 for an empty row (x = -inf)
-  return x == -INFINITY ? 0.f : exp2f(x - m);
+  // e^(x - m) in exp2 form; 0 for an empty row (x = -inf; m is always
+  // finite here: 0 stands in for the max of an empty row)
+  return sfu_exp2(x - m);
 }
 
 template <int D, bool BF16, bool TC>
@@ -444,7 +445,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
                           mbar_wait_bounded(smem_u32(tcb + 6 + ((j - 1) & 1)), ((j - 1) >> 1) & 1));
           if (ok) {
             tc_fence_after();
-            const float alpha = need ? exp2f(m_used - m_new) : 1.f;
+            const float alpha = need ? sfu_exp2(m_used - m_new) : 1.f;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t o[32];
