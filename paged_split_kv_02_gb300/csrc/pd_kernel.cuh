@@ -84,6 +84,13 @@ __device__ __forceinline__ float sfu_exp2(float x) {
   return y;
 }
 
+// 1/x by the SFU (rcp.approx.ftz: ~1 ulp) for the output normalisation
+__device__ __forceinline__ float sfu_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float exp2_or_zero(float x, float m) {
   // e^(x - m) in exp2 form; 0 for an empty row (x = -inf; m is always
   // finite here: 0 stands in for the max of an empty row)
@@ -827,7 +834,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     constexpr int kCols = decltype(cols)::value, kItemsPerRow = D / kCols;
 #pragma unroll 1
     for (int idx = tid; idx < nrows * kItemsPerRow; idx += blockDim.x) {
-      const int r = idx / kItemsPerRow, d16 = (idx % kItemsPerRow) * kCols;
+      // the item's 4-column groups are kItemsPerRow groups apart, so the
+      // threads of a row read consecutive 16-byte words (no bank conflicts)
+      const int r = idx / kItemsPerRow, t4 = (idx % kItemsPerRow) * 4;
+      constexpr int kStride = 4 * kItemsPerRow;
       float ms = -INFINITY;
 #pragma unroll
       for (int gg = 0; gg < kMaxConsumerWarps; ++gg)
@@ -851,7 +861,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
 #pragma unroll
             for (int v = 0; v < kCols / 4; ++v)
               b[u][v] = *reinterpret_cast<const float4 *>(cp + ((size_t)gg * NT8 + r) * D +
-                                                          psw(d16 + 4 * v, r));
+                                                          psw(t4 + kStride * v, r));
           } else {
             mg[u] = -INFINITY;
             lg[u] = 0.f;
@@ -873,20 +883,20 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         }
       }
       if (nseg == 1) {
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const float inv = lsum > 0.f ? sfu_rcp(lsum) : 0.f;
 #pragma unroll
         for (int v = 0; v < kCols / 4; ++v) {
           const float o[4] = {a[v].x * inv, a[v].y * inv, a[v].z * inv, a[v].w * inv};
-          store4<BF16>(out_row(r) + d16 + 4 * v, o);
+          store4<BF16>(out_row(r) + t4 + kStride * v, o);
         }
       } else {
         // DKm is a power of two (>= 4)
 #pragma unroll
         for (int v = 0; v < kCols / 4; ++v) {
-          const int d4 = d16 + 4 * v, k = d4 >> lg_dkm, dk = d4 & (DKm - 1);
+          const int d4 = t4 + kStride * v, k = d4 >> lg_dkm, dk = d4 & (DKm - 1);
           __stcg(reinterpret_cast<float4 *>(pa + ((int64_t)k * NT8 + r) * DKm + dk), a[v]);
         }
-        if (d16 == 0) __stcg(pm + r, make_float2(ms, lsum));
+        if (t4 == 0) __stcg(pm + r, make_float2(ms, lsum));
       }
     }
     };
@@ -959,7 +969,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     for (int idx = tid; idx < nrows * (D / 8); idx += blockDim.x) {
       const int r = idx / (D / 8), c8 = (idx % (D / 8)) * 8;
       const float lr = lfin[r];
-      const float inv = lr > 0.f ? 1.f / lr : 0.f;
+      const float inv = lr > 0.f ? sfu_rcp(lr) : 0.f;
       const float4 a = *reinterpret_cast<const float4 *>(cp + r * D + psw(c8, r));
       const float4 b = *reinterpret_cast<const float4 *>(cp + r * D + psw(c8 + 4, r));
       const float v[8] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv,
@@ -1027,7 +1037,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     for (int idx = tid; idx < nrows * (DS / 8); idx += blockDim.x) {
       const int r = idx / (DS / 8), c8 = (idx % (DS / 8)) * 8;
       const float lr = lcl[r];
-      const float inv = lr > 0.f ? 1.f / lr : 0.f;
+      const float inv = lr > 0.f ? sfu_rcp(lr) : 0.f;
       const float4 a = part4(r, c8), b = part4(r, c8 + 4);
       const float v[8] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv,
                           b.x * inv, b.y * inv, b.z * inv, b.w * inv};
@@ -1204,7 +1214,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         a.w += __shfl_xor_sync(0xffffffffu, a.w, o);
       }
       if (active && sub == 0) {
-        const float inv = lr > 0.f ? 1.f / lr : 0.f;
+        const float inv = lr > 0.f ? sfu_rcp(lr) : 0.f;
         const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
         store4<BF16>(out_row(r) + mi * DK + dd, v);
       }
@@ -1334,7 +1344,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
       }
       if (active && sub == 0) {
         const int r = item >> lg_i, dd = (item & ((DK >> 2) - 1)) * 4;
-        const float inv = lr > 0.f ? 1.f / lr : 0.f;
+        const float inv = lr > 0.f ? sfu_rcp(lr) : 0.f;
         const float v[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
         store4<BF16>(out_row(r) + mi * DK + dd, v);
       }
@@ -1460,7 +1470,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
       if (it < nitems) {
         const int rl = it / (DS / 4), d4 = (it % (DS / 4)) * 4;
         const float lr = lall[rc0 + rl];
-        const float inv = lr > 0.f ? 1.f / lr : 0.f;
+        const float inv = lr > 0.f ? sfu_rcp(lr) : 0.f;
         const float v[4] = {a[k].x * inv, a[k].y * inv, a[k].z * inv, a[k].w * inv};
         store4<BF16>(out_row(rc0 + rl) + (int)rank * DS + d4, v);
       }
