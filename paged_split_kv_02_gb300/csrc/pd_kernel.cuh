@@ -1091,13 +1091,14 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     // K = the largest power of two <= min(K_max, arrivals of this group).
     int K = 1;
     while (2 * K <= min(p.mergers, ncl)) K *= 2;
-    if (tid == 0) flags[1] = atomic_add_acq_rel_gpu(p.counters + 2 * group, 1) - (ncl - K);
-    __syncthreads();
-    const int mi = flags[1];
-    if (mi < 0) return;  // not one of the last K arrivals
+    // Thread 0 counts the CTA in; a merger that is not the last arrival
+    // waits there for the rest (the last one knows from the count that
+    // every part is published, and its acquire already covers them).
     if (tid == 0) {
+      const int old = atomic_add_acq_rel_gpu(p.counters + 2 * group, 1);
+      const int m = old - (ncl - K);
       int ok = 1;
-      if (ld_acquire_gpu(p.counters + 2 * group) < ncl) {
+      if (m >= 0 && old != ncl - 1 && ld_acquire_gpu(p.counters + 2 * group) < ncl) {
         const unsigned long long t0 = global_timer_ns();
         while (ld_acquire_gpu(p.counters + 2 * group) < ncl) {
           __nanosleep(64);
@@ -1108,9 +1109,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
           }
         }
       }
+      flags[1] = m;
       flags[2] = ok;
     }
     __syncthreads();
+    const int mi = flags[1];
+    if (mi < 0) return;  // not one of the last K arrivals
     if (!flags[2]) return;
     // count this merger past its wait now; the answer is needed only at the
     // end, so the round trip overlaps the merge
