@@ -165,3 +165,26 @@ def test_argument_checks_on_host():
     # a well-formed call on a machine without an sm_103 device
     if not torch.cuda.is_available():
         assert _call(c) == -8
+
+
+def test_plan_tensor_memory_path():
+    """path 3: 4 softmax warps + 1 MMA warp + the producer, 16 packed rows
+    per CTA (four copies fill the M = 64 side), four partial states."""
+    sd = _fake_scratch(1, 32, 8, 128, 4, 64)
+    p = pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 2048, 152, scratch_desc=sd,
+                             opts=pd.options(path=3))
+    assert p["path"] == 3 and p["block_threads"] == 192 and p["key_groups"] == 4
+    assert p["rows_per_cta"] <= 16 and p["cluster"] == 1
+    wide = _fake_scratch(1, 64, 8, 128, 8, 64)   # 64 packed rows -> 4 row groups
+    p = pd.paged_decode_plan(1, 64, 8, 128, 16, 8, 0, 256, 152, scratch_desc=wide,
+                             opts=pd.options(path=3))
+    assert p["row_groups"] == 4 and p["rows_per_cta"] == 16
+    assert pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 2048, 152,
+                                scratch_desc=sd)["path"] == 1  # the default is mma.sync
+    with pytest.raises(pd.PagedDecodeError):   # D = 512 does not fit tensor memory
+        pd.paged_decode_plan(1, 8, 1, 512, 16, 1, 0, 64, 152, opts=pd.options(path=3))
+    with pytest.raises(pd.PagedDecodeError):   # no clusters on this path
+        pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 256, 152, scratch_desc=sd,
+                             opts=pd.options(path=3, cluster=2, segments=4))
+    with pytest.raises(pd.PagedDecodeError):   # the dot path is not built
+        pd.paged_decode_plan(1, 32, 8, 128, 16, 1, 0, 256, 152, opts=pd.options(path=2))
