@@ -23,7 +23,7 @@
  * keys of one (sequence, kv head, row group) are cut into segments, one CTA
  * each; each writes unnormalised partials (acc, m, l) to the caller's
  * scratch, and the CTA that arrives last at a per-group counter merges them
- * and resets the counter to 0, so "every launch leaves them zeroed".
+ * and resets the counter to 0: the counters start every launch at zero.
  *
  * Threading and streams: every call is asynchronous on `stream`, performs
  * no host synchronisation and allocates nothing (no cudaMalloc, no host
@@ -111,8 +111,9 @@ PD_API size_t paged_decode_scratch_bytes(int max_num_seqs, int num_q_heads, int 
                                   int head_size, int max_query_len, int max_splits);
 
 /* Prepare a scratch buffer: record its counter area and zero the counters
- * once, asynchronously on `stream` (make_scratch: "Zeroed once; every launch
- * leaves them zeroed").  `data` must stay allocated while calls use it.
+ * once, asynchronously on `stream` (as the RDNA backend's make_scratch does:
+ * the calls leave them at zero afterwards).  `data` must stay allocated
+ * while calls use it.
  * Call it outside graph capture. */
 PD_API int paged_decode_scratch_init(pd_scratch *scratch, void *data, size_t bytes, int max_num_seqs,
                               int num_kv_heads, void *stream);

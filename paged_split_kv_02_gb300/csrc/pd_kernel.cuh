@@ -1,9 +1,9 @@
-// Paged split-KV decode attention on sm_103a, tensor-core path.
+// Paged split-KV decode attention on sm_103a.
 //
-// One CTA per (kv head, row group, KV segment), one sequence per grid.y
-// (the work unit of the gfx1151 decode kernel: "one workgroup per (kv head,
-// row group, KV segment), packing every query row of a kv head so its KV is
-// read once"; batched decode takes "one sequence per grid.y").
+// One CTA per (kv head, row group, KV segment), one sequence per grid.y: the
+// work unit of the gfx1151 decode kernel (ROCm/vllm PR #1330, "Kernel"),
+// where all the query rows of a kv head share a CTA so that its K and V are
+// read from memory once, and a batch puts one sequence on each grid row.
 //
 // Warp roles
 //   * one producer warp: per 32 KiB ring stage, TMA-loads the K and V
@@ -22,15 +22,19 @@
 //   O^T[D x 8] += V^T[D x 16 keys] . P^T[16 x 8]           (mma m16n8k16)
 // with V^T read by ldmatrix.trans from the same swizzled stage.
 //
-// Epilogue: the KG warp groups merge their (acc, m, l) in shared memory.  A
-// sequence cut into several segments then combines the segments of one
-// thread-block cluster through distributed shared memory (each CTA one
-// slice of the head dim), writes the cluster's partial to scratch and
-// increments a per-(sequence, kv head, row group) counter; the cluster that
-// arrives last merges every cluster partial and resets the counter to 0
-// (split-KV with an in-kernel merge; the counters of make_scratch are
-// "zeroed once; every launch leaves them zeroed").  With a cluster size of 1
-// this is the plain last-arriving-CTA merge.
+// A second consumer (TC = true) runs the products on the 5th-generation
+// tensor cores instead: tcgen05 MMAs issued by one thread, accumulators in
+// tensor memory, four softmax warps (see the TC branch below).
+//
+// Epilogue: the warp groups' (acc, m, l) are combined in shared memory into
+// the CTA's partial.  A sequence cut into several segments publishes the
+// partials to scratch and counts arrivals per (sequence, kv head, row group);
+// in a grid that fits on the GPU at once the last K arrivals merge one slice
+// of the head dim each (cooperative launch), otherwise the last arrival
+// merges alone (or, with a thread-block cluster, after a combine through
+// distributed shared memory).  The mergers reset the counters, so every
+// launch starts them at zero (split-KV with an in-kernel merge, as in the
+// vLLM RDNA backend's make_scratch).
 #pragma once
 
 #include <cuda_bf16.h>
