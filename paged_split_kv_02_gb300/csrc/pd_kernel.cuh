@@ -169,41 +169,54 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   }
   __syncthreads();
 
+  // ---- index arithmetic that reads no global memory, done before the wait
+  // so that only loads and a few compares lie between the wait and the
+  // first page copy ----
+  const int rr0 = grow * p.rows_cta;
+  const int rr1 = min(p.R, rr0 + p.rows_cta);
+  const int tok0 = rr0 / p.G, tok1 = (rr1 - 1) / p.G;  // tokens of the first and last row
+  const int cl_id = seg / p.CS;
+  const int bpp = p.P / kBlockKeys;  // 16-key blocks per page
+  const int lg_bpp = (bpp & (bpp - 1)) == 0 ? __ffs(bpp) - 1 : -1;
+  const int seg_cover = p.max_seg * p.seg_blocks;  // blocks the plan's segments cover
+  // Speculative page ids: without a window, segment `seg` starts at block
+  // seg * seg_blocks whenever the sequence fits the plan; the producer reads
+  // those block-table entries while seq_lens is still in flight.
+  constexpr int kSpec = 256;
+  int spec[kSpec / 32];  // block-table column of each block, then its page id
+  const int spec_b0 = seg * p.seg_blocks;
+  const int32_t *bt_row = p.block_table + (int64_t)s * p.bt_stride;
+  const int bt_blocks = p.bt_width * bpp;
+  const bool spec_on = warp == NC && p.window == 0;
+  if (spec_on) {
+#pragma unroll
+    for (int k = 0; k < kSpec / 32; ++k) {
+      const int i = lane + 32 * k, b = spec_b0 + i;
+      spec[k] = (i < p.seg_blocks && b < bt_blocks) ? (lg_bpp >= 0 ? b >> lg_bpp : b / bpp) : -1;
+    }
+  }
+
   // Launched with programmatic stream serialisation: wait here until the
   // previous grid on the stream (which may have written q, the caches, the
   // block table or the scratch) has completed, before reading any of them.
   grid_dependency_wait();
 
-  // ---- speculative page ids ----------------------------------------------
-  // Without a window, segment `seg` starts at block seg * seg_blocks whenever
-  // the sequence fits the plan; the producer reads those block-table entries
-  // while seq_lens is still in flight.
-  constexpr int kSpec = 256;
-  int spec[kSpec / 32];
-  const int spec_b0 = seg * p.seg_blocks;
-  const int32_t *bt_row = p.block_table + (int64_t)s * p.bt_stride;
-  const int bt_blocks = p.bt_width * (p.P / kBlockKeys);
-  if (warp == NC && p.window == 0) {
+  int L = __ldg(p.seq_lens + s);
+  if (spec_on) {
 #pragma unroll
-    for (int k = 0; k < kSpec / 32; ++k) {
-      const int i = lane + 32 * k, b = spec_b0 + i;
-      spec[k] = (i < p.seg_blocks && b < bt_blocks) ? __ldg(bt_row + b / (p.P / kBlockKeys)) : 0;
-    }
+    for (int k = 0; k < kSpec / 32; ++k) spec[k] = spec[k] >= 0 ? __ldg(bt_row + spec[k]) : 0;
   }
 
   // ---- key ranges --------------------------------------------------------
-  int L = __ldg(p.seq_lens + s);
   if (L < 0) L = 0;
   if (L > p.bt_width * p.P) {
     if (tid == 0 && seg == 0) atomicOr(p.status, 0x4u);
     L = p.bt_width * p.P;
   }
-  const int rr0 = grow * p.rows_cta;
-  const int rr1 = min(p.R, rr0 + p.rows_cta);
   int u_lo = 0, u_hi = 0, v_lo = 0, v_hi = 0;  // union / intersection of the rows' key ranges
   if (rr1 > rr0) {
-    const int n0 = max(L - p.M + rr0 / p.G + 1, 0);
-    const int n1 = max(L - p.M + (rr1 - 1) / p.G + 1, 0);
+    const int n0 = max(L - p.M + tok0 + 1, 0);
+    const int n1 = max(L - p.M + tok1 + 1, 0);
     u_hi = n1;
     v_hi = n0;
     u_lo = p.window ? max(0, n0 - p.window) : 0;
@@ -211,15 +224,16 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   }
   const int b_first = u_lo / kBlockKeys;
   const int nb = u_hi > u_lo ? (u_hi + kBlockKeys - 1) / kBlockKeys - b_first : 0;
-  const int sb = max(p.seg_blocks, (nb + p.max_seg - 1) / p.max_seg);
-  const int nseg = max(1, (nb + sb - 1) / sb);
-  const int ncl = (nseg + p.CS - 1) / p.CS;
-  const int cl_id = seg / p.CS;
-  if (cl_id >= ncl) return;         // uniform over the cluster
-  if (nseg == 1 && seg > 0) return;  // no merge: only segment 0 works
+  // blocks per segment: the plan's, unless the sequence is longer than planned
+  const int sb = nb <= seg_cover ? p.seg_blocks : (nb + p.max_seg - 1) / p.max_seg;
+  // Segment x works iff x == 0 or x * sb < nb.
+  if (cl_id > 0 && cl_id * p.CS * sb >= nb) return;  // uniform over the cluster
+  if (seg > 0 && nb <= sb) return;                     // no merge: only segment 0 works
   const int my_b0 = b_first + seg * sb;
   const int my_nb = max(0, min(b_first + nb, my_b0 + sb) - my_b0);
   const int ntile = (my_nb + TB - 1) / TB;
+  const int nseg = max(1, (nb + sb - 1) / sb);  // segments of this (sequence, head, row group)
+  const int ncl = (nseg + p.CS - 1) / p.CS;     // merge clusters
   if constexpr (TC) {
     // tensor memory for the two S buffers and O; freed once the epilogue has
     // read O (every path of the CTA reaches that point)
@@ -259,20 +273,20 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         i0 = kSpec;
       }
       for (int i = i0 + lane; i < n; i += 32)
-        pids[i] = __ldg(bt_row + (my_b0 + base + i) / (p.P / kBlockKeys));
+        pids[i] = __ldg(bt_row + (lg_bpp >= 0 ? (my_b0 + base + i) >> lg_bpp : (my_b0 + base + i) / bpp));
       __syncwarp();
     };
     if (my_nb > 0) load_pids(0);
     int issued = 0;
+    int slot = 0, phase = 0;  // ring slot of stage j and the parity of its round
     for (int j = 0; j < ntile; ++j) {
-      const int slot = j % NS;
       if (j * TB >= pid_base + kBlockIds) {
         pid_base = j * TB;
         load_pids(pid_base);
       }
       if (j >= NS) {
         int ok = 1;
-        if (lane == 0) ok = mbar_wait_bounded(smem_u32(empty + slot), ((j / NS) - 1) & 1);
+        if (lane == 0) ok = mbar_wait_bounded(smem_u32(empty + slot), phase ^ 1);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           if (lane == 0) {
@@ -288,8 +302,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
       __syncwarp();
       if (lane < 2 * nbt) {
         // one copy per 16-key block of K or V (all D/64 swizzle rows at once)
-        const int kv = lane / nbt, b = lane % nbt;
-        const int key0 = (my_b0 + j * TB + b) * kBlockKeys;
+        const int kv = lane >= nbt, b = lane - kv * nbt;
+        const int blk = my_b0 + j * TB + b;
+        const int key_in_page = (lg_bpp >= 0 ? blk & (bpp - 1) : blk % bpp) * kBlockKeys;
         int phys = pids[j * TB + b - pid_base];
         if ((unsigned)phys >= (unsigned)p.num_pool_blocks) {
           atomicOr(p.status, 0x2u);  // a page id outside the pool: report, read page 0
@@ -297,9 +312,13 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         }
         const uint32_t dst =
             smem_u32(ring + slot * STAGE + kv * (TB * BLOCK_BYTES) + b * BLOCK_BYTES);
-        tma_load_5d(dst, kv ? &tmV : &tmK, smem_u32(full + slot), 0, key0 % p.P, 0, h, phys, pol);
+        tma_load_5d(dst, kv ? &tmV : &tmK, smem_u32(full + slot), 0, key_in_page, 0, h, phys, pol);
       }
       issued = j + 1;
+      if (++slot == NS) {
+        slot = 0;
+        phase ^= 1;
+      }
     }
     // Leave no copy in flight: wait (bounded) for the last stages issued.
     if (lane == 0) {
@@ -579,10 +598,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     const int k_row = lane & 15, k_hi = lane >> 4;                     // K ldmatrix roles
     const int v_row = (lane & 7) + ((lane >> 4) << 3), v_hi = (lane >> 3) & 1;  // V^T roles
 
+    int slot = g_k % NS, phase = (g_k / NS) & 1;  // ring slot of tile j and its round parity
     for (int j = g_k; j < ntile; j += KG) {
-      const int slot = j % NS;
       // one verdict for the warp, so no lane leaves the shuffles alone
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), phase))) {
         if (lane == 0) {
           flags[0] = 1;
           atomicOr(p.status, 0x1u);
@@ -723,6 +742,11 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(empty + slot));
+      slot += KG;
+      while (slot >= NS) {
+        slot -= NS;
+        phase ^= 1;
+      }
     }
     // full row sums: the 8 lanes of one (lane & 3) class hold one row pair
 #pragma unroll
