@@ -174,7 +174,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   // first page copy ----
   const int rr0 = grow * p.rows_cta;
   const int rr1 = min(p.R, rr0 + p.rows_cta);
-  const int tok0 = rr0 / p.G, tok1 = (rr1 - 1) / p.G;  // tokens of the first and last row
+  const int lg_g = (p.G & (p.G - 1)) == 0 ? __ffs(p.G) - 1 : -1;  // G a power of two
+  auto token_of = [&](int rr) { return lg_g >= 0 ? rr >> lg_g : rr / p.G; };  // packed row -> token
+  const int tok0 = token_of(rr0), tok1 = token_of(rr1 - 1);  // tokens of the first and last row
+  const int lg_nt = (NT & (NT - 1)) == 0 ? __ffs(NT) - 1 : -1;
+  const int t_n = lg_nt >= 0 ? warp & (NT - 1) : warp % NT;  // consumer n-tile
+  const int g_k = lg_nt >= 0 ? warp >> lg_nt : warp / NT;    // consumer warp group
   const int cl_id = seg / p.CS;
   const int bpp = p.P / kBlockKeys;  // 16-key blocks per page
   const int lg_bpp = (bpp & (bpp - 1)) == 0 ? __ffs(bpp) - 1 : -1;
@@ -250,7 +255,6 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 #pragma unroll
   for (int i = 0; i < KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  const int t_n = warp % NT, g_k = warp / NT;
   const int r0 = t_n * 8 + 2 * (lane & 3), r1 = r0 + 1;
 
   if (warp == NC) {
@@ -556,11 +560,11 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     {
       const int rra = rr0 + r0, rrb = rr0 + r1;
       if (r0 < p.rows_cta && rra < p.R) {
-        hi0 = max(L - p.M + rra / p.G + 1, 0);
+        hi0 = max(L - p.M + token_of(rra) + 1, 0);
         lo0 = p.window ? max(0, hi0 - p.window) : 0;
       }
       if (r1 < p.rows_cta && rrb < p.R) {
-        hi1 = max(L - p.M + rrb / p.G + 1, 0);
+        hi1 = max(L - p.M + token_of(rrb) + 1, 0);
         lo1 = p.window ? max(0, hi1 - p.window) : 0;
       }
     }
@@ -572,7 +576,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         const int rr = rr0 + r;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (r < p.rows_cta && rr < p.R) {
-          const int i = rr / p.G, j = rr % p.G;
+          const int i = token_of(rr), j = rr - i * p.G;
           v = __ldg(reinterpret_cast<const uint4 *>(qbase + (int64_t)(s * p.M + i) * p.q_s0 +
                                                     (int64_t)(h * p.G + j) * p.q_s1 + c * 8));
         }
@@ -770,10 +774,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   float *lfin = mfin + NT8;
 
   T *obase = static_cast<T *>(p.out);
-  const int lg_g = (p.G & (p.G - 1)) == 0 ? __ffs(p.G) - 1 : -1;  // G a power of two
   auto out_row = [&](int r) -> T * {
     const int rr = rr0 + r;
-    const int i = lg_g >= 0 ? rr >> lg_g : rr / p.G;
+    const int i = token_of(rr);
     const int j = rr - i * p.G;
     return obase + (int64_t)(s * p.M + i) * p.o_s0 + (int64_t)(h * p.G + j) * p.o_s1;
   };
@@ -852,7 +855,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         tmem_dealloc(tmem_base, TMEM_COLS);
       }
     }
-    const int DKm = p.coop ? D / p.mergers : D;
+    const int DKm = p.coop ? D >> (__ffs(p.mergers) - 1) : D;  // K_max a power of two
     const int lg_dkm = __ffs(DKm) - 1;
     float *pa = p.part_acc + (gbase + cl_id) * (int64_t)NT8 * D;
     float2 *pm = reinterpret_cast<float2 *>(p.part_ml + (gbase + cl_id) * NT8 * 2);
@@ -899,6 +902,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         }
 #pragma unroll
         for (int u = 0; u < kGroupChunk; ++u) {
+          if (g0 + u >= KG) break;
           const float w = exp2_or_zero(mg[u], mu);
           lsum += w * lg[u];
 #pragma unroll
@@ -1117,8 +1121,11 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     // Every CTA of a cooperative launch is resident, so a merger waiting for
     // the remaining arrivals waits on CTAs that are running (bounded).
     // K = the largest power of two <= min(K_max, arrivals of this group).
-    int K = 1;
-    while (2 * K <= min(p.mergers, ncl)) K *= 2;
+    int K = 1, lg_k = 0;
+    while (2 * K <= min(p.mergers, ncl)) {
+      K *= 2;
+      ++lg_k;
+    }
     // Thread 0 counts the CTA in; a merger that is not the last arrival
     // waits there for the rest (the last one knows from the count that
     // every part is published, and its acquire already covers them).
@@ -1148,7 +1155,8 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     // end, so the round trip overlaps the merge
     const int fin_old = tid == 0 ? atomicAdd(p.counters + 2 * group + 1, 1) : 0;
     // this merger's layout slices: [mi * q, (mi + 1) * q) of the K_max slices
-    const int DKm = D / p.mergers, q = p.mergers / K, DK = q * DKm;
+    const int lg_km = __ffs(p.mergers) - 1;
+    const int DKm = D >> lg_km, q = p.mergers >> lg_k, DK = q * DKm;
     const int64_t part_floats = (int64_t)NT8 * D;
     const int slab = q * NT8 * DKm;  // floats of one part's share
     if (ncl * (2 * NT8 + slab) + 64 <= p.epi_floats &&
