@@ -175,7 +175,10 @@ typedef struct pd_plan {
   int max_segments;  /* segments per (sequence, kv head, row group) in the grid */
   int cluster;
   int max_parts;     /* partial slots per group in the scratch                 */
-  int grid_x, grid_y, block_threads;
+  int grid_x;        /* CTAs per sequence: kv heads x row_groups x max_segments */
+  int grid_y;        /* sequences (the launch grid is (max_segments,            */
+                     /* kv heads x row_groups, sequences))                      */
+  int block_threads;
   int smem_bytes;
   int64_t scratch_needed; /* bytes of scratch this call needs (0 = none)       */
 } pd_plan;

@@ -352,7 +352,9 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   } else if (o.merge == 2 && max_parts > 1) {
     return PD_EINVAL;  // the grid does not fit at once, or a cluster was asked for
   }
-  if ((int64_t)Hkv * rg * nseg > INT32_MAX || S > 65535) return PD_EINVAL;
+  // launched as (segments, kv heads x row groups, sequences)
+  if ((int64_t)Hkv * rg * nseg > INT32_MAX || (int64_t)Hkv * rg > 65535 || S > 65535)
+    return PD_EINVAL;
 
   plan->path = tc ? 3 : 1;
   plan->merge = merge;
@@ -467,7 +469,8 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   }
 
   Launch l;
-  l.grid = dim3(plan.grid_x, plan.grid_y, 1);
+  // (segment, kv head x row group, sequence): plan.grid_x CTAs per sequence
+  l.grid = dim3(plan.max_segments, num_kv_heads * plan.row_groups, plan.grid_y);
   l.block = dim3(plan.block_threads, 1, 1);
   l.smem = plan.smem_bytes;
   l.cluster = plan.cluster;

@@ -141,26 +141,28 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   uint32_t tmem_base = 0;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int s = blockIdx.y;
-  const int seg = blockIdx.x % p.max_seg;
-  const int hg = blockIdx.x / p.max_seg;
-  const int h = hg / p.rg, grow = hg % p.rg;
+  // grid (segment, kv head x row group, sequence)
+  const int seg = blockIdx.x, hg = blockIdx.y, s = blockIdx.z;
+  const int h = p.rg == 1 ? hg : hg / p.rg, grow = hg - h * p.rg;
 
   // ---- set-up that reads no global memory (it overlaps the previous grid's
   // tail): barriers, the tensor-map prefetch (the Q tile is loaded by the
   // consumers later) ----
-  if (tid == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(smem_u32(full + i), 1);
-      mbar_init(smem_u32(empty + i), TC ? 1 : NT);  // TC: freed by the PV MMAs' commit
+  // (one barrier per lane of warp 0)
+  if (warp == 0) {
+    if (lane < NS) {
+      mbar_init(smem_u32(full + lane), 1);
+      mbar_init(smem_u32(empty + lane), TC ? 1 : NT);  // TC: freed by the PV MMAs' commit
     }
     if constexpr (TC) {
-      for (int i = 0; i < kTcBarriers; ++i)
-        mbar_init(smem_u32(tcb + i), (i == 2 || i == 3 || i == 4 || i == 5) ? 4 : 1);
+      if (lane < kTcBarriers)
+        mbar_init(smem_u32(tcb + lane), (lane >= 2 && lane <= 5) ? 4 : 1);
     }
-    mbar_init(smem_u32(mbar_merge), 1);
-    flags[0] = 0;
-    flags[1] = 0;
+    if (lane == 31) {
+      mbar_init(smem_u32(mbar_merge), 1);
+      flags[0] = 0;
+      flags[1] = 0;
+    }
     fence_mbar_init();
   }
   if (warp == NC && lane == 0) {

@@ -125,6 +125,19 @@ def test_page_sizes(P):
     _parity(case)
 
 
+@pytest.mark.parametrize("Hq,Hkv,M,lens", [
+    (12, 4, 3, [2500, 700, 33]),   # G = 3: packed rows -> tokens by division
+    (10, 2, 4, [2500, 700, 33]),   # G = 5, 20 rows: three 8-row n-tiles in a batch
+    (24, 4, 2, [6000]),            # G = 6, one sequence: many segments, cooperative merge
+    (6, 6, 5, [1800, 5]),          # G = 1 (no grouping), M = 5
+])
+def test_head_ratios_not_powers_of_two(Hq, Hkv, M, lens):
+    case = W.make_case("ratios", seed=17, dtype=torch.bfloat16, head_size=128, num_q_heads=Hq,
+                       num_kv_heads=Hkv, page_size=16, max_query_len=M, seq_lens=lens,
+                       layout=W.HND)
+    _parity(case)
+
+
 def test_empty_and_short_sequences():
     case = W.make_case("edge", seed=8, dtype=torch.bfloat16, head_size=128, num_q_heads=8,
                        num_kv_heads=1, page_size=16, max_query_len=4,
