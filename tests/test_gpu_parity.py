@@ -138,6 +138,29 @@ def test_head_ratios_not_powers_of_two(Hq, Hkv, M, lens):
     _parity(case)
 
 
+def test_one_scratch_across_merge_kinds():
+    """One scratch serves calls whose merges differ (cooperative, last
+    arriver, cluster partials, a batch, unsplit) and whose partial layouts
+    overlap: every call must be right whatever the previous one left in the
+    partial area, and leave the counters at zero."""
+    cases = [
+        (W.spec_decode_hnd(4, 4096, seed=21), None),                        # cooperative
+        (W.wide_head(1, 8192, seed=22), None),                              # many parts
+        (W.spec_decode_hnd(2, 4096, seed=23), pd.options(merge=1)),         # last arriver
+        (W.spec_decode_hnd(4, 4096, seed=24), pd.options(cluster=4, segments=16)),
+        (W.batched_hybrid_pages(num_seqs=8, max_len=3000, seed=25), None),  # a batch
+        (W.spec_decode_hnd(1, 1024, seed=26), pd.options(merge=2, key_groups=1, stages=2)),
+        (W.spec_decode_hnd(3, 128, seed=27), None),                         # unsplit
+        (W.spec_decode_hnd(4, 4096, seed=21), None),
+    ]
+    sc = pd.Scratch(8, 16, 2, 512, 4, max_splits=64)
+    for case, opts in cases:
+        g = case.to("cuda")
+        out = run(g, scratch=sc, opts=opts)
+        check(case, out)
+        assert int(sc.counters().abs().sum()) == 0, case.name
+
+
 def test_empty_and_short_sequences():
     case = W.make_case("edge", seed=8, dtype=torch.bfloat16, head_size=128, num_q_heads=8,
                        num_kv_heads=1, page_size=16, max_query_len=4,
