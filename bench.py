@@ -433,6 +433,114 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+VARLEN_WORKLOAD = ("speculative-decode batch with a query length per request: bf16, head_size "
+                   "128, 32 q / 8 kv heads, page_size 16, HND, 32 requests, draft lengths "
+                   "U{1..4}, contexts U[1k, 16k] (one call = paged_decode_attn_varlen)")
+
+
+def _time_graph(calls, stream, reps):
+    """Mean µs per call of a CUDA graph of `calls`, replayed `reps` times."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in calls:
+            c()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * len(calls))
+
+
+def run_varlen(args, world, rank, local):
+    """--workload varlen: the variable-query-length call on a batch (replicas
+    past 2.2 x L2), with the same requests padded to a uniform call timed
+    beside it."""
+    import paged_split_kv_02_gb300 as pd
+    from paged_split_kv_02_gb300 import workloads as W
+
+    pd.build()
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 << 20))
+    peak, peak_kind = _peaks()
+    probe = W.varlen_spec_decode_batch(seed=0)
+    n_rep = max(2, math.ceil(2.2 * l2 / probe.kv_bytes_touched()))
+    var = [W.varlen_spec_decode_batch(seed=r, device=device, gen_device=device)
+           for r in range(n_rep)]
+    uni = [W.varlen_spec_decode_batch(seed=r, uniform=True, device=device, gen_device=device)
+           for r in range(n_rep)]
+    c0 = var[0]
+    scratch = pd.Scratch(c0.num_seqs, c0.num_q_heads, c0.num_kv_heads, c0.head_size, 4,
+                         max_splits=256, device=device)
+    outs_v = [torch.empty_like(c.q) for c in var]
+    outs_u = [torch.empty_like(c.q) for c in uni]
+    stream = torch.cuda.Stream(device=device)
+    calls_v = [(lambda c=c, o=o: pd.decode_case(c, out=o, scratch=scratch)) for c, o in zip(var, outs_v)]
+    calls_u = [(lambda c=c, o=o: pd.decode_case(c, out=o, scratch=scratch)) for c, o in zip(uni, outs_u)]
+    with torch.cuda.stream(stream):
+        for c in calls_v + calls_u:
+            c()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        _time_graph(calls_v, stream, 1)
+    _barrier(world)
+    with ClockSampler(local) as clk:
+        us = _time_graph(calls_v, stream, args.steps)
+    us = _max_over_ranks(us, world)
+    us_u = _time_graph(calls_u, stream, args.steps)
+    kv = sum(c.kv_bytes_touched() for c in var) / n_rep
+    alg = sum(c.algorithmic_bytes() for c in var) / n_rep
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        host = var[0].to("cpu")
+        rows = [(t, h) for t in range(0, host.q.shape[0], 8) for h in range(host.num_q_heads)]
+        n = oracle.default_threads()
+        t0 = time.perf_counter()
+        oracle.attention(host, rows=rows, nthreads=n)
+        dt = time.perf_counter() - t0
+        frac = len(rows) / (host.q.shape[0] * host.num_q_heads)
+        cpu = {"value": round(kv * frac / dt / 1e9, 4), "unit": UNIT, "cores": n,
+               "kind": "oracle", "seconds": round(dt, 2),
+               "sample": f"every 8th token row of one batch, all heads ({frac:.3f} of the "
+                         "rows), fp64 C oracle; value scaled to the sampled rows"}
+    status = pd.paged_decode_device_status(reset=True)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(world * kv / (us * 1e-6) / 1e9, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us * 1e-3, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/K/V, random page permutation)",
+        "config": {"workload": VARLEN_WORKLOAD,
+                   "l2": f"inputs larger than L2: {n_rep} rotating replicas",
+                   "timing": "CUDA graph of the calls, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps * n_rep,
+        "us_per_call": round(us, 3),
+        "padded_uniform_us_per_call": round(us_u, 3),
+        "roofline": {"bound": "hbm", "achieved": round(alg / (us * 1e-6) / 1e9, 1),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(alg / (us * 1e-6) / 1e9 / peak, 4), "traffic": None,
+                     "traffic_basis": "no ncu capture of this workload", "peak_kind": peak_kind},
+        "clocks": clk.summary(),
+        "e2e": None,
+        "cpu_baseline": cpu,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -440,6 +548,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="sweep", choices=["sweep", "varlen"],
+                    help="sweep: the spec-decode sweep (default); varlen: a batch with a "
+                         "query length per request")
     ap.add_argument("--cases", default="",
                     help="restrict the sweep, e.g. 4:32768,1:4096 (profiling runs only)")
     args = ap.parse_args()
@@ -451,6 +562,8 @@ def main():
     world, rank, local = _dist()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.workload == "varlen":
+        run_varlen(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

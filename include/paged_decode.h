@@ -101,6 +101,7 @@ typedef enum {
 #define PD_DEV_WAIT_TIMEOUT 0x1u  /* an internal barrier wait gave up       */
 #define PD_DEV_BAD_PAGE     0x2u  /* a block-table entry outside the pool   */
 #define PD_DEV_BAD_SEQLEN   0x4u  /* seq_len > block-table width * page_size */
+#define PD_DEV_BAD_QSTART   0x8u  /* query_start out of order or out of range */
 
 /* Bytes of scratch for calls of up to `max_num_seqs` sequences
  * (scratch_bytes: 4 * (rows * D + 2 * rows + counters) per sequence).
@@ -162,6 +163,28 @@ PD_API int paged_decode_attn_opts(const pd_tensor *q, const pd_tensor *k_cache, 
                            int num_q_heads, int num_kv_heads, int head_size, int page_size,
                            int max_query_len, int window, float scale, int layout,
                            pd_scratch *scratch, void *stream, const pd_options *opts);
+
+/* A decode batch whose requests have different query lengths (the
+ * query_start_loc / q_to_klen maps of the vLLM ROCm Octave backend,
+ * `_fill_query_maps`): request s owns the rows query_start[s] ..
+ * query_start[s+1] - 1 of q and out, q_len_s = query_start[s+1] -
+ * query_start[s] <= max_query_len <= 8, and its token i sees the keys
+ * [lo, seq_lens[s] - q_len_s + i + 1) (lo as in paged_decode_attn).  Rows at
+ * and past query_start[S] (padding of a captured batch) see no key and are
+ * written as zeros.
+ *   q, out       [T, Hq, D] for any T >= 0 (T = 0: nothing to do)
+ *   query_start  [S + 1] int32 device array, non-decreasing, 0 <= entries <= T
+ * The other arguments are those of paged_decode_attn_opts (opts may be
+ * NULL; path 3 is not built for this call: PD_EINVAL).  Entries outside
+ * [0, T], decreasing ones or a q_len above max_query_len are clamped on the
+ * device and reported as PD_DEV_BAD_QSTART. */
+PD_API int paged_decode_attn_varlen(const pd_tensor *q, const pd_tensor *k_cache,
+                                    const pd_tensor *v_cache, const pd_tensor *block_table,
+                                    const pd_tensor *seq_lens, const pd_tensor *query_start,
+                                    pd_tensor *out, int num_q_heads, int num_kv_heads,
+                                    int head_size, int page_size, int max_query_len, int window,
+                                    float scale, int layout, pd_scratch *scratch, void *stream,
+                                    const pd_options *opts);
 
 /* The launch plan chosen for a call shape, computed on the host only (no
  * device access), for inspection and tests. */

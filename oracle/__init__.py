@@ -9,7 +9,9 @@ per slice of output rows).  This wrapper only hands it raw 16-bit words and
 element strides; it shares no code with the CUDA path.
 
 * ``attention(case, rows=None)``: outputs ``[S*M, Hq, D]`` (fp64), or the
-  selected output rows ``[(t, hq), ...]`` as ``[len(rows), D]``.
+  selected output rows ``[(t, hq), ...]`` as ``[len(rows), D]``.  A case
+  with ``query_start`` (variable query lengths) gives ``[T, Hq, D]`` over
+  its T token rows.
 * ``partial(case, key_lo, key_hi)``: unnormalised ``(acc, m, l)`` over a key
   sub-range, for the split-KV pins.
 * ``merge(parts)``: the split-KV merge of partials, written from its
@@ -54,6 +56,8 @@ def load_library(path: str):
               i32, i32, i32, i32, i32, i32, i32, i32, dbl]
     lib.pdo_attention.argtypes = common + [vp, i64, vp, i32]
     lib.pdo_attention.restype = i32
+    lib.pdo_attention_varlen.argtypes = common + [vp, i64, vp, i64, vp, i32]
+    lib.pdo_attention_varlen.restype = i32
     lib.pdo_partial.argtypes = common + [i64, i64, vp, vp, vp, i32]
     lib.pdo_partial.restype = i32
     lib.pdo_widen.argtypes = [ctypes.c_uint16, i32]
@@ -114,6 +118,24 @@ def attention(case, rows=None, nthreads: int | None = None, lib=None) -> np.ndar
     args, keep = _common_args(case)
     nthreads = nthreads or default_threads()
     D = case.head_size
+    qs = getattr(case, "query_start", None)
+    if qs is not None:
+        # variable query lengths: rows are the batch's tokens
+        qsl = qs.cpu().to(torch.int32).contiguous()
+        T = int(case.q.shape[0])
+        extra = [qsl.data_ptr(), T]
+        if rows is None:
+            sel, nsel, shape = None, 0, (T, case.num_q_heads, D)
+            n = T * case.num_q_heads
+        else:
+            sel_a = np.asarray([int(t) * case.num_q_heads + int(h) for t, h in rows], dtype=np.int64)
+            sel, nsel, shape, n = sel_a.ctypes.data, len(sel_a), (len(sel_a), D), len(sel_a)
+        out = np.empty((n, D), dtype=np.float64)
+        rc = lib.pdo_attention_varlen(*args, *extra, sel, nsel, out.ctypes.data, nthreads)
+        if rc != 0:
+            raise RuntimeError(f"oracle failed: {rc}")
+        del keep, qsl
+        return out.reshape(shape)
     if rows is None:
         n = case.q.shape[0] * case.num_q_heads
         out = np.empty((n, D), dtype=np.float64)

@@ -28,6 +28,13 @@
  *   o    = 0 when no key is visible   (padding queries get K length 0,
  *                                      rocm_octave_attn, _fill_query_maps)
  *
+ * With variable query lengths (rocm_octave_attn, _fill_query_maps) the rows
+ * are the tokens t of a batch described by query_start[0..S]: the request of
+ * t is the number of entries query_start[1..S] that are <= t (a right-sided
+ * search), its q_len is query_start[r+1] - query_start[r], and t sees
+ * K length L_r - q_len + (t - query_start[r]) + 1; a token at or past
+ * query_start[S] belongs to no request and gets K length 0.
+ *
  * Inputs are the raw 16-bit fp16/bf16 words; they are widened to double
  * exactly (IEEE binary16 / bfloat16 definitions below), so the oracle sees
  * exactly the values the GPU reads.  The cache is addressed through four
@@ -78,20 +85,43 @@ typedef struct {
   const int32_t *seq_lens;
   int num_seqs, is_bf16, Hq, Hkv, D, P, M, window;
   double scale;
+  const int32_t *qsl; /* query_start [S + 1], or NULL: token t = s * M + i */
 } pdo_args;
 
 static double widen(const pdo_args *a, uint16_t w) {
   return a->is_bf16 ? bf16_to_double(w) : half_to_double(w);
 }
 
-/* The visible key range [lo, hi) of query token i of sequence s. */
-static void visible_range(const pdo_args *a, int s, int i, int64_t *lo, int64_t *hi) {
-  int64_t L = a->seq_lens[s];
-  int64_t n = L - a->M + i + 1;
+/* The request s of query row t and the keys [lo, hi) it sees; 0 when t
+ * belongs to no request (then it sees no key). */
+static int visible_range(const pdo_args *a, int64_t t, int *s_out, int64_t *lo, int64_t *hi) {
+  int64_t n;
+  int s;
+  *lo = 0;
+  *hi = 0;
+  if (a->qsl) {
+    /* right-sided search of t in query_start[1..S] */
+    int lo_i = 0, hi_i = a->num_seqs;
+    while (lo_i < hi_i) {
+      int mid = (lo_i + hi_i) / 2;
+      if (a->qsl[mid + 1] <= t)
+        lo_i = mid + 1;
+      else
+        hi_i = mid;
+    }
+    s = lo_i;
+    if (s >= a->num_seqs) return 0;
+    int64_t q_len = (int64_t)a->qsl[s + 1] - a->qsl[s];
+    n = (int64_t)a->seq_lens[s] - q_len + (t - a->qsl[s]) + 1;
+  } else {
+    s = (int)(t / a->M);
+    n = (int64_t)a->seq_lens[s] - a->M + (t % a->M) + 1;
+  }
+  *s_out = s;
   if (n < 0) n = 0;
   *hi = n;
-  *lo = 0;
   if (a->window > 0 && n - a->window > 0) *lo = n - a->window;
+  return 1;
 }
 
 static const uint16_t *key_row(const pdo_args *a, const uint16_t *base, int s, int64_t k, int h) {
@@ -109,11 +139,11 @@ static const uint16_t *key_row(const pdo_args *a, const uint16_t *base, int s, i
 static void row_partial(const pdo_args *a, int64_t t, int hq, int64_t klo, int64_t khi,
                         double *x /* scratch, >= khi-klo */, double *acc, double *m_out,
                         double *l_out) {
-  int s = (int)(t / a->M), i = (int)(t % a->M);
   int G = a->Hq / a->Hkv;
   int h = hq / G;
+  int s = 0;
   int64_t lo, hi;
-  visible_range(a, s, i, &lo, &hi);
+  visible_range(a, t, &s, &lo, &hi);
   if (klo > lo) lo = klo;
   if (khi < hi) hi = khi;
   for (int d = 0; d < a->D; ++d) acc[d] = 0.0;
@@ -238,7 +268,7 @@ static int run(const pdo_args *a, const int64_t *sel, int64_t nrows, int64_t klo
   a.block_table = block_table; a.bt_stride = bt_stride; a.bt_width = bt_width;            \
   a.seq_lens = seq_lens; a.num_seqs = num_seqs; a.is_bf16 = is_bf16;                      \
   a.Hq = num_q_heads; a.Hkv = num_kv_heads; a.D = head_size; a.P = page_size;            \
-  a.M = max_query_len; a.window = window; a.scale = scale;
+  a.M = max_query_len; a.window = window; a.scale = scale; a.qsl = NULL;
 
 /* Full outputs: out[r][d] for the selected rows (or all S*M*Hq rows). */
 int pdo_attention(const uint16_t *q, int64_t q_s0, int64_t q_s1, int64_t q_s2,
@@ -250,6 +280,24 @@ int pdo_attention(const uint16_t *q, int64_t q_s0, int64_t q_s1, int64_t q_s2,
                   double *out, int nthreads) {
   PDO_ARGS_FROM_PARAMS
   int64_t nrows = sel ? nsel : (int64_t)num_seqs * max_query_len * num_q_heads;
+  return run(&a, sel, nrows, 0, INT64_MAX, 0, out, NULL, NULL, nthreads);
+}
+
+/* Full outputs of a batch with variable query lengths: rows t in
+ * [0, num_tokens) described by query_start[0..num_seqs] (non-decreasing). */
+int pdo_attention_varlen(const uint16_t *q, int64_t q_s0, int64_t q_s1, int64_t q_s2,
+                         const uint16_t *k, const uint16_t *v, int64_t kv_sp, int64_t kv_st,
+                         int64_t kv_sh, int64_t kv_sd, const int32_t *block_table,
+                         int64_t bt_stride, int64_t bt_width, const int32_t *seq_lens,
+                         int num_seqs, int is_bf16, int num_q_heads, int num_kv_heads,
+                         int head_size, int page_size, int max_query_len, int window,
+                         double scale, const int32_t *query_start, int64_t num_tokens,
+                         const int64_t *sel, int64_t nsel, double *out, int nthreads) {
+  PDO_ARGS_FROM_PARAMS
+  a.qsl = query_start;
+  for (int s = 0; s < num_seqs; ++s)
+    if (query_start[s + 1] < query_start[s] || query_start[s] < 0) return -4;
+  int64_t nrows = sel ? nsel : num_tokens * num_q_heads;
   return run(&a, sel, nrows, 0, INT64_MAX, 0, out, NULL, NULL, nthreads);
 }
 

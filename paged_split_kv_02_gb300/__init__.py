@@ -35,7 +35,7 @@ STATUS_NAMES = {
     0: "PD_OK", -1: "PD_EINVAL", -2: "PD_EDTYPE", -3: "PD_EHEAD", -4: "PD_EQLEN",
     -5: "PD_EALIGN", -6: "PD_ESCRATCH", -7: "PD_ECUDA", -8: "PD_ENODEV",
 }
-DEV_WAIT_TIMEOUT, DEV_BAD_PAGE, DEV_BAD_SEQLEN = 0x1, 0x2, 0x4
+DEV_WAIT_TIMEOUT, DEV_BAD_PAGE, DEV_BAD_SEQLEN, DEV_BAD_QSTART = 0x1, 0x2, 0x4, 0x8
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
                       "paged_decode.h")
@@ -110,6 +110,8 @@ def lib():
         L.paged_decode_attn.restype = i32
         L.paged_decode_attn_opts.argtypes = attn_args + [ctypes.POINTER(PdOptions)]
         L.paged_decode_attn_opts.restype = i32
+        L.paged_decode_attn_varlen.argtypes = [T] * 7 + attn_args[6:] + [ctypes.POINTER(PdOptions)]
+        L.paged_decode_attn_varlen.restype = i32
         L.paged_decode_attn_static.argtypes = attn_args[:14] + [vp]
         L.paged_decode_attn_static.restype = i32
         L.paged_decode_plan.argtypes = [i32] * 9 + [ctypes.POINTER(PdScratch),
@@ -224,6 +226,27 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, out, num_q_hea
     return rc
 
 
+def paged_decode_attn_varlen(q, k_cache, v_cache, block_table, seq_lens, query_start, out,
+                             num_q_heads, num_kv_heads, head_size, page_size, max_query_len,
+                             window, scale, layout, scratch: Optional[Scratch] = None,
+                             stream=None, opts: Optional[PdOptions] = None,
+                             check: bool = True) -> int:
+    """The decode call for a batch with a query length per request:
+    ``query_start`` [S + 1] int32 gives each request's first row of q / out
+    (see the C header); rows past the last request are written as zeros."""
+    L = lib()
+    descs = [tensor_desc(t) for t in (q, k_cache, v_cache, block_table, seq_lens, query_start,
+                                      out)]
+    sp = ctypes.byref(scratch.desc) if scratch is not None else None
+    rc = L.paged_decode_attn_varlen(
+        *[ctypes.byref(d) for d in descs], int(num_q_heads), int(num_kv_heads), int(head_size),
+        int(page_size), int(max_query_len), int(window), float(scale), int(layout), sp,
+        _stream_handle(stream), ctypes.byref(opts) if opts is not None else None)
+    if check and rc != PD_OK:
+        raise PagedDecodeError(rc, "paged_decode_attn_varlen")
+    return rc
+
+
 def paged_decode_attn_static(q, k_cache, v_cache, block_table, seq_lens, out, num_q_heads,
                              num_kv_heads, head_size, page_size, max_query_len, window, scale,
                              layout, stream=None, check: bool = True) -> int:
@@ -274,6 +297,13 @@ def decode_case(case, out=None, scratch=None, stream=None, opts=None):
     """Run the kernel on a ``workloads.DecodeCase`` (tensors on the GPU)."""
     if out is None:
         out = torch.empty_like(case.q)
+    if getattr(case, "query_start", None) is not None:
+        paged_decode_attn_varlen(case.q, case.k_cache, case.v_cache, case.block_table,
+                                 case.seq_lens, case.query_start, out, case.num_q_heads,
+                                 case.num_kv_heads, case.head_size, case.page_size,
+                                 case.max_query_len, case.window, case.scale, case.layout,
+                                 scratch, stream, opts)
+        return out
     paged_decode_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, out,
                       case.num_q_heads, case.num_kv_heads, case.head_size, case.page_size,
                       case.max_query_len, case.window, case.scale, case.layout, scratch,

@@ -380,10 +380,10 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
 int element_dtype_ok(const pd_tensor *t, int want) { return t->dtype == want; }
 
 int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_cache,
-              const pd_tensor *block_table, const pd_tensor *seq_lens, pd_tensor *out,
-              int num_q_heads, int num_kv_heads, int head_size, int page_size, int max_query_len,
-              int window, float scale, int layout, pd_scratch *scratch, void *stream,
-              const pd_options *opts) {
+              const pd_tensor *block_table, const pd_tensor *seq_lens,
+              const pd_tensor *query_start, pd_tensor *out, int num_q_heads, int num_kv_heads,
+              int head_size, int page_size, int max_query_len, int window, float scale,
+              int layout, pd_scratch *scratch, void *stream, const pd_options *opts) {
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PD_EINVAL;
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return PD_EINVAL;
   if (head_size != 64 && head_size != 128 && head_size != 256 && head_size != 512) return PD_EHEAD;
@@ -398,9 +398,21 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   if (block_table->ndim != 2 || !block_table->data || block_table->shape[0] != S ||
       block_table->shape[1] < 1 || block_table->stride[1] != 1 || block_table->stride[0] < 0)
     return PD_EINVAL;
+  // rows of q and out: S * M (uniform), or any count T with query_start
+  // [S + 1] giving each sequence's first row (variable query lengths)
+  int64_t T = S * max_query_len;
+  if (query_start) {
+    if (query_start->ndim != 1 || !query_start->data || query_start->shape[0] != S + 1 ||
+        query_start->stride[0] != 1)
+      return PD_EINVAL;
+    if (!element_dtype_ok(query_start, PD_I32)) return PD_EDTYPE;
+    if (!q->data || q->ndim != 3) return PD_EINVAL;
+    T = q->shape[0];
+    if (T < 0 || T > INT32_MAX) return PD_EINVAL;
+  }
   int rc;
-  if ((rc = check_rows_tensor(q, S * max_query_len, num_q_heads, head_size)) != PD_OK) return rc;
-  if ((rc = check_rows_tensor(out, S * max_query_len, num_q_heads, head_size)) != PD_OK) return rc;
+  if ((rc = check_rows_tensor(q, T, num_q_heads, head_size)) != PD_OK) return rc;
+  if ((rc = check_rows_tensor(out, T, num_q_heads, head_size)) != PD_OK) return rc;
   if ((rc = check_cache(k_cache, layout, num_kv_heads, page_size, head_size)) != PD_OK) return rc;
   if ((rc = check_cache(v_cache, layout, num_kv_heads, page_size, head_size)) != PD_OK) return rc;
   if (q->dtype != out->dtype || q->dtype != k_cache->dtype || q->dtype != v_cache->dtype)
@@ -409,7 +421,7 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
     if (k_cache->shape[i] != v_cache->shape[i]) return PD_EINVAL;
   if (block_table->shape[1] > INT32_MAX || block_table->shape[1] * (int64_t)page_size > INT32_MAX)
     return PD_EINVAL;
-  if (S == 0) return PD_OK;
+  if (S == 0 || T == 0) return PD_OK;
 
   DeviceInfo dev;
   if ((rc = device_info(&dev)) != PD_OK) return rc;
@@ -417,6 +429,7 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   rc = make_plan((int)S, num_q_heads, num_kv_heads, head_size, page_size, max_query_len, window,
                  (int)block_table->shape[1], dev.num_sms, scratch, opts, &plan);
   if (rc != PD_OK) return rc;
+  if (query_start && plan.path == 3) return PD_EINVAL;  // not built for variable lengths
 
   CUtensorMap tk, tv;
   if ((rc = encode_cache_map(k_cache, layout, &tk)) != PD_OK) return rc;
@@ -433,6 +446,8 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   p.bt_stride = block_table->stride[0];
   p.bt_width = (int)block_table->shape[1];
   p.seq_lens = static_cast<const int32_t *>(seq_lens->data);
+  p.query_start = query_start ? static_cast<const int32_t *>(query_start->data) : nullptr;
+  p.num_tokens = (int)T;
   p.num_pool_blocks = (int)k_cache->shape[0];
   p.Hq = num_q_heads;
   p.Hkv = num_kv_heads;
@@ -531,9 +546,9 @@ int paged_decode_attn(const pd_tensor *q, const pd_tensor *k_cache, const pd_ten
                       int num_q_heads, int num_kv_heads, int head_size, int page_size,
                       int max_query_len, int window, float scale, int layout,
                       pd_scratch *scratch, void *stream) {
-  return attn_impl(q, k_cache, v_cache, block_table, seq_lens, out, num_q_heads, num_kv_heads,
-                   head_size, page_size, max_query_len, window, scale, layout, scratch, stream,
-                   nullptr);
+  return attn_impl(q, k_cache, v_cache, block_table, seq_lens, nullptr, out, num_q_heads,
+                   num_kv_heads, head_size, page_size, max_query_len, window, scale, layout,
+                   scratch, stream, nullptr);
 }
 
 int paged_decode_attn_opts(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_cache,
@@ -541,9 +556,22 @@ int paged_decode_attn_opts(const pd_tensor *q, const pd_tensor *k_cache, const p
                            int num_q_heads, int num_kv_heads, int head_size, int page_size,
                            int max_query_len, int window, float scale, int layout,
                            pd_scratch *scratch, void *stream, const pd_options *opts) {
-  return attn_impl(q, k_cache, v_cache, block_table, seq_lens, out, num_q_heads, num_kv_heads,
-                   head_size, page_size, max_query_len, window, scale, layout, scratch, stream,
-                   opts);
+  return attn_impl(q, k_cache, v_cache, block_table, seq_lens, nullptr, out, num_q_heads,
+                   num_kv_heads, head_size, page_size, max_query_len, window, scale, layout,
+                   scratch, stream, opts);
+}
+
+int paged_decode_attn_varlen(const pd_tensor *q, const pd_tensor *k_cache,
+                             const pd_tensor *v_cache, const pd_tensor *block_table,
+                             const pd_tensor *seq_lens, const pd_tensor *query_start,
+                             pd_tensor *out, int num_q_heads, int num_kv_heads, int head_size,
+                             int page_size, int max_query_len, int window, float scale,
+                             int layout, pd_scratch *scratch, void *stream,
+                             const pd_options *opts) {
+  if (!query_start) return PD_EINVAL;
+  return attn_impl(q, k_cache, v_cache, block_table, seq_lens, query_start, out, num_q_heads,
+                   num_kv_heads, head_size, page_size, max_query_len, window, scale, layout,
+                   scratch, stream, opts);
 }
 
 int paged_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,

@@ -33,6 +33,9 @@ struct Params {
   int64_t bt_stride;
   int bt_width;
   const int32_t *seq_lens;
+  const int32_t *query_start;  // [S + 1] first q / out row of each sequence, or null
+                               // (then sequence s owns rows s * M .. s * M + M - 1)
+  int num_tokens;              // rows of q and out
   int num_pool_blocks;  // pages in the pool, for the page-id bounds check
   int Hq, Hkv, G, M, P, window, layout;
   float scale_log2;  // scale * log2(e): softmax runs on exp2

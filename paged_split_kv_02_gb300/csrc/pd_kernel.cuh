@@ -209,6 +209,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   grid_dependency_wait();
 
   int L = __ldg(p.seq_lens + s);
+  // q / out rows of the sequence: [s * M, s * M + M), or from query_start
+  int qa = s * p.M, qb = qa + p.M;
+  if (p.query_start) {
+    qa = __ldg(p.query_start + s);
+    qb = __ldg(p.query_start + s + 1);
+  }
   if (spec_on) {
 #pragma unroll
     for (int k = 0; k < kSpec / 32; ++k) spec[k] = spec[k] >= 0 ? __ldg(bt_row + spec[k]) : 0;
@@ -220,10 +226,23 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     if (tid == 0 && seg == 0) atomicOr(p.status, 0x4u);
     L = p.bt_width * p.P;
   }
+  // first row and query tokens of the sequence (clamped into [0, num_tokens]
+  // and to M, and reported, when query_start is out of order or range)
+  int q0 = qa, ml = p.M;
+  if (p.query_start) {
+    const int a = min(max(qa, 0), p.num_tokens), b = min(max(qb, a), p.num_tokens);
+    if ((a != qa || b != qb || b - a > p.M) && tid == 0 && seg == 0 && hg == 0)
+      atomicOr(p.status, 0x8u);
+    q0 = a;
+    ml = min(b - a, p.M);
+  }
+  // rows of real query tokens: a prefix of the CTA's rows (token-major packing)
+  const int rr1v = min(rr1, ml * p.G);
+  const int tok1v = rr1v < rr1 ? ml - 1 : tok1;
   int u_lo = 0, u_hi = 0, v_lo = 0, v_hi = 0;  // union / intersection of the rows' key ranges
-  if (rr1 > rr0) {
-    const int n0 = max(L - p.M + tok0 + 1, 0);
-    const int n1 = max(L - p.M + tok1 + 1, 0);
+  if (rr1v > rr0) {
+    const int n0 = max(L - ml + tok0 + 1, 0);
+    const int n1 = max(L - ml + tok1v + 1, 0);
     u_hi = n1;
     v_hi = n0;
     u_lo = p.window ? max(0, n0 - p.window) : 0;
@@ -360,9 +379,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         const int r = idx / (D / 8), c = idx % (D / 8);
         const int rp = r & 15, rr = rr0 + rp;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (rp < p.rows_cta && rr < p.R) {
+        if (rp < p.rows_cta && rr < rr1v) {
           const int i = rr / p.G, jq = rr % p.G;
-          v = __ldg(reinterpret_cast<const uint4 *>(qbase + (int64_t)(s * p.M + i) * p.q_s0 +
+          v = __ldg(reinterpret_cast<const uint4 *>(qbase + (int64_t)(q0 + i) * p.q_s0 +
                                                     (int64_t)(h * p.G + jq) * p.q_s1 + c * 8));
         }
         const int tn = r >> 3, rw = r & 7, box = c >> 3, cc = c & 7;
@@ -429,10 +448,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     } else {
       // ---- softmax (warp q = copy q, keys [q KPC, (q + 1) KPC) of a stage) ----
       const int r = lane & 15, prow = 16 * warp + r;  // packed row, P / MMA row
-      const bool live = lane < 16 && r < p.rows_cta && rr0 + r < p.R;
+      const bool live = lane < 16 && r < p.rows_cta && rr0 + r < rr1v;
       int lo = 0, hi = 0;
       if (live) {
-        hi = max(L - p.M + (rr0 + r) / p.G + 1, 0);
+        hi = max(L - ml + (rr0 + r) / p.G + 1, 0);
         lo = p.window ? max(0, hi - p.window) : 0;
       }
       const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
@@ -561,12 +580,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
     {
       const int rra = rr0 + r0, rrb = rr0 + r1;
-      if (r0 < p.rows_cta && rra < p.R) {
-        hi0 = max(L - p.M + token_of(rra) + 1, 0);
+      if (rra < rr1v) {
+        hi0 = max(L - ml + token_of(rra) + 1, 0);
         lo0 = p.window ? max(0, hi0 - p.window) : 0;
       }
-      if (r1 < p.rows_cta && rrb < p.R) {
-        hi1 = max(L - p.M + token_of(rrb) + 1, 0);
+      if (rrb < rr1v) {
+        hi1 = max(L - ml + token_of(rrb) + 1, 0);
         lo1 = p.window ? max(0, hi1 - p.window) : 0;
       }
     }
@@ -577,9 +596,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         const int r = idx / (D / 8), c = idx % (D / 8);
         const int rr = rr0 + r;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < p.rows_cta && rr < p.R) {
+        if (rr < rr1v) {
           const int i = token_of(rr), j = rr - i * p.G;
-          v = __ldg(reinterpret_cast<const uint4 *>(qbase + (int64_t)(s * p.M + i) * p.q_s0 +
+          v = __ldg(reinterpret_cast<const uint4 *>(qbase + (int64_t)(q0 + i) * p.q_s0 +
                                                     (int64_t)(h * p.G + j) * p.q_s1 + c * 8));
         }
         const int tn = r >> 3, rw = r & 7, box = c >> 3, cc = c & 7;
@@ -780,9 +799,22 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     const int rr = rr0 + r;
     const int i = token_of(rr);
     const int j = rr - i * p.G;
-    return obase + (int64_t)(s * p.M + i) * p.o_s0 + (int64_t)(h * p.G + j) * p.o_s1;
+    return obase + (int64_t)(q0 + i) * p.o_s0 + (int64_t)(h * p.G + j) * p.o_s1;
   };
-  const int nrows = max(0, rr1 - rr0);  // valid rows of this CTA
+  const int nrows = max(0, rr1v - rr0);  // valid rows of this CTA
+  if (p.query_start && seg == 0 && hg == 0 && s == 0) {
+    // rows at and past the last request's end (padding of a captured batch)
+    // see no key: zeros
+    const int t0 = min(max(__ldg(p.query_start + gridDim.z), 0), p.num_tokens);
+    const int per_row = p.Hq * (D / 8);
+#pragma unroll 1
+    for (int64_t i = tid; i < (int64_t)(p.num_tokens - t0) * per_row; i += blockDim.x) {
+      const int t = t0 + (int)(i / per_row), rem = (int)(i - (int64_t)(t - t0) * per_row);
+      const int hq = rem / (D / 8), c = rem - hq * (D / 8);
+      *reinterpret_cast<uint4 *>(obase + (int64_t)t * p.o_s0 + (int64_t)hq * p.o_s1 + c * 8) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
 
   const int CS = p.CS;
   const int DS = D / CS;

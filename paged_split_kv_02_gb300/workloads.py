@@ -69,6 +69,10 @@ class DecodeCase:
     packed: bool = False
     # host copy of seq_lens (the inputs are made on the host; kept for sizing)
     seq_lens_host: Optional[list] = None
+    # variable query lengths: [S + 1] int32, request s owns q rows
+    # query_start[s] .. query_start[s+1] - 1 (None: uniform, s*M .. s*M+M-1)
+    query_start: Optional[torch.Tensor] = None
+    query_start_host: Optional[list] = None
 
     @property
     def num_seqs(self) -> int:
@@ -93,6 +97,7 @@ class DecodeCase:
             v_cache=v,
             block_table=self.block_table.to(device),
             seq_lens=self.seq_lens.to(device),
+            query_start=None if self.query_start is None else self.query_start.to(device),
         )
 
     def _pool_shape(self):
@@ -109,11 +114,20 @@ class DecodeCase:
         e = self.q.element_size()
         total = 0
         lens = self.seq_lens_host or self.seq_lens.tolist()
-        for L in lens:
+        for s, L in enumerate(lens):
             L = max(int(L), 0)
-            u = min(L, self.window + self.max_query_len - 1) if self.window else L
+            m = self.query_len(s)
+            if m == 0:
+                continue
+            u = min(L, self.window + m - 1) if self.window else L
             total += u * self.num_kv_heads * 2 * self.head_size * e
         return total
+
+    def query_len(self, s: int) -> int:
+        """Query tokens of sequence s."""
+        if self.query_start_host is None:
+            return self.max_query_len
+        return self.query_start_host[s + 1] - self.query_start_host[s]
 
     def pages_touched(self) -> int:
         lens = self.seq_lens_host or self.seq_lens.tolist()
@@ -128,7 +142,7 @@ class DecodeCase:
     def algorithmic_bytes(self) -> int:
         """K+V read, Q read and O write, block-table entries and seq_lens."""
         e = self.q.element_size()
-        qo = 2 * self.num_seqs * self.max_query_len * self.num_q_heads * self.head_size * e
+        qo = 2 * self.q.shape[0] * self.num_q_heads * self.head_size * e
         return self.kv_bytes_touched() + qo + 4 * self.pages_touched() + 4 * self.num_seqs
 
 
@@ -266,6 +280,33 @@ def make_case(
     )
 
 
+def make_varlen_case(name: str, *, seed: int, q_lens: Sequence[int], pad_tokens: int = 0,
+                     **kw) -> DecodeCase:
+    """A decode batch with a query length per request (q_lens[s] <= 8,
+    zero allowed) and ``pad_tokens`` rows past the last request, as in a
+    captured batch padded to a fixed token count.  The pool and block table
+    are those of ``make_case`` with ``max_query_len = max(q_lens)`` (at least
+    1); q holds sum(q_lens) + pad_tokens rows, request s at query_start[s]."""
+    q_lens = [int(m) for m in q_lens]
+    assert all(0 <= m <= 8 for m in q_lens) and len(q_lens) == len(kw["seq_lens"])
+    M = max(1, max(q_lens) if q_lens else 1)
+    if kw.get("max_query_len") is None:
+        kw["max_query_len"] = M
+    assert kw["max_query_len"] >= M
+    case = make_case(name, seed=seed, **kw)
+    qsl = [0]
+    for m in q_lens:
+        qsl.append(qsl[-1] + m)
+    T = qsl[-1] + int(pad_tokens)
+    g_q = _gen(seed, _STREAM_Q, kw.get("gen_device", "cpu"))
+    q = _rounded_normal((T, case.num_q_heads, case.head_size), kw.get("std", 1.0), 0.0,
+                        case.dtype, g_q, kw.get("gen_device", "cpu"))
+    dev = case.q.device
+    return dataclasses.replace(case, q=q.to(dev),
+                               query_start=torch.tensor(qsl, dtype=torch.int32, device=dev),
+                               query_start_host=qsl)
+
+
 # ---------------------------------------------------------------------------
 # The five workloads.  Sizes follow the decode configurations the kernel is
 # specified on; the pages' own harness (vLLM's attention_benchmarks, HND,
@@ -339,3 +380,22 @@ def batched_hybrid_pages(seed: int = 0, num_seqs: int = 64, max_len: int = 16384
 
 SPEC_DECODE_CONTEXTS = (128, 1024, 4096, 16384, 32768)
 SPEC_DECODE_M = (1, 2, 3, 4)
+
+
+def varlen_spec_decode_batch(seed: int = 0, num_seqs: int = 32, min_len: int = 1024,
+                             max_len: int = 16384, max_draft: int = 4, pad_tokens: int = 0,
+                             uniform: bool = False, device: str = "cpu",
+                             gen_device: str = "cpu") -> DecodeCase:
+    """Speculative decoding over a batch: bf16, D=128, 32 q / 8 kv heads,
+    P=16, HND; request s has 1..max_draft query tokens (seeded) and a context
+    uniform in [min_len, max_len].  ``uniform=True`` gives the same requests
+    padded to max_draft query rows each (the uniform call's layout)."""
+    g = torch.Generator().manual_seed(seed * 7919 + 3)
+    q_lens = torch.randint(1, max_draft + 1, (num_seqs,), generator=g).tolist()
+    lens = torch.randint(min_len, max_len + 1, (num_seqs,), generator=g).tolist()
+    kw = dict(seed=seed, dtype=torch.bfloat16, head_size=128, num_q_heads=32, num_kv_heads=8,
+              page_size=16, seq_lens=lens, layout=HND, device=device, gen_device=gen_device)
+    if uniform:
+        return make_case("varlen_batch_padded", max_query_len=max_draft, **kw)
+    return make_varlen_case("varlen_batch", q_lens=q_lens, pad_tokens=pad_tokens,
+                            max_query_len=max_draft, **kw)

@@ -305,10 +305,89 @@ def pin_widen_exact(lib=None):
             assert (math.isnan(got) and math.isnan(r)) or got == r, (dt, hex(w), got, r)
 
 
+def _varlen_case(q_lens, seq_lens, pad=0, **kw):
+    base = dict(seed=4, dtype=torch.float16, head_size=16, num_q_heads=4, num_kv_heads=2,
+                page_size=4, seq_lens=seq_lens, layout=W.HND)
+    base.update(kw)
+    return W.make_varlen_case("pin_varlen", q_lens=q_lens, pad_tokens=pad, **base)
+
+
+def pin_varlen_uniform(lib=None):
+    """Equal query lengths M with query_start = [0, M, 2M, ...] are the
+    uniform batch: the same outputs, bit for bit."""
+    M = 3
+    c = _case(seq_lens=[17, 5, 9], max_query_len=M, window=4, seed=6)
+    o = oracle.attention(c, lib=lib)
+    qsl = [M * s for s in range(4)]
+    v = W.DecodeCase(**{**c.__dict__, "query_start": torch.tensor(qsl, dtype=torch.int32),
+                        "query_start_host": qsl})
+    assert np.array_equal(oracle.attention(v, lib=lib), o)
+
+
+def pin_varlen_request_alone(lib=None):
+    """Each request of a mixed batch (lengths 3, 0, 1, 5, 2, a window) gives
+    the outputs of a uniform call of that request alone with M = its q_len,
+    on the same cache and block-table row."""
+    q_lens, lens = [3, 0, 1, 5, 2], [14, 6, 1, 23, 2]
+    c = _varlen_case(q_lens, lens, pad=2, window=6)
+    o = oracle.attention(c, lib=lib)
+    qsl = c.query_start_host
+    for s, m in enumerate(q_lens):
+        if m == 0:
+            continue
+        c1 = W.DecodeCase(**{**c.__dict__, "q": c.q[qsl[s]:qsl[s + 1]].clone(),
+                             "block_table": c.block_table[s:s + 1].clone(),
+                             "seq_lens": c.seq_lens[s:s + 1].clone(), "seq_lens_host": None,
+                             "max_query_len": m, "query_start": None, "query_start_host": None})
+        assert np.array_equal(oracle.attention(c1, lib=lib), o[qsl[s]:qsl[s + 1]])
+
+
+def pin_varlen_padding_zero(lib=None):
+    """Tokens at and past query_start[S] belong to no request: zeros; the
+    rows of the requests are not all zero."""
+    c = _varlen_case([2, 1], [9, 4], pad=3)
+    o = oracle.attention(c, lib=lib)
+    assert np.all(o[3:] == 0.0) and np.abs(o[:3]).max() > 0
+
+
+def pin_varlen_library_sdpa(lib=None):
+    """Against torch's scaled_dot_product_attention (fp64) on densely
+    gathered keys, each token's request found with numpy's right-sided
+    searchsorted over query_start[1:] and its key length seq_len - q_len +
+    (t - query_start[r]) + 1 (the query maps of the pages)."""
+    q_lens, lens, window = [2, 4, 0, 1, 3], [19, 8, 5, 1, 30], 5
+    c = _varlen_case(q_lens, lens, pad=1, window=window, num_q_heads=8, head_size=32,
+                     page_size=8, dtype=torch.bfloat16, seed=12)
+    o = oracle.attention(c, lib=lib)
+    qsl = np.asarray(c.query_start_host)
+    T = c.q.shape[0]
+    req = np.searchsorted(qsl[1:], np.arange(T), side="right")
+    G = 4
+    for t in range(T):
+        r = int(req[t])
+        if r >= len(q_lens):
+            assert np.all(o[t] == 0.0)
+            continue
+        L = lens[r]
+        klen = max(L - q_lens[r] + (t - int(qsl[r])) + 1, 0)
+        lo = max(0, klen - window)
+        if klen <= lo:
+            assert np.all(o[t] == 0.0)
+            continue
+        K = np.stack([_logical_rows(c, "k", r, h) for h in range(2)])
+        V = np.stack([_logical_rows(c, "v", r, h) for h in range(2)])
+        Kt = torch.from_numpy(K).repeat_interleave(G, dim=0)[:, lo:klen]
+        Vt = torch.from_numpy(V).repeat_interleave(G, dim=0)[:, lo:klen]
+        Q = c.q[t:t + 1].double().permute(1, 0, 2)  # [Hq, 1, D]
+        ref = torch.nn.functional.scaled_dot_product_attention(Q, Kt, Vt, scale=c.scale)
+        np.testing.assert_allclose(o[t], ref.permute(1, 0, 2)[0].numpy(), rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_single_key, pin_identical_keys_mean, pin_zero_query_mean, pin_position_mean,
     pin_window_one, pin_wide_window_is_full, pin_page_permutation, pin_layouts,
     pin_split_merge, pin_causal_rows, pin_gqa_is_repeated_mha, pin_gqa_group_of_head,
     pin_one_hot_logit, pin_two_keys_logistic, pin_empty_rows_zero, pin_poison_never_read,
-    pin_library_sdpa, pin_widen_exact,
+    pin_library_sdpa, pin_widen_exact, pin_varlen_uniform, pin_varlen_request_alone,
+    pin_varlen_padding_zero, pin_varlen_library_sdpa,
 ]

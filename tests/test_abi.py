@@ -19,7 +19,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = pd.declared_symbols()
-    assert len(names) == 9
+    assert len(names) == 10
     for n in names:
         assert hasattr(lib, n), n
 
@@ -165,6 +165,32 @@ def test_argument_checks_on_host():
     # a well-formed call on a machine without an sm_103 device
     if not torch.cuda.is_available():
         assert _call(c) == -8
+
+
+def test_varlen_argument_checks_on_host():
+    """The variable-length call refuses a missing or malformed query_start
+    and rows that do not match before any CUDA call."""
+    c = W.make_varlen_case("abi_varlen", seed=1, q_lens=[2, 0, 3], pad_tokens=1,
+                           dtype=torch.float16, head_size=128, num_q_heads=8, num_kv_heads=2,
+                           page_size=16, seq_lens=[40, 7, 19])
+
+    def call(**over):
+        a = dict(q=c.q, k_cache=c.k_cache, v_cache=c.v_cache, block_table=c.block_table,
+                 seq_lens=c.seq_lens, query_start=c.query_start, out=torch.empty_like(c.q),
+                 num_q_heads=8, num_kv_heads=2, head_size=128, page_size=16,
+                 max_query_len=c.max_query_len, window=0, scale=c.scale, layout=c.layout)
+        a.update(over)
+        return pd.paged_decode_attn_varlen(**a, stream=0, check=False)
+
+    assert call(query_start=c.query_start[:3]) == -1          # S + 1 entries
+    assert call(query_start=c.query_start.long()) == -2       # int32
+    assert call(query_start=c.query_start.view(1, -1)) == -1
+    assert call(out=torch.empty(c.q.shape[0] + 1, 8, 128, dtype=c.q.dtype)) == -1
+    assert call(max_query_len=9) == -4
+    assert pd.lib().paged_decode_attn_varlen(*([None] * 7), 8, 2, 128, 16, 3, 0, 1.0, 1,
+                                             None, None, None) == -1
+    if not torch.cuda.is_available():
+        assert call() == -8
 
 
 def test_plan_tensor_memory_path():

@@ -252,3 +252,69 @@ def test_scales_of_any_sign(scale):
                        num_kv_heads=4, page_size=16, max_query_len=3, seq_lens=[1500, 40],
                        layout=W.HND, scale=scale)
     _parity(case)
+
+
+# ---- decode batches with a query length per request (query_start) ----------
+
+@pytest.mark.parametrize("q_lens,lens,pad,D,layout,dtype,window,P,opts", [
+    # mixed lengths with an empty request and padding tokens (a batch)
+    ([1, 4, 2, 0, 3, 8, 5, 1], [900, 37, 2000, 15, 1, 700, 64, 3], 5, 128, W.HND,
+     torch.bfloat16, 0, 16, None),
+    # the same, merges forced: last arriver, cooperative
+    ([1, 4, 2, 0, 3, 8, 5, 1], [900, 37, 2000, 15, 1, 700, 64, 3], 5, 128, W.HND,
+     torch.bfloat16, 0, 16, "merge1"),
+    ([2, 3, 1, 4], [3000, 1200, 40, 2500], 0, 128, W.HND, torch.bfloat16, 0, 16, "merge2"),
+    # sliding window, wide heads, NHD, small heads
+    ([4, 1, 3], [1500, 600, 2100], 2, 256, W.HND, torch.float16, 100, 32, None),
+    ([2, 7, 1], [300, 77, 9], 1, 64, W.NHD, torch.bfloat16, 0, 16, None),
+    ([5, 2], [2200, 48], 0, 512, W.HND, torch.float16, 0, 16, None),
+    # one request shorter than the planned M: many segments, cooperative merge
+    ([3], [9000], 4, 128, W.HND, torch.bfloat16, 0, 16, None),
+])
+def test_varlen(q_lens, lens, pad, D, layout, dtype, window, P, opts):
+    G = 4 if D <= 256 else 8
+    case = W.make_varlen_case("varlen", seed=40 + len(q_lens), q_lens=q_lens, pad_tokens=pad,
+                              dtype=dtype, head_size=D, num_q_heads=2 * G, num_kv_heads=2,
+                              page_size=P, seq_lens=lens, layout=layout, window=window,
+                              max_query_len=8 if len(q_lens) == 1 else None)
+    o = {None: None, "merge1": pd.options(merge=1),
+         "merge2": pd.options(merge=2, row_groups=1, segments=16)}[opts]
+    out, _ = _parity(case, opts=o)
+    t_end = case.query_start_host[-1]
+    assert torch.all(out[t_end:] == 0), "padding rows not zero"
+
+
+def test_varlen_rejects_tensor_memory_path_and_bad_shapes():
+    case = W.make_varlen_case("varlen_args", seed=50, q_lens=[2, 1], dtype=torch.bfloat16,
+                              head_size=128, num_q_heads=8, num_kv_heads=2, page_size=16,
+                              seq_lens=[100, 20])
+    g = case.to("cuda")
+    out = torch.empty_like(g.q)
+    args = (g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens)
+    tail = (g.num_q_heads, g.num_kv_heads, g.head_size, g.page_size, g.max_query_len, g.window,
+            g.scale, g.layout, scratch_for(case))
+    assert pd.paged_decode_attn_varlen(*args, g.query_start, out, *tail,
+                                       opts=pd.options(path=3), check=False) == -1
+    assert pd.paged_decode_attn_varlen(*args, g.query_start[:2], out, *tail, check=False) == -1
+    assert pd.paged_decode_attn_varlen(*args, g.query_start.to(torch.int64), out, *tail,
+                                       check=False) < 0
+    torch.cuda.synchronize()
+    assert pd.paged_decode_device_status(reset=True) == 0
+
+
+def test_varlen_out_of_order_query_start_is_clamped_and_reported():
+    """A decreasing query_start and one past the rows are clamped on the
+    device (no access outside q and out) and reported as PD_DEV_BAD_QSTART."""
+    case = W.make_varlen_case("varlen_bad", seed=51, q_lens=[3, 2, 2], dtype=torch.bfloat16,
+                              head_size=128, num_q_heads=8, num_kv_heads=2, page_size=16,
+                              seq_lens=[300, 90, 40])
+    g = case.to("cuda")
+    g.query_start = torch.tensor([0, 5, 2, 40], dtype=torch.int32, device="cuda")
+    sentinel = torch.full((4, g.q.shape[1], g.q.shape[2]), 7.0, dtype=g.q.dtype, device="cuda")
+    out_full = torch.cat([torch.empty_like(g.q), sentinel])
+    out = out_full[: g.q.shape[0]]
+    pd.decode_case(g, out=out, scratch=scratch_for(case))
+    torch.cuda.synchronize()
+    assert torch.all(out_full[g.q.shape[0]:] == 7.0), "a row past out was written"
+    assert torch.isfinite(out.float()).all()
+    assert pd.paged_decode_device_status(reset=True) == pd.DEV_BAD_QSTART

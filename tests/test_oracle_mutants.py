@@ -18,7 +18,15 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "paged_decode_oracle.c")
 
 MUTANTS = {
-    "causal_off_by_one": ("int64_t n = L - a->M + i + 1;", "int64_t n = L - a->M + i;"),
+    "causal_off_by_one": ("n = (int64_t)a->seq_lens[s] - a->M + (t % a->M) + 1;",
+                          "n = (int64_t)a->seq_lens[s] - a->M + (t % a->M);"),
+    "varlen_left_search": ("if (a->qsl[mid + 1] <= t)", "if (a->qsl[mid + 1] < t)"),
+    "varlen_klen_off_by_one": ("n = (int64_t)a->seq_lens[s] - q_len + (t - a->qsl[s]) + 1;",
+                               "n = (int64_t)a->seq_lens[s] - q_len + (t - a->qsl[s]);"),
+    "varlen_uniform_qlen": ("n = (int64_t)a->seq_lens[s] - q_len + (t - a->qsl[s]) + 1;",
+                            "n = (int64_t)a->seq_lens[s] - a->M + (t - a->qsl[s]) + 1;"),
+    "varlen_padding_kept": ("if (s >= a->num_seqs) return 0;",
+                            "if (s >= a->num_seqs) s = a->num_seqs - 1;"),
     "window_off_by_one": ("*lo = n - a->window;", "*lo = n - a->window + 1;"),
     "gqa_modulo": ("int h = hq / G;", "int h = hq % a->Hkv;"),
     "dropped_scale": ("x[k - lo] = a->scale * dot;", "x[k - lo] = dot;"),
