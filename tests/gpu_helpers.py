@@ -46,15 +46,19 @@ def check(case_cpu, gpu_out, rows=None, tol=None, ref=None):
 
 def sample_rows(case, n, seed=0):
     """n (token row, q head) pairs spread over the call, always including
-    the first and last rows of every sequence."""
+    the first and last rows of every sequence (of every request, with
+    variable query lengths) and the call's last row."""
     g = np.random.default_rng(seed)
     T, Hq = case.q.shape[0], case.num_q_heads
     n = min(n, T * Hq)  # a small call has fewer rows than asked for
     rows = {(0, 0), (T - 1, Hq - 1)}
     M = case.max_query_len
+    qsl = getattr(case, "query_start_host", None)
     for s in range(case.num_seqs):
-        rows.add((s * M + M - 1, int(g.integers(Hq))))
-        rows.add((s * M, int(g.integers(Hq))))
+        first, last = (s * M, s * M + M - 1) if qsl is None else (qsl[s], qsl[s + 1] - 1)
+        if last >= first:
+            rows.add((last, int(g.integers(Hq))))
+            rows.add((first, int(g.integers(Hq))))
     while len(rows) < n:
         rows.add((int(g.integers(T)), int(g.integers(Hq))))
     return sorted(rows)

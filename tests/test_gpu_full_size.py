@@ -69,3 +69,12 @@ def test_batched_hybrid_pages_full():
     empty = [s for s, L in enumerate(case.seq_lens_host) if L == 0]
     for s in empty:
         assert torch.all(out[s * 4:(s + 1) * 4] == 0)
+
+
+def test_varlen_batch_full():
+    """The variable-length batch of bench.py --workload varlen (32 requests,
+    drafts of 1-4 tokens, contexts 1k-16k, bf16 D=128 32/8) plus padding
+    rows, which must be zero."""
+    case = W.varlen_spec_decode_batch(seed=7, pad_tokens=6, device="cuda", gen_device="cuda")
+    out = _full_size(case, seed=7)
+    assert torch.all(out[case.query_start_host[-1]:] == 0)
