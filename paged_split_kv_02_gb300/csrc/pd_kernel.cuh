@@ -1,9 +1,13 @@
 // Paged split-KV decode attention on sm_103a.
 //
-// One CTA per (kv head, row group, KV segment), one sequence per grid.y: the
-// work unit of the gfx1151 decode kernel (ROCm/vllm PR #1330, "Kernel"),
-// where all the query rows of a kv head share a CTA so that its K and V are
-// read from memory once, and a batch puts one sequence on each grid row.
+// One CTA per (KV segment, kv head x row group, sequence) = blockIdx (x, y,
+// z): the work unit of the gfx1151 decode kernel (ROCm/vllm PR #1330,
+// "Kernel"), where all the query rows of a kv head share a CTA so that its K
+// and V are read from memory once, and a batch puts one sequence on each
+// grid slice.  A sequence's query rows are s * M .. s * M + M - 1, or, with
+// variable query lengths, query_start[s] .. query_start[s+1] - 1 (the query
+// maps of the vLLM ROCm Octave backend, _fill_query_maps); packed rows are
+// token-major, so a shorter request only shortens the CTA's valid rows.
 //
 // Warp roles
 //   * one producer warp: per 32 KiB ring stage, TMA-loads the K and V
