@@ -270,6 +270,8 @@ def test_scales_of_any_sign(scale):
     ([5, 2], [2200, 48], 0, 512, W.HND, torch.float16, 0, 16, None),
     # one request shorter than the planned M: many segments, cooperative merge
     ([3], [9000], 4, 128, W.HND, torch.bfloat16, 0, 16, None),
+    # seq_len below q_len: the first tokens of those requests see no key
+    ([5, 4, 2], [3, 1, 700], 1, 128, W.HND, torch.bfloat16, 0, 16, None),
 ])
 def test_varlen(q_lens, lens, pad, D, layout, dtype, window, P, opts):
     G = 4 if D <= 256 else 8
@@ -282,6 +284,18 @@ def test_varlen(q_lens, lens, pad, D, layout, dtype, window, P, opts):
     out, _ = _parity(case, opts=o)
     t_end = case.query_start_host[-1]
     assert torch.all(out[t_end:] == 0), "padding rows not zero"
+
+
+def test_varlen_window_pages_only():
+    """A windowed batch whose block table holds only the pages the window
+    reaches for the longest query (earlier entries point at a NaN page):
+    shorter requests must not read before their own window either."""
+    for w in (1, 17, 300):
+        case = W.make_varlen_case("varlen_win", seed=52, q_lens=[1, 4, 2, 3], pad_tokens=2,
+                                  dtype=torch.float16, head_size=256, num_q_heads=8,
+                                  num_kv_heads=1, page_size=32, seq_lens=[1500, 900, 40, 2600],
+                                  layout=W.HND, window=w, window_pages_only=True)
+        _parity(case)
 
 
 def test_varlen_rejects_tensor_memory_path_and_bad_shapes():
