@@ -339,30 +339,60 @@ def run_ours(args, world, rank, local):
 
 
 def measure_e2e(pd, cases, outs, scratch, stream, keys, args):
-    """The same sweep through the C ABI with pinned host buffers: every step
-    copies each case's q, block table and seq_lens host->device, runs the
-    call and copies the output back."""
-    host_in, dev_in, host_out = {}, {}, {}
-    for k in keys:
+    """The same sweep through the C ABI with pinned host buffers, driven the
+    way a serving loop would: each step copies every case's q, block table
+    and seq_lens host->device in one transfer (one pinned staging buffer),
+    makes the C calls with descriptors built once, and copies every output
+    back in one transfer before the step's single synchronisation."""
+    import ctypes
+
+    def layout_of(tensors):
+        offs, off = [], 0
+        for t in tensors:
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, off
+
+    ins = [t for k in keys for t in (cases[k][0].q, cases[k][0].block_table, cases[k][0].seq_lens)]
+    in_offs, in_bytes = layout_of(ins)
+    out_shapes = [cases[k][0].q for k in keys]
+    out_offs, out_bytes = layout_of(out_shapes)
+    dev = ins[0].device
+    host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    dev_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+    host_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+    dev_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+
+    def view(buf, off, like):
+        n = like.numel() * like.element_size()
+        return buf[off:off + n].view(like.dtype).view(like.shape)
+
+    for t, off in zip(ins, in_offs):
+        view(host_in, off, t).copy_(t.cpu())
+    lib = pd.lib()
+    calls = []
+    for i, k in enumerate(keys):
         c = cases[k][0]
-        host_in[k] = [t.cpu().pin_memory() for t in (c.q, c.block_table, c.seq_lens)]
-        dev_in[k] = [torch.empty_like(t) for t in (c.q, c.block_table, c.seq_lens)]
-        host_out[k] = torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for k in keys for t in host_in[k])
-    d2h = sum(host_out[k].numel() * host_out[k].element_size() for k in keys)
+        q, bt, sl = (view(dev_in, in_offs[3 * i + j], t)
+                     for j, t in enumerate((c.q, c.block_table, c.seq_lens)))
+        o = view(dev_out, out_offs[i], c.q)
+        descs = [pd.tensor_desc(t) for t in (q, c.k_cache, c.v_cache, bt, sl, o)]
+        cargs = [ctypes.byref(d) for d in descs] + [
+            c.num_q_heads, c.num_kv_heads, c.head_size, c.page_size, c.max_query_len, c.window,
+            ctypes.c_float(c.scale), c.layout, ctypes.byref(scratch.desc),
+            ctypes.c_void_p(stream.cuda_stream)]
+        calls.append((descs, cargs))
+    h2d, d2h = in_bytes, out_bytes
     kv_step = sum(cases[k][0].kv_bytes_touched() for k in keys)
 
     def step():
         with torch.cuda.stream(stream):
-            for k in keys:
-                for d, h in zip(dev_in[k], host_in[k]):
-                    d.copy_(h, non_blocking=True)
-                c = cases[k][0]
-                pd.paged_decode_attn(dev_in[k][0], c.k_cache, c.v_cache, dev_in[k][1],
-                                     dev_in[k][2], outs[k][0], c.num_q_heads, c.num_kv_heads,
-                                     c.head_size, c.page_size, c.max_query_len, c.window,
-                                     c.scale, c.layout, scratch, stream)
-                host_out[k].copy_(outs[k][0], non_blocking=True)
+            dev_in.copy_(host_in, non_blocking=True)
+            for _, a in calls:
+                rc = lib.paged_decode_attn(*a)
+                if rc != 0:
+                    raise RuntimeError(f"paged_decode_attn: {rc}")
+            host_out.copy_(dev_out, non_blocking=True)
         stream.synchronize()
 
     for _ in range(args.warmup):
@@ -372,7 +402,9 @@ def measure_e2e(pd, cases, outs, scratch, stream, keys, args):
         step()
     dt = (time.perf_counter() - t0) / args.steps
     return {"value": round(kv_step / dt / 1e9, 1), "unit": UNIT, "ms_per_step": round(dt * 1e3, 4),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "transfers": "one pinned host->device copy of every call's inputs and one "
+                         "device->host copy of every output per step"}
 
 
 def _oracle_sweep(host_cases, keys, nthreads):
