@@ -416,17 +416,23 @@ def _oracle_sweep(host_cases, keys, nthreads):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(cases, keys):
-    """The fp64 oracle on the host cores over one call of every case."""
+def cpu_baseline(cases, keys, min_seconds=10.0, max_sweeps=200):
+    """The fp64 oracle on the host cores, repeating one call of every case
+    until at least `min_seconds` have passed (a bounded sample)."""
     import oracle
 
     oracle.build()
     host = {k: cases[k][0].to("cpu") for k in keys}
     n = oracle.default_threads()
-    dt = _oracle_sweep(host, keys, n)
+    dt, sweeps = 0.0, 0
+    while dt < min_seconds and sweeps < max_sweeps:
+        dt += _oracle_sweep(host, keys, n)
+        sweeps += 1
     kv = sum(host[k].kv_bytes_touched() for k in keys)
-    return {"value": round(kv / dt / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
-            "sample": "one call of each of the 20 sweep cases (all heads), fp64 C oracle",
+    return {"value": round(sweeps * kv / dt / 1e9, 4), "unit": UNIT, "cores": n,
+            "kind": "oracle",
+            "sample": f"{sweeps} repetitions of one call of each of the {len(keys)} sweep "
+                      "cases (all heads), fp64 C oracle",
             "seconds": round(dt, 2)}
 
 
