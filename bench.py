@@ -49,6 +49,8 @@ WORKLOAD = ("spec-decode sweep: bf16, head_size 128, 32 q / 8 kv heads, page_siz
 # M4_L32768.md (M=4, 32768 keys).  It holds for the kernel sources the
 # capture was taken on only: with any other sources `traffic` is null.
 TRAFFIC_CAPTURE = {"sources": "3e59f272d0324eaa", "dram_over_algorithmic": 1.0238}
+# the same for the variable-length batch (one capture of an 8-request batch)
+VARLEN_TRAFFIC_CAPTURE = {"sources": "3e59f272d0324eaa", "dram_over_algorithmic": 1.0115}
 
 
 def _kernel_sources_digest() -> str:
@@ -516,12 +518,13 @@ def run_varlen(args, world, rank, local):
     props = torch.cuda.get_device_properties(local)
     l2 = int(getattr(props, "L2_cache_size", 126 << 20))
     peak, peak_kind = _peaks()
-    probe = W.varlen_spec_decode_batch(seed=0)
+    nreq = args.requests
+    probe = W.varlen_spec_decode_batch(seed=0, num_seqs=nreq)
     n_rep = max(2, math.ceil(2.2 * l2 / probe.kv_bytes_touched()))
-    var = [W.varlen_spec_decode_batch(seed=r, device=device, gen_device=device)
+    var = [W.varlen_spec_decode_batch(seed=r, num_seqs=nreq, device=device, gen_device=device)
            for r in range(n_rep)]
-    uni = [W.varlen_spec_decode_batch(seed=r, uniform=True, device=device, gen_device=device)
-           for r in range(n_rep)]
+    uni = [W.varlen_spec_decode_batch(seed=r, num_seqs=nreq, uniform=True, device=device,
+                                      gen_device=device) for r in range(n_rep)]
     c0 = var[0]
     scratch = pd.Scratch(c0.num_seqs, c0.num_q_heads, c0.num_kv_heads, c0.head_size, 4,
                          max_splits=256, device=device)
@@ -562,13 +565,18 @@ def run_varlen(args, world, rank, local):
     status = pd.paged_decode_device_status(reset=True)
     if rank != 0:
         return
+    traffic, traffic_basis = None, "no ncu capture of these kernel sources"
+    if _kernel_sources_digest() == VARLEN_TRAFFIC_CAPTURE["sources"]:
+        traffic = round(VARLEN_TRAFFIC_CAPTURE["dram_over_algorithmic"] * alg)
+        traffic_basis = ("bytes per launch: the DRAM/algorithmic ratio of one ncu capture of "
+                         "an 8-request batch of this workload x the algorithmic bytes")
     line = {
         "metric": METRIC, "value": round(world * kv / (us * 1e-6) / 1e9, 1), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(us * 1e-3, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/K/V, random page permutation)",
-        "config": {"workload": VARLEN_WORKLOAD,
+        "config": {"workload": VARLEN_WORKLOAD.replace("32 requests", f"{nreq} requests"),
                    "l2": f"inputs larger than L2: {n_rep} rotating replicas",
                    "timing": "CUDA graph of the calls, CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
@@ -577,8 +585,8 @@ def run_varlen(args, world, rank, local):
         "padded_uniform_us_per_call": round(us_u, 3),
         "roofline": {"bound": "hbm", "achieved": round(alg / (us * 1e-6) / 1e9, 1),
                      "peak": peak, "unit": "GB/s",
-                     "frac": round(alg / (us * 1e-6) / 1e9 / peak, 4), "traffic": None,
-                     "traffic_basis": "no ncu capture of this workload", "peak_kind": peak_kind},
+                     "frac": round(alg / (us * 1e-6) / 1e9 / peak, 4), "traffic": traffic,
+                     "traffic_basis": traffic_basis, "peak_kind": peak_kind},
         "clocks": clk.summary(),
         "e2e": None,
         "cpu_baseline": cpu,
@@ -597,6 +605,8 @@ def main():
     ap.add_argument("--workload", default="sweep", choices=["sweep", "varlen"],
                     help="sweep: the spec-decode sweep (default); varlen: a batch with a "
                          "query length per request")
+    ap.add_argument("--requests", type=int, default=32,
+                    help="requests of the varlen batch (fewer for profiling runs)")
     ap.add_argument("--cases", default="",
                     help="restrict the sweep, e.g. 4:32768,1:4096 (profiling runs only)")
     args = ap.parse_args()
