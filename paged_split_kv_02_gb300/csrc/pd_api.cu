@@ -190,7 +190,7 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   if (D != 64 && D != 128 && D != 256 && D != 512) return PD_EHEAD;
   if (M < 1 || M > 8) return PD_EQLEN;
   // path: 0 = auto (mma.sync), 1 = mma.sync, 3 = tcgen05 with tensor memory
-  // (D <= 256); the warp-dot path (2) is not part of this build
+  // (D <= 256); the warp-dot path (2) is not built
   if (o.path < 0 || o.path > 3 || o.path == 2) return PD_EINVAL;
   const bool tc = o.path == 3;
   if (tc && D > 256) return PD_EINVAL;
