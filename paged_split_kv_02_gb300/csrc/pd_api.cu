@@ -259,8 +259,14 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
     // (fewer, longer segments measured faster than ~4 waves: 300 -> 288 us
     // for 64 sequences of U[1, 16384] keys at D=256; the last-arriver merge
     // of a (sequence, kv head) then reads fewer parts)
+    // Segments are also capped at 384 blocks (6144 keys): with many groups
+    // the estimate alone gives segments of ~9k keys, and the last wave of
+    // such long CTAs runs unbalanced (32 requests x 8 kv heads of 1k-16k
+    // keys: 2 segments 220 us, 3-6 segments 205 us; 64 sequences x 2 kv
+    // heads at D=256 keep their 4).
     const int64_t est = std::max<int64_t>(1, units * nb_max / 2);
     int64_t sb = std::max(min_seg_blocks, cdiv(2 * est, 3 * target));
+    sb = std::min(sb, std::max<int64_t>(min_seg_blocks, kMaxBatchSegBlocks));
     nseg = cdiv(nb_max, sb);
   }
   nseg = std::max<int64_t>(1, std::min<int64_t>(nseg, nb_max));
