@@ -53,7 +53,7 @@ TRAFFIC_CAPTURE = {"sources": "7a33dd81b07528b5", "dram_over_algorithmic": 1.023
 VARLEN_TRAFFIC_CAPTURE = {"sources": "7a33dd81b07528b5", "dram_over_algorithmic": 1.0115}
 
 
-def _kernel_sources_digest() -> str:
+def _kernel_sources_digest(csrc: str | None = None) -> str:
     """Digest of the CUDA sources with comments and blank lines removed, so
     that a comment edit keeps an ncu capture valid and a code edit does not."""
     import glob
@@ -61,7 +61,9 @@ def _kernel_sources_digest() -> str:
     import re
 
     h = hashlib.sha256()
-    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_split_kv_02_gb300", "csrc")
+    if csrc is None:
+        csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_split_kv_02_gb300",
+                            "csrc")
     for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
                     glob.glob(os.path.join(csrc, "*.h"))):
         h.update(os.path.basename(f).encode())
