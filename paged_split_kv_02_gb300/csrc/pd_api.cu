@@ -253,6 +253,10 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   } else if (S <= 1) {
     nseg = std::max<int64_t>(1, target / std::max<int64_t>(units, 1));
     nseg = std::min(nseg, std::max<int64_t>(1, nb_max / min_seg_blocks));
+    // a CTA that would move at most kNoSplitBytes of K and V alone is not
+    // split: the merge's round trips cost more than the stream time a split
+    // saves (300 keys at D=128: 5.8 us unsplit, 6.6 us in 3 segments)
+    if (nb_max * kBlockKeys * 4LL * D <= kNoSplitBytes) nseg = 1;
   } else {
     // a batch: lengths are only known on the device; aim at ~1.5 waves of
     // equal segments assuming an average length of half the table width

@@ -16,6 +16,7 @@ constexpr int kMaxThreads = 32 * (kMaxConsumerWarps + 1);
 constexpr int kSmemAlign = 1024;      // the 128-byte TMA swizzle repeats every 1 KiB
 constexpr int kBlockIds = 512;        // page ids of 16-key blocks staged in shared memory
 constexpr int kMaxBatchSegBlocks = 384;  // longest planned segment of a batch (6144 keys)
+constexpr int64_t kNoSplitBytes = 256 << 10;  // K+V per (sequence, kv head) left unsplit
 // Tensor-memory path: 4 softmax warps (one per tensor-memory sub-partition)
 // and one warp that issues the tcgen05 MMAs, plus the producer warp; the
 // packed rows (<= 64) are the M = 64 side of every MMA.
