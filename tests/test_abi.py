@@ -193,6 +193,23 @@ def test_varlen_argument_checks_on_host():
         assert call() == -8
 
 
+def test_plan_small_calls_unsplit_and_batch_segments_capped():
+    """A single sequence whose K+V per kv head is at most 256 KiB is one CTA
+    per head; a batch's segments hold at most 384 blocks (6144 keys)."""
+    def plan(S, Hq, Hkv, D, P, M, W_):
+        sd = _fake_scratch(S, Hq, Hkv, D, M, 256)
+        return pd.paged_decode_plan(S, Hq, Hkv, D, P, M, 0, W_, 152, scratch_desc=sd)
+
+    p = plan(1, 8, 2, 128, 16, 1, 19)        # 300 keys, D=128: 152 KiB per head
+    assert p["max_segments"] == 1 and p["merge"] == 0
+    p = plan(1, 32, 8, 128, 16, 4, 64)       # 1k keys: 512 KiB per head, split
+    assert p["max_segments"] > 1
+    p = plan(32, 32, 8, 128, 16, 4, 1013)    # 32 requests of up to 16k keys
+    assert p["seg_blocks"] <= 384 and p["max_segments"] >= 3
+    p = plan(8, 32, 8, 128, 16, 4, 1008)     # fewer groups: the estimate rules
+    assert p["seg_blocks"] < 384
+
+
 def test_plan_tensor_memory_path():
     """path 3: 4 softmax warps + 1 MMA warp + the producer, 16 packed rows
     per CTA (four copies fill the M = 64 side), four partial states."""
