@@ -433,7 +433,14 @@ def cpu_baseline(cases, keys, min_seconds=10.0, max_sweeps=200):
         dt += _oracle_sweep(host, keys, n)
         sweeps += 1
     kv = sum(host[k].kv_bytes_touched() for k in keys)
+    # and on one thread, over the cases up to 4k keys (a bounded sample)
+    small = [k for k in keys if k[1] <= 4096] or list(keys)
+    dt1 = _oracle_sweep(host, small, 1)
+    kv1 = sum(host[k].kv_bytes_touched() for k in small)
     return {"value": round(sweeps * kv / dt / 1e9, 4), "unit": UNIT, "cores": n,
+            "single_thread": {"value": round(kv1 / dt1 / 1e9, 4), "unit": UNIT,
+                              "seconds": round(dt1, 2),
+                              "sample": "one call of each sweep case up to 4096 keys"},
             "kind": "oracle",
             "sample": f"{sweeps} repetitions of one call of each of the {len(keys)} sweep "
                       "cases (all heads), fp64 C oracle",
