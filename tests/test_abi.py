@@ -210,6 +210,18 @@ def test_plan_small_calls_unsplit_and_batch_segments_capped():
     assert p["seg_blocks"] < 384
 
 
+def test_plan_windowed_segments():
+    """A windowed single-sequence call split into row groups takes segments
+    of two blocks; with one row group the usual floor holds."""
+    def plan(M):
+        sd = _fake_scratch(1, 8, 1, 256, M, 256)
+        return pd.paged_decode_plan(1, 8, 1, 256, 32, M, 512, 1024, 152, scratch_desc=sd)
+
+    p4, p1 = plan(4), plan(1)
+    assert p4["row_groups"] == 2 and p4["max_segments"] == 17
+    assert p1["row_groups"] == 1 and p1["max_segments"] == 8
+
+
 def test_plan_tensor_memory_path():
     """path 3: 4 softmax warps + 1 MMA warp + the producer, 16 packed rows
     per CTA (four copies fill the M = 64 side), four partial states."""
