@@ -325,56 +325,79 @@ def single_seq_nhd(seed: int = 0, device: str = "cpu") -> DecodeCase:
 
 
 def spec_decode_hnd(M: int, L: int, seed: int = 0, device: str = "cpu",
-                    gen_device: str = "cpu") -> DecodeCase:
-    """bf16, D=128, 32 q / 8 kv heads, P=16, HND, batch 1, M in 1..4."""
+                    gen_device: str = "cpu", v_mean: float = 0.0,
+                    packed: bool = False) -> DecodeCase:
+    """bf16, D=128, 32 q / 8 kv heads, P=16, HND, batch 1, M in 1..4.
+    ``v_mean`` shifts the V values (outputs stay O(1) at long contexts);
+    ``packed`` stores K and V side by side in one pool."""
     return make_case(
-        f"spec_decode_hnd_bf16_d128_M{M}_L{L}",
+        f"spec_decode_hnd_bf16_d128_M{M}_L{L}" + (f"_vmean{v_mean:g}" if v_mean else "")
+        + ("_packed" if packed else ""),
         seed=seed, dtype=torch.bfloat16, head_size=128, num_q_heads=32,
         num_kv_heads=8, page_size=16, max_query_len=M, seq_lens=[L],
-        layout=HND, device=device, gen_device=gen_device,
+        layout=HND, v_mean=v_mean, packed=packed, device=device, gen_device=gen_device,
     )
 
 
 def sliding_window(dtype: torch.dtype, M: int, L: int, seed: int = 0,
-                   device: str = "cpu", gen_device: str = "cpu") -> DecodeCase:
+                   device: str = "cpu", gen_device: str = "cpu",
+                   v_mean: float = 0.0) -> DecodeCase:
     """D=256, 8 q / 1 kv head, window 512, P=32; the block table holds only
     the pages the window reaches (earlier entries point at a NaN page)."""
     tag = "fp16" if dtype == torch.float16 else "bf16"
     return make_case(
-        f"sliding_window_{tag}_d256_w512_M{M}_L{L}",
+        f"sliding_window_{tag}_d256_w512_M{M}_L{L}" + (f"_vmean{v_mean:g}" if v_mean else ""),
         seed=seed, dtype=dtype, head_size=256, num_q_heads=8, num_kv_heads=1,
         page_size=32, max_query_len=M, seq_lens=[L], layout=HND, window=512,
-        window_pages_only=True, device=device, gen_device=gen_device,
+        window_pages_only=True, v_mean=v_mean, device=device, gen_device=gen_device,
     )
 
 
 def wide_head(M: int, L: int, seed: int = 0, device: str = "cpu",
-              gen_device: str = "cpu") -> DecodeCase:
+              gen_device: str = "cpu", v_mean: float = 0.0,
+              packed: bool = False) -> DecodeCase:
     """fp16, D=512, 8 q / 1 kv head, full causal, P=16, values N(0, 0.5)."""
     return make_case(
-        f"wide_head_fp16_d512_M{M}_L{L}",
+        f"wide_head_fp16_d512_M{M}_L{L}" + (f"_vmean{v_mean:g}" if v_mean else "")
+        + ("_packed" if packed else ""),
         seed=seed, dtype=torch.float16, head_size=512, num_q_heads=8,
         num_kv_heads=1, page_size=16, max_query_len=M, seq_lens=[L],
-        layout=HND, std=0.5, device=device, gen_device=gen_device,
+        layout=HND, std=0.5, v_mean=v_mean, packed=packed, device=device,
+        gen_device=gen_device,
     )
 
 
 def batched_hybrid_pages(seed: int = 0, num_seqs: int = 64, max_len: int = 16384,
-                         device: str = "cpu", gen_device: str = "cpu") -> DecodeCase:
+                         device: str = "cpu", gen_device: str = "cpu", v_mean: float = 0.0,
+                         page_size: int = 1056) -> DecodeCase:
     """bf16, D=256, 16 q / 2 kv heads, P=1056, M=4, 64 sequences with lengths
     uniform in [1, max_len] and one empty (padded) slot; a shared pool with
     10 % slack pages, randomly permuted."""
     g = _gen(seed, _STREAM_LEN)
     lens = torch.randint(1, max_len + 1, (num_seqs,), generator=g).tolist()
     lens[num_seqs // 3] = 0
-    P = 1056
+    P = page_size
     used = sum((L + P - 1) // P for L in lens)
     return make_case(
-        f"batched_hybrid_bf16_d256_P1056_S{num_seqs}",
+        f"batched_hybrid_bf16_d256_P{P}_S{num_seqs}" + (f"_vmean{v_mean:g}" if v_mean else ""),
         seed=seed, dtype=torch.bfloat16, head_size=256, num_q_heads=16,
         num_kv_heads=2, page_size=P, max_query_len=4, seq_lens=lens,
-        layout=HND, pool_pages=used + max(1, used // 10),
+        layout=HND, pool_pages=used + max(1, used // 10), v_mean=v_mean,
         table_width=(max_len + P - 1) // P, device=device, gen_device=gen_device,
+    )
+
+
+def hybrid_page(P: int, M: int, L: int, seed: int = 0, device: str = "cpu",
+                gen_device: str = "cpu", v_mean: float = 0.0, packed: bool = False,
+                layout: int = HND) -> DecodeCase:
+    """One sequence on the page sizes of hybrid attention / state-space
+    models (528, 544, 784, 1056 tokens): bf16, D=256, 16 q / 2 kv heads."""
+    return make_case(
+        f"hybrid_page_bf16_d256_P{P}_M{M}_L{L}" + (f"_vmean{v_mean:g}" if v_mean else "")
+        + ("_packed" if packed else ""),
+        seed=seed, dtype=torch.bfloat16, head_size=256, num_q_heads=16, num_kv_heads=2,
+        page_size=P, max_query_len=M, seq_lens=[L], layout=layout, v_mean=v_mean,
+        packed=packed, device=device, gen_device=gen_device,
     )
 
 
@@ -385,7 +408,7 @@ SPEC_DECODE_M = (1, 2, 3, 4)
 def varlen_spec_decode_batch(seed: int = 0, num_seqs: int = 32, min_len: int = 1024,
                              max_len: int = 16384, max_draft: int = 4, pad_tokens: int = 0,
                              uniform: bool = False, device: str = "cpu",
-                             gen_device: str = "cpu") -> DecodeCase:
+                             gen_device: str = "cpu", v_mean: float = 0.0) -> DecodeCase:
     """Speculative decoding over a batch: bf16, D=128, 32 q / 8 kv heads,
     P=16, HND; request s has 1..max_draft query tokens (seeded) and a context
     uniform in [min_len, max_len].  ``uniform=True`` gives the same requests
@@ -394,8 +417,116 @@ def varlen_spec_decode_batch(seed: int = 0, num_seqs: int = 32, min_len: int = 1
     q_lens = torch.randint(1, max_draft + 1, (num_seqs,), generator=g).tolist()
     lens = torch.randint(min_len, max_len + 1, (num_seqs,), generator=g).tolist()
     kw = dict(seed=seed, dtype=torch.bfloat16, head_size=128, num_q_heads=32, num_kv_heads=8,
-              page_size=16, seq_lens=lens, layout=HND, device=device, gen_device=gen_device)
+              page_size=16, seq_lens=lens, layout=HND, v_mean=v_mean, device=device,
+              gen_device=gen_device)
     if uniform:
         return make_case("varlen_batch_padded", max_query_len=max_draft, **kw)
     return make_varlen_case("varlen_batch", q_lens=q_lens, pad_tokens=pad_tokens,
                             max_query_len=max_draft, **kw)
+
+
+# ---------------------------------------------------------------------------
+# Inputs of the rotary embedding + paged KV-cache write that runs ahead of
+# decode: new tokens' q, k, v, their positions and cache slots, a cos / sin
+# table, and the pools to write into.
+# ---------------------------------------------------------------------------
+
+def rope_cos_sin_table(max_pos: int, rot_dim: int, base: float = 10000.0) -> torch.Tensor:
+    """fp32 [max_pos, rot_dim]: cos of position x frequency i in the first
+    rot_dim/2 columns, sin in the rest, frequency i = base^(-2i/rot_dim)
+    (the table a model's rotary embedding precomputes; computed in fp64 and
+    rounded once)."""
+    i = torch.arange(rot_dim // 2, dtype=torch.float64)
+    inv_freq = base ** (-2.0 * i / rot_dim)
+    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv_freq[None, :]
+    return torch.cat([ang.cos(), ang.sin()], dim=1).to(torch.float32).contiguous()
+
+
+@dataclasses.dataclass
+class RopeCase:
+    """One call's inputs of the rotary embedding + cache write."""
+
+    name: str
+    dtype: torch.dtype
+    head_size: int
+    rot_dim: int
+    is_neox: bool
+    num_q_heads: int
+    num_kv_heads: int
+    page_size: int
+    layout: int
+    q: torch.Tensor            # [T, Hq, D]
+    k: torch.Tensor            # [T, Hkv, D]
+    v: torch.Tensor            # [T, Hkv, D]
+    positions: torch.Tensor    # [T] int32
+    slot_mapping: torch.Tensor  # [T] int32, -1 = padding token
+    cos_sin: torch.Tensor      # [max_pos, rot_dim] fp32
+    k_cache: torch.Tensor      # pool before the call
+    v_cache: torch.Tensor
+    packed: bool = False
+
+    def to(self, device) -> "RopeCase":
+        if self.packed:
+            pool = self.k_cache.as_strided(
+                tuple(list(self.k_cache.shape[:-1]) + [2 * self.head_size]),
+                self.k_cache.stride(), self.k_cache.storage_offset()).to(device)
+            k_cache, v_cache = pool[..., :self.head_size], pool[..., self.head_size:]
+        else:
+            k_cache, v_cache = self.k_cache.to(device), self.v_cache.to(device)
+        return dataclasses.replace(
+            self, q=self.q.to(device), k=self.k.to(device), v=self.v.to(device),
+            positions=self.positions.to(device), slot_mapping=self.slot_mapping.to(device),
+            cos_sin=self.cos_sin.to(device), k_cache=k_cache, v_cache=v_cache)
+
+    def bytes_moved(self) -> int:
+        """q read + q_out written + k, v read + k, v written for every token
+        with a slot, + one table row per token (fp32)."""
+        e = self.q.element_size()
+        T = self.q.shape[0]
+        live = int((self.slot_mapping >= 0).sum())
+        D = self.head_size
+        return (2 * T * self.num_q_heads * D * e + 2 * T * self.num_kv_heads * D * e
+                + 2 * live * self.num_kv_heads * D * e + T * self.rot_dim * 4)
+
+
+def make_rope_case(name: str, *, seed: int, dtype: torch.dtype, num_tokens: int,
+                   num_q_heads: int, num_kv_heads: int, head_size: int, rot_dim: int,
+                   page_size: int, num_pages: int, layout: int = HND, is_neox: bool = True,
+                   max_pos: int = 4096, pad_tokens: int = 0, packed: bool = False,
+                   device: str = "cpu", gen_device: str = "cpu") -> RopeCase:
+    """T = num_tokens new tokens at random distinct positions and random
+    distinct cache slots; the last ``pad_tokens`` of them are padding (slot
+    -1).  The pools hold seeded values before the call, so an untouched slot
+    can be checked bit for bit."""
+    D, P = head_size, page_size
+    T = num_tokens
+    assert num_pages * P >= T and max_pos >= 1
+    g = _gen(seed, _STREAM_PERM)
+    slots = torch.randperm(num_pages * P, generator=g)[:T].to(torch.int32)
+    if pad_tokens:
+        slots[T - pad_tokens:] = -1
+    positions = torch.randint(0, max_pos, (T,), generator=_gen(seed, _STREAM_LEN),
+                              dtype=torch.int64).to(torch.int32)
+    if T:
+        positions[0] = 0                       # position 0 (no rotation) is always in
+        positions[-1] = max_pos - 1            # and the table's last row
+    g_q, g_k, g_v = (_gen(seed, st, gen_device) for st in (_STREAM_Q, _STREAM_K, _STREAM_V))
+    q = _rounded_normal((T, num_q_heads, D), 1.0, 0.0, dtype, g_q, gen_device)
+    k = _rounded_normal((T, num_kv_heads, D), 1.0, 0.0, dtype, g_k, gen_device)
+    v = _rounded_normal((T, num_kv_heads, D), 1.0, 0.0, dtype, g_v, gen_device)
+    shape_pool = (num_pages, P, num_kv_heads, D) if layout == NHD else (num_pages, num_kv_heads, P, D)
+    g_pool = _gen(seed + 1, _STREAM_K, gen_device)
+    if packed:
+        full = list(shape_pool)
+        full[-1] = 2 * D
+        pool = _rounded_normal(tuple(full), 1.0, 0.0, dtype, g_pool, gen_device)
+        k_cache, v_cache = pool[..., :D], pool[..., D:]
+    else:
+        k_cache = _rounded_normal(shape_pool, 1.0, 0.0, dtype, g_pool, gen_device)
+        v_cache = _rounded_normal(shape_pool, 1.0, 0.0, dtype, g_pool, gen_device)
+    case = RopeCase(name=name, dtype=dtype, head_size=D, rot_dim=rot_dim, is_neox=is_neox,
+                    num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, page_size=P,
+                    layout=layout, q=q, k=k, v=v, positions=positions, slot_mapping=slots,
+                    cos_sin=rope_cos_sin_table(max_pos, rot_dim), k_cache=k_cache,
+                    v_cache=v_cache, packed=packed)
+    return case.to(device)
