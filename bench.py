@@ -45,9 +45,9 @@ WORKLOAD = ("spec-decode sweep: bf16, head_size 128, 32 q / 8 kv heads, page_siz
 
 
 # DRAM bytes (read + write) over algorithmic bytes of the decode kernel, from
-# the ncu capture summarised in profiles/pd_decode_mma_d128_bf16_spec_decode_
-# M4_L32768.md (M=4, 32768 keys).  It holds for the kernel sources the
-# capture was taken on only: with any other sources `traffic` is null.
+# one ncu capture of the spec-decode case M=4, 32768 keys.  It holds for the
+# kernel sources the capture was taken on only: with any other sources
+# `traffic` is null.
 TRAFFIC_CAPTURE = {"sources": "224766cf43d51fc3", "dram_over_algorithmic": 1.0238}
 # the same for the variable-length batch (one capture of an 8-request batch)
 VARLEN_TRAFFIC_CAPTURE = {"sources": "224766cf43d51fc3", "dram_over_algorithmic": 1.0115}

@@ -102,6 +102,16 @@ typedef enum {
 #define PD_DEV_BAD_PAGE     0x2u  /* a block-table entry outside the pool   */
 #define PD_DEV_BAD_SEQLEN   0x4u  /* seq_len > block-table width * page_size */
 #define PD_DEV_BAD_QSTART   0x8u  /* query_start out of order or out of range */
+#define PD_DEV_BAD_SCRATCH  0x10u /* a split-KV counter did not start the call at
+                                     zero: the scratch served two overlapping
+                                     calls, or a merger gave up waiting
+                                     (PD_DEV_WAIT_TIMEOUT) in an earlier call;
+                                     the groups concerned are not merged and
+                                     the scratch must be initialised again */
+
+/* int32 counters a scratch reserves per (sequence, kv head): an arrival
+ * count and a finished-merger count for each of up to 8 row groups. */
+#define PD_COUNTERS_PER_PAIR 16
 
 /* Bytes of scratch for calls of up to `max_num_seqs` sequences
  * (scratch_bytes: 4 * (rows * D + 2 * rows + counters) per sequence).
@@ -111,11 +121,15 @@ typedef enum {
 PD_API size_t paged_decode_scratch_bytes(int max_num_seqs, int num_q_heads, int num_kv_heads,
                                   int head_size, int max_query_len, int max_splits);
 
-/* Prepare a scratch buffer: record its counter area and zero the counters
- * once, asynchronously on `stream` (as the RDNA backend's make_scratch does:
- * the calls leave them at zero afterwards).  `data` must stay allocated
- * while calls use it.
- * Call it outside graph capture. */
+/* Prepare a scratch buffer: record its counter area (PD_COUNTERS_PER_PAIR
+ * int32 per (sequence, kv head)) and zero the counters once, asynchronously
+ * on `stream` (as the RDNA backend's make_scratch does: the calls leave them
+ * at zero afterwards).  `data` must stay allocated while calls use it.
+ * Call it outside graph capture.  Call it again on a buffer after a call
+ * that reported PD_DEV_WAIT_TIMEOUT or PD_DEV_BAD_SCRATCH: a merger that
+ * gave up leaves its group's counter deliberately out of range, and every
+ * later call on that buffer skips the merge of that group (reporting
+ * PD_DEV_BAD_SCRATCH) until the counters are zeroed again. */
 PD_API int paged_decode_scratch_init(pd_scratch *scratch, void *data, size_t bytes, int max_num_seqs,
                               int num_kv_heads, void *stream);
 
@@ -155,6 +169,10 @@ typedef struct pd_options {
   int merge;         /* split-KV merge: 0 = auto, 1 = the last-arriving CTA,
                         2 = the last K arrivals of a co-resident (cooperative)
                         grid, one D/K slice each                                */
+  int wait_limit_us; /* how long a cooperative merger waits for the remaining
+                        arrivals before it gives up and reports
+                        PD_DEV_WAIT_TIMEOUT (0 = one second); for tests of
+                        that path                                              */
 } pd_options;
 
 /* paged_decode_attn with explicit knobs (opts may be NULL). */
@@ -214,10 +232,10 @@ PD_API int paged_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, in
 /* Size of the scratch array compiled into the library for
  * paged_decode_attn_static, and the part of it kept for counters. */
 #define PD_STATIC_SCRATCH_BYTES (16u << 20)
-#define PD_STATIC_COUNTER_BYTES (256u << 10)
+#define PD_STATIC_COUNTER_BYTES (512u << 10)
 
-/* The decode call without caller scratch.  Not from the paper: it has no
- * counterpart there.  For callers that cannot allocate device memory (a host
+/* The decode call without caller scratch.  The paper has no counterpart to
+ * it.  For callers that cannot allocate device memory (a host
  * framework that owns all device allocation, a runtime that forbids
  * allocation after start-up, an integration that only hands over inputs and
  * outputs), the split-KV scratch is a fixed array of
@@ -233,8 +251,11 @@ PD_API int paged_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, in
  *   - Every call shares the one array: calls that overlap on the GPU (on two
  *     streams, or two host threads) race on it.  Serialise them.
  *   - A call whose sequences x kv heads need more than
- *     PD_STATIC_COUNTER_BYTES of counters (8 int32 per pair, i.e. more than
- *     8192 pairs) returns PD_ESCRATCH. */
+ *     PD_STATIC_COUNTER_BYTES of counters (PD_COUNTERS_PER_PAIR int32 per
+ *     pair, i.e. more than 8192 pairs) returns PD_ESCRATCH before it
+ *     touches the device.
+ *   - On a device that is not sm_103 it returns PD_ENODEV, as the other
+ *     entry points do. */
 PD_API int paged_decode_attn_static(const pd_tensor *q, const pd_tensor *k_cache,
                                     const pd_tensor *v_cache, const pd_tensor *block_table,
                                     const pd_tensor *seq_lens, pd_tensor *out, int num_q_heads,

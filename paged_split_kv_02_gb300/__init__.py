@@ -36,6 +36,8 @@ STATUS_NAMES = {
     -5: "PD_EALIGN", -6: "PD_ESCRATCH", -7: "PD_ECUDA", -8: "PD_ENODEV",
 }
 DEV_WAIT_TIMEOUT, DEV_BAD_PAGE, DEV_BAD_SEQLEN, DEV_BAD_QSTART = 0x1, 0x2, 0x4, 0x8
+DEV_BAD_SCRATCH = 0x10
+COUNTERS_PER_PAIR = 16  # PD_COUNTERS_PER_PAIR
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
                       "paged_decode.h")
@@ -60,7 +62,7 @@ class PdScratch(ctypes.Structure):
 class PdOptions(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("segments", "row_groups", "key_groups", "stages", "cluster", "path",
-                 "max_ctas_hint", "merge")]
+                 "max_ctas_hint", "merge", "wait_limit_us")]
 
 
 class PdPlan(ctypes.Structure):
@@ -193,8 +195,15 @@ class Scratch:
         off = (-self.buffer.data_ptr()) % 256
         self.view = self.buffer[off: off + int(nbytes)]
         self.desc = PdScratch()
+        self._init_args = (int(max_num_seqs), int(num_kv_heads))
+        self.reinit(stream)
+
+    def reinit(self, stream=None):
+        """``paged_decode_scratch_init`` again on the same buffer: zero the
+        counters (needed after a call reported a wait timeout or a bad
+        scratch)."""
         rc = lib().paged_decode_scratch_init(ctypes.byref(self.desc), self.view.data_ptr(),
-                                             int(nbytes), int(max_num_seqs), int(num_kv_heads),
+                                             int(self.view.numel()), *self._init_args,
                                              _stream_handle(stream))
         if rc != PD_OK:
             raise PagedDecodeError(rc, "paged_decode_scratch_init")

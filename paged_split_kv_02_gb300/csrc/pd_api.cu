@@ -10,6 +10,7 @@
 
 #include "paged_decode.h"
 #include "pd_internal.h"
+#include "pd_ptx.cuh"
 
 namespace pd {
 
@@ -17,7 +18,7 @@ __device__ unsigned int g_status;  // PD_DEV_* bits; read by paged_decode_device
 
 namespace {
 
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 10100;  // 1.1.0
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block on sm_100-class parts
 constexpr int kMaxDevices = 64;
 
@@ -192,6 +193,7 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   // path: 0 = auto (mma.sync), 1 = mma.sync, 3 = tcgen05 with tensor memory
   // (D <= 256); the warp-dot path (2) is not built
   if (o.path < 0 || o.path > 3 || o.path == 2) return PD_EINVAL;
+  if (o.wait_limit_us < 0) return PD_EINVAL;
   const bool tc = o.path == 3;
   if (tc && D > 256) return PD_EINVAL;
   if (tc && o.cluster > 1) return PD_EINVAL;
@@ -485,6 +487,9 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   p.status = dev.status;
   p.coop = plan.merge == 2 ? 1 : 0;
   p.mergers = plan.mergers > 0 ? plan.mergers : 1;
+  p.wait_limit_ns = (opts && opts->wait_limit_us > 0)
+                        ? (unsigned long long)opts->wait_limit_us * 1000ull
+                        : kWaitLimitNs;
   p.epi_floats = (plan.path == 3 ? epilogue_bytes_tc(head_size, plan.stages)
                                   : epilogue_bytes(head_size, plan.n_tiles, plan.stages)) / 4;
   if (plan.max_parts > 0) {
@@ -515,6 +520,7 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
 }
 
 }  // namespace
+
 }  // namespace pd
 
 using namespace pd;
@@ -529,9 +535,16 @@ size_t paged_decode_scratch_bytes(int max_num_seqs, int num_q_heads, int num_kv_
     return 0;
   if (head_size != 64 && head_size != 128 && head_size != 256 && head_size != 512) return 0;
   const int64_t R = (int64_t)(num_q_heads / num_kv_heads) * max_query_len;
-  const int64_t rg = std::max<int64_t>(1, cdiv(R, 64));
-  const int64_t nt8 = rg * 8 * cdiv(cdiv(R, rg), 8);  // padded rows over all row groups
-  const int64_t counters = ((int64_t)max_num_seqs * num_kv_heads * kMaxRowGroups * 4 + 255) / 256 * 256;
+  // padded rows over all row groups, for the larger of the two row-group
+  // rules of the planner (at most 64 rows per CTA for a batch, 16 for one
+  // sequence)
+  int64_t nt8 = 0;
+  for (int64_t rows_max : {64, 16}) {
+    const int64_t rg = std::min<int64_t>(kMaxRowGroups, std::max<int64_t>(1, cdiv(R, rows_max)));
+    nt8 = std::max(nt8, rg * 8 * cdiv(cdiv(R, rg), 8));
+  }
+  const int64_t counters =
+      ((int64_t)max_num_seqs * num_kv_heads * kCountersPerPair * 4 + 255) / 256 * 256;
   const int64_t parts = (int64_t)max_num_seqs * num_kv_heads * max_splits;
   const int64_t acc = (parts * nt8 * head_size * 4 + 255) / 256 * 256;
   const int64_t ml = (parts * nt8 * 2 * 4 + 255) / 256 * 256;
@@ -542,7 +555,7 @@ int paged_decode_scratch_init(pd_scratch *scratch, void *data, size_t bytes, int
                               int num_kv_heads, void *stream) {
   if (!scratch || !data || max_num_seqs < 0 || num_kv_heads <= 0) return PD_EINVAL;
   if ((reinterpret_cast<uintptr_t>(data) & 255u) != 0) return PD_EALIGN;
-  const int64_t slots = (int64_t)max_num_seqs * num_kv_heads * kMaxRowGroups;
+  const int64_t slots = (int64_t)max_num_seqs * num_kv_heads * kCountersPerPair;
   const int64_t cbytes = (slots * 4 + 255) / 256 * 256;
   if ((int64_t)bytes < cbytes) return PD_ESCRATCH;
   scratch->data = data;

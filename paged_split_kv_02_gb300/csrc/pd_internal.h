@@ -6,11 +6,17 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "paged_decode.h"
+
 namespace pd {
 
 constexpr int kBlockKeys = 16;        // keys per TMA box and per mma m-tile
 constexpr int kStageBytes = 32768;    // K + V bytes of one shared-memory ring stage
-constexpr int kMaxRowGroups = 8;      // counters reserved per (sequence, kv head)
+constexpr int kMaxRowGroups = 8;      // row groups of one kv head at most
+// int32 counters reserved per (sequence, kv head): arrivals and finished
+// mergers of every row group
+constexpr int kCountersPerPair = 2 * kMaxRowGroups;
+static_assert(kCountersPerPair == PD_COUNTERS_PER_PAIR, "counter reservation of the C ABI");
 constexpr int kMaxConsumerWarps = 8;  // warps that compute; one more loads
 constexpr int kMaxThreads = 32 * (kMaxConsumerWarps + 1);
 constexpr int kSmemAlign = 1024;      // the 128-byte TMA swizzle repeats every 1 KiB
@@ -58,6 +64,7 @@ struct Params {
   int64_t epi_floats;  // floats of the epilogue region (dead ring + Q tile)
   int coop;            // 1: co-resident grid, the last `mergers` arrivals merge
   int mergers;         // K_max of the cooperative merge (a power of two)
+  unsigned long long wait_limit_ns;  // bound of a cooperative merger's wait for arrivals
 };
 
 struct Launch {
@@ -117,7 +124,5 @@ inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
 
 cudaError_t launch_mma(int D, bool bf16, bool tc, const CUtensorMap &tk, const CUtensorMap &tv,
                        const Params &p, const Launch &l, cudaStream_t stream);
-
-unsigned int *device_status_ptr();
 
 }  // namespace pd

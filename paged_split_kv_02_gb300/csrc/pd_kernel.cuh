@@ -1169,15 +1169,26 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     // every part is published, and its acquire already covers them).
     if (tid == 0) {
       const int old = atomic_add_acq_rel_gpu(p.counters + 2 * group, 1);
-      const int m = old - (ncl - K);
+      int m = old - (ncl - K);
       int ok = 1;
-      if (m >= 0 && old != ncl - 1 && ld_acquire_gpu(p.counters + 2 * group) < ncl) {
+      if (old < 0 || old >= ncl) {
+        // the counter did not start this launch at zero (a scratch shared by
+        // overlapping calls, or left behind by a merger that gave up): no
+        // merge from it; every later index stays in bounds
+        atomicOr(p.status, 0x10u);
+        m = -1;
+      } else if (m >= 0 && old != ncl - 1 && ld_acquire_gpu(p.counters + 2 * group) < ncl) {
         const unsigned long long t0 = global_timer_ns();
         while (ld_acquire_gpu(p.counters + 2 * group) < ncl) {
           __nanosleep(64);
-          if (global_timer_ns() - t0 > kWaitLimitNs) {
+          if (global_timer_ns() - t0 > p.wait_limit_ns) {
             ok = 0;
             atomicOr(p.status, 0x1u);
+            // poison the group's arrival count so that the next launch on
+            // this scratch sees it out of range (and reports it) instead of
+            // electing mergers from a stale count; the scratch must be
+            // initialised again before it serves another call
+            atomicAdd(p.counters + 2 * group, 1 << 24);
             break;
           }
         }
@@ -1187,7 +1198,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     }
     __syncthreads();
     const int mi = flags[1];
-    if (mi < 0) return;  // not one of the last K arrivals
+    if (mi < 0 || mi >= K) return;  // not one of the last K arrivals
     if (!flags[2]) return;
     // count this merger past its wait now; the answer is needed only at the
     // end, so the round trip overlaps the merge
@@ -1442,6 +1453,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     const int old = atomic_add_acq_rel_gpu(p.counters + 2 * group, 1);
     const int last = old == ncl - 1;
     if (last) atomicExch(p.counters + 2 * group, 0);
+    if (old < 0 || old >= ncl) atomicOr(p.status, 0x10u);  // did not start at zero
     flags[1] = last;
 #pragma unroll 1
     for (int x = 1; x < CS; ++x)

@@ -14,7 +14,7 @@ namespace {
 
 constexpr size_t kStaticScratchBytes = PD_STATIC_SCRATCH_BYTES;
 constexpr size_t kStaticCounterBytes = PD_STATIC_COUNTER_BYTES;
-constexpr int kCountersPerPair = 8;  // counters reserved per (sequence, kv head)
+constexpr int kCountersPerPair = PD_COUNTERS_PER_PAIR;  // per (sequence, kv head)
 constexpr int kMaxDevices = 64;
 
 // The scratch itself.  In host code this name is only a stand-in for the
@@ -35,11 +35,23 @@ int static_scratch_address(void **out) {
   }
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_addr[dev]) {
+    // the array exists only in this library's sm_103a image: another
+    // device is refused the way the other entry points refuse it
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        major != 10 || minor != 3) {
+      cudaGetLastError();
+      return PD_ENODEV;
+    }
     void *ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
     if (e != cudaSuccess || ptr == nullptr) {
       cudaGetLastError();
-      return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? PD_ENODEV : PD_ECUDA;
+      return e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ||
+                     e == cudaErrorNoKernelImageForDevice
+                 ? PD_ENODEV
+                 : PD_ECUDA;
     }
     g_scratch_addr[dev] = ptr;
   }

@@ -25,7 +25,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert pd.paged_decode_version() == 10000
+    assert pd.paged_decode_version() == 10100
     for code in range(0, -9, -1):
         assert lib.paged_decode_strerror(code)
     assert b"unknown" in lib.paged_decode_strerror(-99)
@@ -47,7 +47,7 @@ def _fake_scratch(S, Hq, Hkv, D, M, splits):
     d = pd.PdScratch()
     d.data = 1 << 30
     d.bytes = pd.paged_decode_scratch_bytes(S, Hq, Hkv, D, M, splits)
-    d.counter_slots = S * Hkv * 8
+    d.counter_slots = S * Hkv * pd.COUNTERS_PER_PAIR
     return d
 
 
@@ -81,6 +81,66 @@ def test_plan_invariants(shape):
     assert p["seg_blocks"] * p["max_segments"] >= nb_max
     if S == 1 and Wd * P >= 32768 and not w:
         assert p["grid_x"] >= 128                      # a long sequence fills the SMs
+
+
+def test_counters_per_pair_matches_header():
+    text = open(pd.HEADER).read()
+    assert f"#define PD_COUNTERS_PER_PAIR {pd.COUNTERS_PER_PAIR}" in text
+    # the counter area of scratch_bytes: PD_COUNTERS_PER_PAIR int32 per pair
+    # (no partials with max_splits = 0), rounded to 256 bytes, plus 256
+    n = pd.paged_decode_scratch_bytes(1000, 32, 8, 128, 4, 0)
+    assert n == -(-1000 * 8 * pd.COUNTERS_PER_PAIR * 4 // 256) * 256 + 256
+
+
+def test_plan_splits_with_eight_row_groups():
+    # one sequence with G * M = 128 packed rows takes 8 row groups, i.e. 16
+    # counters per (sequence, kv head): a scratch sized and initialised by
+    # the library must still let it split
+    S, Hq, Hkv, D, M = 1, 16, 1, 128, 8
+    sd = _fake_scratch(S, Hq, Hkv, D, M, 256)
+    p = pd.paged_decode_plan(S, Hq, Hkv, D, 16, M, 0, 2048, 148, scratch_desc=sd)
+    assert p["row_groups"] == 8
+    assert p["max_parts"] > 1 and p["max_segments"] > 1 and p["merge"] > 0
+    assert p["scratch_needed"] <= sd.bytes
+    # the same with 64 q heads over 4 kv heads
+    sd = _fake_scratch(S, 64, 4, D, M, 256)
+    p = pd.paged_decode_plan(S, 64, 4, D, 16, M, 0, 2048, 148, scratch_desc=sd)
+    assert p["row_groups"] == 8 and p["max_parts"] > 1
+
+
+def test_scratch_bytes_covers_single_sequence_row_groups():
+    # R = 20 packed rows: a batch plan keeps one row group of 24 padded rows,
+    # a single-sequence plan two groups of 16; the size covers the larger
+    for Hq, Hkv, M in [(20, 4, 4), (40, 8, 4), (12, 2, 3)]:
+        sd = _fake_scratch(1, Hq, Hkv, 128, M, 8)
+        p = pd.paged_decode_plan(1, Hq, Hkv, 128, 16, M, 0, 2048, 152, scratch_desc=sd,
+                                 opts=pd.options(segments=8))
+        assert p["max_parts"] == 8 and p["scratch_needed"] <= sd.bytes
+
+
+def test_static_entry_refuses_too_many_pairs_before_the_device(lib):
+    # more sequence x kv-head pairs than the static counter area holds:
+    # PD_ESCRATCH from the host checks, with no device touched
+    def call(num_seqs, hkv):
+        sl = pd.PdTensor()
+        sl.data, sl.dtype, sl.ndim = 1 << 20, 2, 1
+        sl.shape[0], sl.stride[0] = num_seqs, 1
+        d = pd.PdTensor()
+        return lib.paged_decode_attn_static(*[ctypes.byref(x) for x in (d, d, d, d, sl, d)],
+                                            8 * hkv, hkv, 128, 16, 1, 0, 0.1, 1, None)
+    pairs = (512 << 10) // (4 * pd.COUNTERS_PER_PAIR)
+    assert pairs == 8192
+    assert call(pairs // 2 + 1, 2) == -6
+    assert call(pairs + 1, 1) == -6
+    if not torch.cuda.is_available():
+        # at the limit the call goes on to the device, which is missing here
+        assert call(pairs, 1) == -8
+
+
+def test_wait_limit_option_checked():
+    with pytest.raises(pd.PagedDecodeError):
+        pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 256, 152,
+                             opts=pd.options(wait_limit_us=-1))
 
 
 def test_plan_without_scratch_does_not_split():

@@ -4,6 +4,12 @@ merge), checked on sampled output rows that the oracle computes one by one,
 plus properties that hold at any size (finite outputs, a clean device
 status word, counters left at zero).
 
+With N(0,1) values the outputs average towards zero at long contexts (the
+oracle's RMS is about 0.01 at 32k keys), where a max-abs bound alone says
+little: every check also bounds the error relative to the oracle's RMS, and
+each configuration at >= 16k keys has a twin whose V values are N(1, 1), so
+that its outputs stay O(1) as the tolerance presumes.
+
 Inputs are drawn on the device with the seeded CUDA generator (the sizes
 reach 1 GB of K/V) and copied to the host for the oracle."""
 
@@ -78,3 +84,71 @@ def test_varlen_batch_full():
     case = W.varlen_spec_decode_batch(seed=7, pad_tokens=6, device="cuda", gen_device="cuda")
     out = _full_size(case, seed=7)
     assert torch.all(out[case.query_start_host[-1]:] == 0)
+
+
+# ---- twins with V ~ N(1, 1): O(1) outputs at long contexts ----------------
+
+@pytest.mark.parametrize("L", [16384, 32768])
+@pytest.mark.parametrize("M", [1, 4])
+def test_spec_decode_full_shifted(M, L):
+    _full_size(W.spec_decode_hnd(M, L, seed=110 + M, device="cuda", gen_device="cuda",
+                                 v_mean=1.0), seed=M)
+
+
+@pytest.mark.parametrize("L", [16384, 32768])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_sliding_window_full_shifted(dtype, L):
+    _full_size(W.sliding_window(dtype, 4, L, seed=210, device="cuda", gen_device="cuda",
+                                v_mean=1.0), seed=4)
+
+
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_wide_head_full_shifted(M):
+    _full_size(W.wide_head(M, 32768, seed=310 + M, device="cuda", gen_device="cuda",
+                           v_mean=1.0), seed=M)
+
+
+def test_batched_hybrid_pages_full_shifted():
+    _full_size(W.batched_hybrid_pages(seed=410, device="cuda", gen_device="cuda", v_mean=1.0),
+               seed=6)
+
+
+def test_varlen_batch_full_shifted():
+    case = W.varlen_spec_decode_batch(seed=8, pad_tokens=3, device="cuda", gen_device="cuda",
+                                      v_mean=1.0)
+    out = _full_size(case, seed=8)
+    assert torch.all(out[case.query_start_host[-1]:] == 0)
+
+
+# ---- the cache forms of the next rows at scale ----------------------------
+
+@pytest.mark.parametrize("M,L", [(4, 32768), (1, 16384)])
+@pytest.mark.parametrize("v_mean", [0.0, 1.0])
+def test_spec_decode_packed_kv_full(M, L, v_mean):
+    """K and V side by side in one pool row (the packed-cache strides)."""
+    _full_size(W.spec_decode_hnd(M, L, seed=120 + M, device="cuda", gen_device="cuda",
+                                 v_mean=v_mean, packed=True), seed=M)
+
+
+@pytest.mark.parametrize("M", [4, 8])
+def test_wide_head_packed_kv_full(M):
+    _full_size(W.wide_head(M, 32768, seed=320 + M, device="cuda", gen_device="cuda",
+                           v_mean=1.0, packed=True), seed=M)
+
+
+@pytest.mark.parametrize("L", [16384, 32768])
+@pytest.mark.parametrize("P", [528, 544, 784, 1056])
+def test_hybrid_page_sizes_full(P, L):
+    """16 q / 2 kv heads at D=256, M=4, on the hybrid models' page sizes
+    (784 = 49 blocks of 16 keys: the page is not a power-of-two number of
+    blocks)."""
+    _full_size(W.hybrid_page(P, 4, L, seed=500 + P, device="cuda", gen_device="cuda"), seed=P)
+    _full_size(W.hybrid_page(P, 4, L, seed=510 + P, device="cuda", gen_device="cuda",
+                             v_mean=1.0), seed=P + 1)
+
+
+@pytest.mark.parametrize("P", [528, 784])
+def test_hybrid_pages_batched_full(P):
+    """The 64-sequence batch of lengths U[1, 16384] on other hybrid pages."""
+    _full_size(W.batched_hybrid_pages(seed=420 + P, device="cuda", gen_device="cuda",
+                                      page_size=P, v_mean=1.0), seed=P)
