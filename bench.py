@@ -288,6 +288,11 @@ def run_ours(args, world, rank, local):
         traffic_basis = ("bytes per launch, averaged over the step's calls: the DRAM/algorithmic "
                          "ratio of one ncu capture (M=4, 32768 keys) x the algorithmic bytes")
 
+    # ---- the other decode configurations, timed the same way ----------------
+    configs = None
+    if not args.no_configs:
+        configs = measure_other_configs(pd, device, l2, peak, stream)
+
     # ---- end to end through the C ABI with host buffers --------------------
     e2e = None
     if rank == 0 or world > 1:
@@ -334,12 +339,91 @@ def run_ours(args, world, rank, local):
         },
         "median_pct_hbm_4k_32k": round(statistics.median(long_ctx), 2) if long_ctx else None,
         "cases": per_case,
+        "other_configs": configs,
         "clocks": clk.summary(),
         "e2e": e2e,
         "cpu_baseline": cpu,
         "device_status": status,
     }
     print(json.dumps(line), flush=True)
+
+
+def other_configs():
+    """The other decode configurations, timed beside the sweep: (name, maker
+    of replica r, L2-resident note)."""
+    from paged_split_kv_02_gb300 import workloads as W
+
+    out = [("single sequence: fp16 D=128 8/2, 300 keys, P=16, NHD",
+            lambda r, dev: W.single_seq_nhd(seed=r).to(dev), True)]
+    for M in (1, 4):
+        out.append((f"sliding window 512: fp16 D=256 8/1, P=32, M={M}, 32768 keys",
+                    lambda r, dev, M=M: W.sliding_window(torch.float16, M, 32768, seed=r,
+                                                         device=dev, gen_device=dev), True))
+    for L in (4096, 32768):
+        for M in (1, 4, 8):
+            out.append((f"wide head: fp16 D=512 8/1, P=16, M={M}, {L} keys",
+                        lambda r, dev, M=M, L=L: W.wide_head(M, L, seed=r, device=dev,
+                                                             gen_device=dev), False))
+    out.append(("batched: bf16 D=256 16/2, P=1056, 64 sequences U[1,16384], M=4",
+                lambda r, dev: W.batched_hybrid_pages(seed=r, device=dev, gen_device=dev), False))
+    for P in (784, 1056):
+        out.append((f"hybrid page: bf16 D=256 16/2, P={P}, M=4, 16384 keys",
+                    lambda r, dev, P=P: W.hybrid_page(P, 4, 16384, seed=r, device=dev,
+                                                      gen_device=dev), False))
+    out.append(("packed K|V: bf16 D=128 32/8, P=16, HND, M=4, 32768 keys",
+                lambda r, dev: W.spec_decode_hnd(4, 32768, seed=r, device=dev, gen_device=dev,
+                                                 packed=True), False))
+    return out
+
+
+def run_configs(args, world, rank, local):
+    """--workload configs: only the other decode configurations (those whose
+    name contains --config-filter), one JSON line; for profiling runs."""
+    import paged_split_kv_02_gb300 as pd
+
+    pd.build()
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    l2 = int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 126 << 20))
+    peak, peak_kind = _peaks()
+    stream = torch.cuda.Stream(device=device)
+    res = measure_other_configs(pd, device, l2, peak, stream, args.config_filter)
+    status = pd.paged_decode_device_status(reset=True)
+    if rank == 0:
+        print(json.dumps({"metric": METRIC, "unit": "us per call", "n_gpus": world,
+                          "configs": res, "peak": peak, "peak_kind": peak_kind,
+                          "device_status": status}), flush=True)
+
+
+def measure_other_configs(pd, device, l2, peak, stream, name_filter=""):
+    """µs per call, K+V GB/s and % of the HBM peak of each configuration
+    (CUDA graphs over replicas that exceed 2.2 x L2, as for the sweep; a
+    windowed or 300-key call moves under 1 MB and is timed on 16 replicas
+    that stay in L2: it is bound by latency either way)."""
+    res = []
+    for name, make, small in other_configs():
+        if name_filter and name_filter not in name:
+            continue
+        first = make(0, device)
+        kv = max(1, first.kv_bytes_touched())
+        n = 16 if small else max(2, min(12, math.ceil(2.2 * l2 / kv)))
+        reps = [first] + [make(r, device) for r in range(1, n)]
+        sc = pd.Scratch(first.num_seqs, first.num_q_heads, first.num_kv_heads, first.head_size,
+                        first.max_query_len, max_splits=256, device=device)
+        outs = [torch.empty_like(c.q) for c in reps]
+        calls = [(lambda c=c, o=o: pd.decode_case(c, out=o, scratch=sc)) for c, o in zip(reps, outs)]
+        with torch.cuda.stream(stream):
+            for c in calls:
+                c()
+        torch.cuda.synchronize()
+        us = _time_graph(calls, stream, max(3, min(50, int(600 / n))))
+        res.append({"config": name, "us": round(us, 3),
+                    "kv_gbs": round(kv / (us * 1e-6) / 1e9, 1),
+                    "pct_hbm": round(100 * first.algorithmic_bytes() / (us * 1e-6) / 1e9 / peak, 2),
+                    "replicas": n, "l2_resident": small})
+        del reps, outs, calls, sc
+        torch.cuda.empty_cache()
+    return res
 
 
 def measure_e2e(pd, cases, outs, scratch, stream, keys, args):
@@ -604,6 +688,190 @@ def run_varlen(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+ROPE_WORKLOAD = ("rotary embedding + paged KV-cache write ahead of decode: bf16, head_size 128, "
+                 "32 q / 8 kv heads, all 128 dims rotated (NeoX pairing), page_size 16, HND; "
+                 "16384 new tokens at random positions and distinct cache slots (one call)")
+
+
+def run_rope(args, world, rank, local):
+    """--workload rope: paged_rope_cache_write on a prefill-sized token
+    batch (HBM-bound: ~0.4 GB per call), with a decode-sized batch (64
+    sequences x 4 tokens, latency-bound) timed beside it."""
+    import paged_split_kv_02_gb300 as pd
+    from paged_split_kv_02_gb300 import workloads as W
+
+    pd.build()
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    peak, peak_kind = _peaks()
+    stream = torch.cuda.Stream(device=device)
+
+    def make(T, pages, seed):
+        return W.make_rope_case(f"rope_T{T}", seed=seed, dtype=torch.bfloat16, num_tokens=T,
+                                num_q_heads=32, num_kv_heads=8, head_size=128, rot_dim=128,
+                                page_size=16, num_pages=pages, layout=W.HND, max_pos=32768,
+                                device=device, gen_device=device)
+
+    big = [make(16384, 2048, r) for r in range(2)]  # two replicas of ~0.4 GB each
+    small = [make(256, 64, 10 + r) for r in range(64)]
+    outs_b = [torch.empty_like(c.q) for c in big]
+    outs_s = [torch.empty_like(c.q) for c in small]
+    calls_b = [(lambda c=c, o=o: pd.rope_case(c, q_out=o)) for c, o in zip(big, outs_b)]
+    calls_s = [(lambda c=c, o=o: pd.rope_case(c, q_out=o)) for c, o in zip(small, outs_s)]
+    with torch.cuda.stream(stream):
+        for c in calls_b + calls_s:
+            c()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        _time_graph(calls_b, stream, 1)
+    _barrier(world)
+    with ClockSampler(local) as clk:
+        us = _time_graph(calls_b, stream, args.steps)
+    us = _max_over_ranks(us, world)
+    us_small = _time_graph(calls_s, stream, max(3, args.steps // 4))
+    nbytes = big[0].bytes_moved()
+    status = pd.paged_decode_device_status(reset=True)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        from oracle import rope_cache as R
+
+        c = make(512, 64, 99).to("cpu")
+        n = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 5.0:
+            R.rope_cache_write(c.q, c.k, c.v, c.positions, c.slot_mapping, c.cos_sin,
+                               c.k_cache, c.v_cache, c.layout, c.rot_dim, c.is_neox)
+            n += 1
+        dt = (time.perf_counter() - t0) / n
+        cpu = {"value": round(c.bytes_moved() / dt / 1e9, 4), "unit": UNIT, "cores": 1,
+               "kind": "oracle", "seconds": round(dt * n, 2),
+               "sample": f"{n} calls on 512 tokens of the same shape (fp64 numpy oracle, "
+                         "one thread)"}
+    line = {
+        "metric": "GB/s moved by the rotary embedding + KV-cache write, and us per call",
+        "value": round(world * nbytes / (us * 1e-6) / 1e9, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us * 1e-3, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, random positions and slots)",
+        "config": {"workload": ROPE_WORKLOAD,
+                   "l2": "inputs larger than L2: two replicas of ~0.4 GB alternate",
+                   "timing": "CUDA graph of the calls, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps * len(calls_b),
+        "us_per_call": round(us, 3),
+        "decode_batch_us_per_call": round(us_small, 3),
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4),
+                     "traffic": None, "traffic_basis": "no ncu capture of this kernel",
+                     "peak_kind": peak_kind},
+        "clocks": clk.summary(),
+        "e2e": None,
+        "cpu_baseline": cpu,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
+PREFILL_WORKLOAD = ("paged prefill: bf16, head_size 128, 32 q / 8 kv heads, page_size 16, HND; "
+                    "4 requests x 2048 new tokens after 2048 cached ones (one call over the "
+                    "host-made work list)")
+
+
+def run_prefill(args, world, rank, local):
+    """--workload prefill: paged_prefill_attn on a batch of long requests;
+    the plan is made once on the host, its work list copied to the device."""
+    import paged_split_kv_02_gb300 as pd
+    from paged_split_kv_02_gb300 import workloads as W
+
+    pd.build()
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+        peak, peak_kind = float(peaks["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback"
+    stream = torch.cuda.Stream(device=device)
+    reps = [W.make_prefill_case("prefill_bench", seed=r, q_lens=[2048] * 4, contexts=[2048] * 4,
+                                device=device, gen_device=device) for r in range(2)]
+    c0 = reps[0]
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    plan = pd.paged_prefill_plan(c0.query_start_host, c0.seq_lens_host, c0.num_q_heads,
+                                 c0.num_kv_heads, c0.window, sms)
+    items, info = plan
+    work = items.to(device)
+    sc = pd.prefill_scratch(c0.num_kv_heads, c0.head_size, sms, device=device)
+    outs = [torch.empty_like(c.q) for c in reps]
+
+    def call(c, o):
+        pd.paged_prefill_attn(c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens,
+                              c.query_start, work, info, o, c.num_q_heads, c.num_kv_heads,
+                              c.head_size, c.page_size, c.window, c.scale, c.layout, sc)
+
+    calls = [(lambda c=c, o=o: call(c, o)) for c, o in zip(reps, outs)]
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        _time_graph(calls, stream, 1)
+    _barrier(world)
+    with ClockSampler(local) as clk:
+        us = _time_graph(calls, stream, args.steps)
+    us = _max_over_ranks(us, world)
+    flops = W.prefill_flops(c0)
+    status = pd.paged_decode_device_status(reset=True)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        host = c0.to("cpu")
+        T = host.q.shape[0]
+        rows = [(t, h) for t in range(0, T, 64) for h in range(host.num_q_heads)]
+        n = oracle.default_threads()
+        t0 = time.perf_counter()
+        oracle.attention(host, rows=rows, nthreads=n)
+        dt = time.perf_counter() - t0
+        frac = len(rows) / (T * host.num_q_heads)
+        cpu = {"value": round(flops * frac / dt / 1e12, 5), "unit": "TFLOP/s", "cores": n,
+               "kind": "oracle", "seconds": round(dt, 2),
+               "sample": f"every 64th token row of the batch, all heads ({frac:.4f} of the "
+                         "rows), fp64 C oracle; value scaled to the sampled rows"}
+    tflops = flops / (us * 1e-6) / 1e12
+    line = {
+        "metric": "TFLOP/s of a paged prefill call (QK^T and PV over the keys each row sees)",
+        "value": round(world * tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us * 1e-3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/K/V, random page permutation)",
+        "config": {"workload": PREFILL_WORKLOAD,
+                   "l2": "two replicas alternate (prefill is bound by arithmetic)",
+                   "timing": "CUDA graph of the calls, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}",
+                   "plan": info.as_dict()},
+        "gpu_launches": args.steps * len(calls),
+        "us_per_call": round(us, 3),
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                     "traffic_basis": "no ncu capture of this launch", "peak_kind": peak_kind,
+                     "note": "products on mma.sync m16n8k16 (keys on the M side, 8-row "
+                             "n-tiles), against the measured tcgen05-class bf16 peak"},
+        "clocks": clk.summary(),
+        "e2e": None,
+        "cpu_baseline": cpu,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -611,9 +879,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="sweep", choices=["sweep", "varlen"],
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other decode configurations timed beside the sweep")
+    ap.add_argument("--config-filter", default="",
+                    help="--workload configs: only configurations whose name contains this")
+    ap.add_argument("--workload", default="sweep",
+                    choices=["sweep", "varlen", "rope", "prefill", "configs"],
                     help="sweep: the spec-decode sweep (default); varlen: a batch with a "
-                         "query length per request")
+                         "query length per request; rope: the rotary embedding + KV-cache "
+                         "write; prefill: paged prefill over a work list; configs: the other "
+                         "decode configurations only")
     ap.add_argument("--requests", type=int, default=32,
                     help="requests of the varlen batch (fewer for profiling runs)")
     ap.add_argument("--cases", default="",
@@ -629,6 +904,12 @@ def main():
         run_reference(args, world, rank)
     elif args.workload == "varlen":
         run_varlen(args, world, rank, local)
+    elif args.workload == "rope":
+        run_rope(args, world, rank, local)
+    elif args.workload == "prefill":
+        run_prefill(args, world, rank, local)
+    elif args.workload == "configs":
+        run_configs(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

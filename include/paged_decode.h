@@ -57,7 +57,7 @@ extern "C" {
 /* Element types.  q, the caches and out share one of PD_F16 / PD_BF16
  * (KernelVariant.__post_init__: fp16 or bf16 only); block_table and
  * seq_lens are PD_I32. */
-typedef enum { PD_F16 = 0, PD_BF16 = 1, PD_I32 = 2 } pd_dtype;
+typedef enum { PD_F16 = 0, PD_BF16 = 1, PD_I32 = 2, PD_F32 = 3 } pd_dtype;
 
 /* Cache layouts (KernelVariant.layout: 0 = NHD, 1 = HND).
  *   PD_NHD: [num_blocks, page_size, num_kv_heads, head_size]
@@ -108,6 +108,13 @@ typedef enum {
                                      (PD_DEV_WAIT_TIMEOUT) in an earlier call;
                                      the groups concerned are not merged and
                                      the scratch must be initialised again */
+
+#define PD_DEV_BAD_POSITION 0x20u /* paged_rope_cache_write: a position outside
+                                     the cos/sin table (clamped into it)     */
+#define PD_DEV_BAD_SLOT     0x40u /* paged_rope_cache_write: a slot past the
+                                     pool's pages x page_size (not written)  */
+#define PD_DEV_BAD_WORK     0x80u /* paged_prefill_attn: a work item outside
+                                     the launch (skipped)                    */
 
 /* int32 counters a scratch reserves per (sequence, kv head): an arrival
  * count and a finished-merger count for each of up to 8 row groups. */
@@ -262,6 +269,114 @@ PD_API int paged_decode_attn_static(const pd_tensor *q, const pd_tensor *k_cache
                                     int num_kv_heads, int head_size, int page_size,
                                     int max_query_len, int window, float scale, int layout,
                                     void *stream);
+
+/* The rotary position embedding of the new tokens' q and k and the store of
+ * their k and v into the paged cache, in one kernel, ahead of the decode call
+ * that reads the cache.  The pages only name this step (the fused RoPE /
+ * KV-cache write that ROCm/vllm PR #1330, "Summary", moved to a stacked draft
+ * PR); the slot convention is the cache store of the vLLM ROCm Octave
+ * backend (`do_kv_cache_update(layer, key, value, kv_cache, slot_mapping)`)
+ * and the rotary part of the head its `rope_dim`.  For token t, head h and
+ * rotated pair i < rot_dim / 2 with (c, s) = cos_sin_cache[positions[t]]
+ * [i], [rot_dim / 2 + i]:
+ *     x1' = x1 c - x2 s,   x2' = x2 c + x1 s       (fp32, rounded once)
+ * where (x1, x2) = dims (i, i + rot_dim/2) when is_neox, else (2i, 2i + 1);
+ * dims at and past rot_dim pass through.  q' goes to q_out; k' and v go to
+ * the cache slot slot_mapping[t] (page slot / page_size, token slot %
+ * page_size) of every kv head; a slot of -1 (a padding token) writes
+ * nothing.
+ *   q, q_out      [T, Hq, D], fp16/bf16; q_out may be q itself (in place)
+ *   k, v          [T, Hkv, D], the same dtype
+ *   positions     [T] int32 device array, rows of the table
+ *   slot_mapping  [T] int32 device array, distinct slots or -1
+ *   cos_sin_cache [max_pos, >= rot_dim] fp32 (PD_F32), rows 16-byte aligned
+ *   k_cache, v_cache  the decode call's pools (NHD or HND, packed allowed)
+ *   rot_dim       rotated dims, <= D; a multiple of 16 (NeoX) or 8 (GPT-J)
+ * Asynchronous on `stream`, allocates nothing.  A position outside the table
+ * is clamped into it and a slot past the pool is skipped, both reported in
+ * the device status word (PD_DEV_BAD_POSITION, PD_DEV_BAD_SLOT). */
+PD_API int paged_rope_cache_write(const pd_tensor *q, const pd_tensor *k, const pd_tensor *v,
+                                  const pd_tensor *positions, const pd_tensor *slot_mapping,
+                                  const pd_tensor *cos_sin_cache, pd_tensor *q_out,
+                                  pd_tensor *k_cache, pd_tensor *v_cache, int num_q_heads,
+                                  int num_kv_heads, int head_size, int rot_dim, int page_size,
+                                  int layout, int is_neox, void *stream);
+
+/* ---- Paged prefill (plan_prefill, prefill_target_workgroups and
+ * _BuiltinPrefill.prefill_attn on the vllm.v1.attention.ops.rocm_rdna_hip
+ * page) ----
+ *
+ * The same attention as paged_decode_attn_varlen, for requests of any query
+ * length: request s owns the rows query_start[s] .. query_start[s+1] - 1 of
+ * q and out, and its token i sees the keys [lo, seq_lens[s] - q_len_s + i +
+ * 1) (lo as in paged_decode_attn).  A launch runs a host-made work list: a
+ * request's query tokens are packed token-major into rows (token i, q head
+ * h*G + j -> row i*G + j), cut into tiles of PD_PREFILL_TILE_ROWS rows, and
+ * a tile whose keys (from its window start rounded down to 16 keys, to the
+ * last key its last token sees) exceed the mean load per resident CTA is cut
+ * into segments, merged in the kernel by the last-arriving segment.  Items
+ * are ordered heaviest first.  Each item runs once per kv head. */
+#define PD_PREFILL_TILE_ROWS 64
+#define PD_PREFILL_MAX_SEGMENTS 32
+
+/* One work item: a segment of the keys of one tile of one request. */
+typedef struct pd_prefill_item {
+  int32_t seq;      /* request of the batch                                   */
+  int32_t tile;     /* tile of PD_PREFILL_TILE_ROWS packed rows of it          */
+  int32_t seg;      /* segment of the tile's keys, 0 .. nseg - 1               */
+  int32_t nseg;     /* segments of the tile (1: not split)                    */
+  int32_t split;    /* index of the split tile, -1 when nseg == 1             */
+  int32_t slot;     /* first partial slot of the split tile's segments, or -1 */
+  int32_t blocks;   /* 16-key blocks of the tile's keys (its load)            */
+  int32_t reserved; /* 0                                                      */
+} pd_prefill_item;
+
+typedef struct pd_prefill_plan_info {
+  int64_t num_items;       /* work items (launch rows x kv heads)             */
+  int32_t num_split_tiles; /* tiles cut into segments                         */
+  int32_t num_slots;       /* partial slots of their segments (per kv head)  */
+  int32_t tile_rows;       /* PD_PREFILL_TILE_ROWS                            */
+  int32_t max_segments;    /* PD_PREFILL_MAX_SEGMENTS                         */
+  int32_t target_ctas;     /* CTAs resident at once the split aims at         */
+  int32_t reserved;
+  int64_t total_blocks;    /* 16-key blocks over all tiles (one kv head)      */
+  double load_blocks;      /* blocks per CTA a tile is split above            */
+} pd_prefill_plan_info;
+
+/* The work list of a prefill launch, computed on the host from host copies
+ * of query_start [num_seqs + 1] and seq_lens [num_seqs] (each length, or an
+ * upper bound).  num_sms: CTAs resident at once (0 = the current device's
+ * SM count; this kernel runs one CTA per SM).  items NULL: fill `info` only
+ * (a size query); else items[0 .. info->num_items) are written and
+ * `capacity` must hold them.  Returns PD_EINVAL on a malformed query_start
+ * (negative or decreasing). */
+PD_API int paged_prefill_plan(const int32_t *query_start, const int32_t *seq_lens, int num_seqs,
+                              int num_q_heads, int num_kv_heads, int window, int num_sms,
+                              pd_prefill_item *items, int64_t capacity,
+                              pd_prefill_plan_info *info);
+
+/* Scratch bytes that serve every prefill plan made with this num_sms.
+ * Prepare the buffer with paged_decode_scratch_init(scratch, data, bytes,
+ * num_sms, 1, stream). */
+PD_API size_t paged_prefill_scratch_bytes(int num_kv_heads, int head_size, int num_sms);
+
+/* The prefill call.
+ *   q, out       [T, Hq, D] fp16/bf16, T = query_start's last entry or more
+ *                (rows past it are written as zeros)
+ *   k_cache, v_cache, block_table, seq_lens: as paged_decode_attn
+ *   query_start  [S + 1] int32 device array (the plan's, on the device)
+ *   work         [num_items, 8] int32 device copy of the plan's items
+ *   info         the plan's info (host)
+ *   scratch      needed when info->num_split_tiles > 0 (else may be NULL)
+ * Items that do not fit the launch (a request, tile, segment or slot out of
+ * range) are skipped and reported as PD_DEV_BAD_WORK. */
+PD_API int paged_prefill_attn(const pd_tensor *q, const pd_tensor *k_cache,
+                              const pd_tensor *v_cache, const pd_tensor *block_table,
+                              const pd_tensor *seq_lens, const pd_tensor *query_start,
+                              const pd_tensor *work, const pd_prefill_plan_info *info,
+                              pd_tensor *out, int num_q_heads, int num_kv_heads, int head_size,
+                              int page_size, int window, float scale, int layout,
+                              pd_scratch *scratch, void *stream);
 
 /* Read the device status word (PD_DEV_* bits) of the current device after
  * synchronising `stream`; reset it to 0 when `reset` is non-zero. */

@@ -13,6 +13,10 @@ Names follow the C ABI:
   scale, layout, scratch, stream)``
 * ``paged_decode_scratch_bytes(...)`` / ``Scratch`` (``paged_decode_scratch_init``)
 * ``paged_decode_plan(...)``, ``paged_decode_device_status(...)``
+* ``paged_rope_cache_write(...)``: rotary embedding of the new tokens' q
+  and k and the store of k and v into the paged cache, ahead of decode
+* ``paged_prefill_plan(...)`` / ``paged_prefill_attn(...)``: attention for
+  requests of any query length over a host-made work list
 """
 
 from __future__ import annotations
@@ -36,7 +40,7 @@ STATUS_NAMES = {
     -5: "PD_EALIGN", -6: "PD_ESCRATCH", -7: "PD_ECUDA", -8: "PD_ENODEV",
 }
 DEV_WAIT_TIMEOUT, DEV_BAD_PAGE, DEV_BAD_SEQLEN, DEV_BAD_QSTART = 0x1, 0x2, 0x4, 0x8
-DEV_BAD_SCRATCH = 0x10
+DEV_BAD_SCRATCH, DEV_BAD_POSITION, DEV_BAD_SLOT, DEV_BAD_WORK = 0x10, 0x20, 0x40, 0x80
 COUNTERS_PER_PAIR = 16  # PD_COUNTERS_PER_PAIR
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
@@ -73,6 +77,22 @@ class PdPlan(ctypes.Structure):
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class PdPrefillItem(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("seq", "tile", "seg", "nseg", "split", "slot", "blocks", "reserved")]
+
+
+class PdPrefillPlanInfo(ctypes.Structure):
+    _fields_ = [("num_items", ctypes.c_int64), ("num_split_tiles", ctypes.c_int32),
+                ("num_slots", ctypes.c_int32), ("tile_rows", ctypes.c_int32),
+                ("max_segments", ctypes.c_int32), ("target_ctas", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("total_blocks", ctypes.c_int64),
+                ("load_blocks", ctypes.c_double)]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
 
 
 _lib = None
@@ -126,6 +146,16 @@ def lib():
         L.paged_decode_strerror.restype = ctypes.c_char_p
         L.paged_decode_version.argtypes = []
         L.paged_decode_version.restype = i32
+        L.paged_rope_cache_write.argtypes = [T] * 9 + [i32] * 7 + [vp]
+        L.paged_rope_cache_write.restype = i32
+        L.paged_prefill_plan.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, i64,
+                                         ctypes.POINTER(PdPrefillPlanInfo)]
+        L.paged_prefill_plan.restype = i32
+        L.paged_prefill_scratch_bytes.argtypes = [i32, i32, i32]
+        L.paged_prefill_scratch_bytes.restype = sz
+        L.paged_prefill_attn.argtypes = [T] * 7 + [ctypes.POINTER(PdPrefillPlanInfo), T] + \
+            [i32] * 5 + [f32, i32, ctypes.POINTER(PdScratch), vp]
+        L.paged_prefill_attn.restype = i32
         _lib = L
     return _lib
 
@@ -133,7 +163,7 @@ def lib():
 def declared_symbols() -> list:
     """Function names the public header declares."""
     text = open(HEADER).read()
-    return re.findall(r"PD_API\s+[\w\s\*]*?\b(paged_decode_\w+)\s*\(", text)
+    return re.findall(r"PD_API\s+[\w\s\*]*?\b(paged_\w+)\s*\(", text)
 
 
 def _strerror(code: int) -> str:
@@ -143,7 +173,7 @@ def _strerror(code: int) -> str:
         return "?"
 
 
-_DTYPES = {torch.float16: 0, torch.bfloat16: 1, torch.int32: 2}
+_DTYPES = {torch.float16: 0, torch.bfloat16: 1, torch.int32: 2, torch.float32: 3}
 
 
 def tensor_desc(t: torch.Tensor) -> PdTensor:
@@ -167,6 +197,8 @@ def options(**kw) -> PdOptions:
 
 def _stream_handle(stream) -> Optional[int]:
     if stream is None:
+        if not torch.cuda.is_available():
+            return None  # the call itself reports the missing device
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
@@ -288,6 +320,108 @@ def paged_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_size, page_size,
     if rc != PD_OK:
         raise PagedDecodeError(rc, "paged_decode_plan")
     return plan.as_dict()
+
+
+def paged_rope_cache_write(q, k, v, positions, slot_mapping, cos_sin_cache, q_out, k_cache,
+                           v_cache, num_q_heads, num_kv_heads, head_size, rot_dim, page_size,
+                           layout, is_neox=True, stream=None, check: bool = True) -> int:
+    """Rotary embedding of q and k and the store of k and v into the paged
+    cache at ``slot_mapping`` (see the C header); ``q_out`` may be ``q``."""
+    descs = [tensor_desc(t) for t in (q, k, v, positions, slot_mapping, cos_sin_cache, q_out,
+                                      k_cache, v_cache)]
+    rc = lib().paged_rope_cache_write(*[ctypes.byref(d) for d in descs], int(num_q_heads),
+                                      int(num_kv_heads), int(head_size), int(rot_dim),
+                                      int(page_size), int(layout), int(bool(is_neox)),
+                                      _stream_handle(stream))
+    if check and rc != PD_OK:
+        raise PagedDecodeError(rc, "paged_rope_cache_write")
+    return rc
+
+
+def rope_case(case, q_out=None, stream=None):
+    """Run the rotary embedding + cache write on a ``workloads.RopeCase``
+    (tensors on the GPU); returns q_out (the caches are written in place)."""
+    if q_out is None:
+        q_out = torch.empty_like(case.q)
+    paged_rope_cache_write(case.q, case.k, case.v, case.positions, case.slot_mapping,
+                           case.cos_sin, q_out, case.k_cache, case.v_cache, case.num_q_heads,
+                           case.num_kv_heads, case.head_size, case.rot_dim, case.page_size,
+                           case.layout, case.is_neox, stream)
+    return q_out
+
+
+def paged_prefill_plan(query_start, seq_lens, num_q_heads, num_kv_heads, window, num_sms=0):
+    """The work list of a prefill launch, made on the host (see the C
+    header): returns (items int32 [n, 8] as a CPU tensor, PdPrefillPlanInfo)."""
+    qs = torch.as_tensor(query_start, dtype=torch.int32).contiguous()
+    sl = torch.as_tensor(seq_lens, dtype=torch.int32).contiguous()
+    S = int(sl.shape[0])
+    if qs.shape[0] != S + 1:
+        raise PagedDecodeError(-1, "paged_prefill_plan")
+    info = PdPrefillPlanInfo()
+    L = lib()
+    rc = L.paged_prefill_plan(qs.data_ptr(), sl.data_ptr(), S, int(num_q_heads),
+                              int(num_kv_heads), int(window), int(num_sms), None, 0,
+                              ctypes.byref(info))
+    if rc != PD_OK:
+        raise PagedDecodeError(rc, "paged_prefill_plan")
+    items = torch.zeros((int(info.num_items), 8), dtype=torch.int32)
+    rc = L.paged_prefill_plan(qs.data_ptr(), sl.data_ptr(), S, int(num_q_heads),
+                              int(num_kv_heads), int(window), int(num_sms),
+                              items.data_ptr() if items.numel() else None, int(info.num_items),
+                              ctypes.byref(info))
+    if rc != PD_OK:
+        raise PagedDecodeError(rc, "paged_prefill_plan")
+    return items, info
+
+
+def paged_prefill_scratch_bytes(num_kv_heads, head_size, num_sms) -> int:
+    return int(lib().paged_prefill_scratch_bytes(int(num_kv_heads), int(head_size), int(num_sms)))
+
+
+def prefill_scratch(num_kv_heads, head_size, num_sms=None, device=None, stream=None) -> "Scratch":
+    """A scratch buffer for every prefill plan made with ``num_sms``."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(device or 0).multi_processor_count
+    nbytes = paged_prefill_scratch_bytes(num_kv_heads, head_size, num_sms)
+    if nbytes == 0:
+        raise PagedDecodeError(-1, "paged_prefill_scratch_bytes")
+    return Scratch(num_sms, 1, 1, head_size, 1, nbytes=nbytes, device=device, stream=stream)
+
+
+def paged_prefill_attn(q, k_cache, v_cache, block_table, seq_lens, query_start, work, info, out,
+                       num_q_heads, num_kv_heads, head_size, page_size, window, scale, layout,
+                       scratch: Optional["Scratch"] = None, stream=None, check: bool = True) -> int:
+    """The prefill call over a work list (``work``: the plan's items on the
+    device, ``info``: its PdPrefillPlanInfo)."""
+    descs = [tensor_desc(t) for t in (q, k_cache, v_cache, block_table, seq_lens, query_start,
+                                      work)]
+    od = tensor_desc(out)
+    sp = ctypes.byref(scratch.desc) if scratch is not None else None
+    rc = lib().paged_prefill_attn(*[ctypes.byref(d) for d in descs], ctypes.byref(info),
+                                  ctypes.byref(od), int(num_q_heads), int(num_kv_heads),
+                                  int(head_size), int(page_size), int(window), float(scale),
+                                  int(layout), sp, _stream_handle(stream))
+    if check and rc != PD_OK:
+        raise PagedDecodeError(rc, "paged_prefill_attn")
+    return rc
+
+
+def prefill_case(case, out=None, scratch=None, stream=None, num_sms=0, plan=None):
+    """Plan (on the host, from the case's host lengths) and run a prefill
+    call on a ``workloads.DecodeCase`` with ``query_start``; returns out."""
+    if plan is None:
+        plan = paged_prefill_plan(case.query_start_host, case.seq_lens_host, case.num_q_heads,
+                                  case.num_kv_heads, case.window, num_sms)
+    items, info = plan
+    work = items.to(case.q.device)
+    if out is None:
+        out = torch.empty_like(case.q)
+    paged_prefill_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens,
+                       case.query_start, work, info, out, case.num_q_heads, case.num_kv_heads,
+                       case.head_size, case.page_size, case.window, case.scale, case.layout,
+                       scratch, stream)
+    return out
 
 
 def paged_decode_device_status(reset: bool = False, stream=None) -> int:

@@ -487,6 +487,8 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   p.status = dev.status;
   p.coop = plan.merge == 2 ? 1 : 0;
   p.mergers = plan.mergers > 0 ? plan.mergers : 1;
+  p.num_seqs = (int)S;
+  p.work = nullptr;
   p.wait_limit_ns = (opts && opts->wait_limit_us > 0)
                         ? (unsigned long long)opts->wait_limit_us * 1000ull
                         : kWaitLimitNs;
@@ -497,7 +499,7 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
     const int64_t cbytes = (scratch->counter_slots * 4 + 255) / 256 * 256;
     const int64_t units = S * num_kv_heads * plan.row_groups;
     const int64_t acc_bytes =
-        (units * plan.max_parts * 8LL * plan.n_tiles * head_size * 4 + 255) / 256 * 256;
+        (units * p.max_parts * 8LL * plan.n_tiles * head_size * 4 + 255) / 256 * 256;
     p.counters = reinterpret_cast<int *>(base);
     p.part_acc = reinterpret_cast<float *>(base + cbytes);
     p.part_ml = reinterpret_cast<float *>(base + cbytes + acc_bytes);
@@ -520,6 +522,27 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
 }
 
 }  // namespace
+
+int device_check(int *num_sms, unsigned int **status) {
+  DeviceInfo d;
+  const int rc = device_info(&d);
+  if (rc != PD_OK) return rc;
+  if (num_sms) *num_sms = d.num_sms;
+  if (status) *status = d.status;
+  return PD_OK;
+}
+
+int check_cache_tensor(const pd_tensor *t, int layout, int Hkv, int P, int D) {
+  return check_cache(t, layout, Hkv, P, D);
+}
+
+int check_rows(const pd_tensor *t, int64_t rows, int Hq, int D) {
+  return check_rows_tensor(t, rows, Hq, D);
+}
+
+int cache_tensor_map(const pd_tensor *t, int layout, CUtensorMap *out) {
+  return encode_cache_map(t, layout, out);
+}
 
 }  // namespace pd
 

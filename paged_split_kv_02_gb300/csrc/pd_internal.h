@@ -65,6 +65,12 @@ struct Params {
   int coop;            // 1: co-resident grid, the last `mergers` arrivals merge
   int mergers;         // K_max of the cooperative merge (a power of two)
   unsigned long long wait_limit_ns;  // bound of a cooperative merger's wait for arrivals
+  int num_seqs;                      // sequences of the call (rows of seq_lens)
+  // prefill: the work list (int32 [items][8]: sequence, tile, segment,
+  // segments, split tile, first partial slot, blocks, 0), or null; the
+  // split tiles and partial slots (per kv head) the scratch holds
+  const int32_t *work;
+  int pf_groups, pf_slots;
 };
 
 struct Launch {
@@ -124,5 +130,33 @@ inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
 
 cudaError_t launch_mma(int D, bool bf16, bool tc, const CUtensorMap &tk, const CUtensorMap &tv,
                        const Params &p, const Launch &l, cudaStream_t stream);
+
+// The current device, checked (an sm_103 part): its SM count and the
+// device status word.  Returns a pd_status.
+int device_check(int *num_sms, unsigned int **status);
+
+// Argument check of a paged cache pool descriptor and of a [rows, Hq, D]
+// token-row descriptor, and the TMA tensor map of a pool (pd_api.cu).
+int check_cache_tensor(const pd_tensor *t, int layout, int Hkv, int P, int D);
+int check_rows(const pd_tensor *t, int64_t rows, int Hq, int D);
+int cache_tensor_map(const pd_tensor *t, int layout, CUtensorMap *out);
+
+// The rotary embedding + paged KV-cache write (pd_rope.cu).
+struct RopeParams {
+  const void *q, *k, *v;
+  int64_t q_s0, q_s1, k_s0, k_s1, v_s0, v_s1;  // element strides of [t][head][:]
+  void *q_out;
+  int64_t qo_s0, qo_s1;
+  void *k_cache, *v_cache;
+  int64_t kc_page, kc_tok, kc_head;  // element strides of (page, token, kv head)
+  int64_t vc_page, vc_tok, vc_head;
+  const int32_t *positions, *slots;
+  const float *cos_sin;
+  int64_t cs_s0;  // floats between table rows
+  int max_pos;
+  int T, Hq, Hkv, D, rot, P;
+  int64_t num_slots;  // pages x page_size
+  unsigned int *status;
+};
 
 }  // namespace pd

@@ -145,9 +145,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   uint32_t tmem_base = 0;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // grid (segment, kv head x row group, sequence)
-  const int seg = blockIdx.x, hg = blockIdx.y, s = blockIdx.z;
-  const int h = p.rg == 1 ? hg : hg / p.rg, grow = hg - h * p.rg;
+  // grid (segment, kv head x row group, sequence); a prefill launch's grid
+  // is (work item, kv head) and its item names the sequence, the tile of
+  // packed rows (the row group) and the segment
+  const bool prefill = p.work != nullptr;
+  int seg = blockIdx.x, hg = blockIdx.y, s = blockIdx.z;
+  int h = p.rg == 1 ? hg : hg / p.rg, grow = hg - h * p.rg;
 
   // ---- set-up that reads no global memory (it overlaps the previous grid's
   // tail): barriers, the tensor-map prefetch (the Q tile is loaded by the
@@ -178,15 +181,15 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   // ---- index arithmetic that reads no global memory, done before the wait
   // so that only loads and a few compares lie between the wait and the
   // first page copy ----
-  const int rr0 = grow * p.rows_cta;
-  const int rr1 = min(p.R, rr0 + p.rows_cta);
+  int rr0 = grow * p.rows_cta;
+  int rr1 = min(p.R, rr0 + p.rows_cta);
   const int lg_g = (p.G & (p.G - 1)) == 0 ? __ffs(p.G) - 1 : -1;  // G a power of two
   auto token_of = [&](int rr) { return lg_g >= 0 ? rr >> lg_g : rr / p.G; };  // packed row -> token
-  const int tok0 = token_of(rr0), tok1 = token_of(rr1 - 1);  // tokens of the first and last row
+  int tok0 = token_of(rr0), tok1 = token_of(rr1 - 1);  // tokens of the first and last row
   const int lg_nt = (NT & (NT - 1)) == 0 ? __ffs(NT) - 1 : -1;
   const int t_n = lg_nt >= 0 ? warp & (NT - 1) : warp % NT;  // consumer n-tile
   const int g_k = lg_nt >= 0 ? warp >> lg_nt : warp / NT;    // consumer warp group
-  const int cl_id = seg / p.CS;
+  int cl_id = seg / p.CS;
   const int bpp = p.P / kBlockKeys;  // 16-key blocks per page
   const int lg_bpp = (bpp & (bpp - 1)) == 0 ? __ffs(bpp) - 1 : -1;
   const int seg_cover = p.max_seg * p.seg_blocks;  // blocks the plan's segments cover
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   const int spec_b0 = seg * p.seg_blocks;
   const int32_t *bt_row = p.block_table + (int64_t)s * p.bt_stride;
   const int bt_blocks = p.bt_width * bpp;
-  const bool spec_on = warp == NC && p.window == 0;
+  const bool spec_on = warp == NC && p.window == 0 && !prefill;
   if (spec_on) {
 #pragma unroll
     for (int k = 0; k < kSpec / 32; ++k) {
@@ -212,12 +215,45 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   // block table or the scratch) has completed, before reading any of them.
   grid_dependency_wait();
 
+  // prefill: the work item (sequence, tile, segment, segments, split tile,
+  // first partial slot), checked against the launch before anything is
+  // addressed with it
+  int pf_nseg = 1, pf_split = 0, pf_slot = 0;
+  if (prefill) {
+    const int4 w0 = __ldg(reinterpret_cast<const int4 *>(p.work) + 2 * (int64_t)blockIdx.x);
+    const int4 w1 = __ldg(reinterpret_cast<const int4 *>(p.work) + 2 * (int64_t)blockIdx.x + 1);
+    s = w0.x;
+    grow = w0.y;
+    seg = w0.z;
+    pf_nseg = w0.w;
+    pf_split = w1.x;
+    pf_slot = w1.y;
+    h = hg = blockIdx.y;
+    const bool ok = s >= 0 && s < p.num_seqs && grow >= 0 && grow <= (INT32_MAX - 64) / p.rows_cta &&
+                    pf_nseg >= 1 && pf_nseg <= p.max_parts && seg >= 0 && seg < pf_nseg &&
+                    (pf_nseg == 1 || (pf_split >= 0 && pf_split < p.pf_groups && pf_slot >= 0 &&
+                                      pf_slot <= p.pf_slots - pf_nseg));
+    if (!ok) {
+      if (tid == 0) atomicOr(p.status, 0x80u);
+      return;
+    }
+    rr0 = grow * p.rows_cta;
+    rr1 = rr0 + p.rows_cta;
+    tok0 = token_of(rr0);
+    tok1 = token_of(rr1 - 1);
+    cl_id = seg;
+    bt_row = p.block_table + (int64_t)s * p.bt_stride;
+  }
+
   int L = __ldg(p.seq_lens + s);
   // q / out rows of the sequence: [s * M, s * M + M), or from query_start
-  int qa = s * p.M, qb = qa + p.M;
+  int qa, qb;
   if (p.query_start) {
     qa = __ldg(p.query_start + s);
     qb = __ldg(p.query_start + s + 1);
+  } else {
+    qa = s * p.M;
+    qb = qa + p.M;
   }
   if (spec_on) {
 #pragma unroll
@@ -254,16 +290,22 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   }
   const int b_first = u_lo / kBlockKeys;
   const int nb = u_hi > u_lo ? (u_hi + kBlockKeys - 1) / kBlockKeys - b_first : 0;
-  // blocks per segment: the plan's, unless the sequence is longer than planned
-  const int sb = nb <= seg_cover ? p.seg_blocks : (nb + p.max_seg - 1) / p.max_seg;
+  // blocks per segment: the plan's, unless the sequence is longer than
+  // planned; a prefill tile's segments are its work items' (every one of
+  // them arrives at the merge, an empty one with an empty partial)
+  const int sb = prefill ? max(1, (nb + pf_nseg - 1) / pf_nseg)
+                         : (nb <= seg_cover ? p.seg_blocks : (nb + p.max_seg - 1) / p.max_seg);
   // Segment x works iff x == 0 or x * sb < nb.
-  if (cl_id > 0 && cl_id * p.CS * sb >= nb) return;  // uniform over the cluster
-  if (seg > 0 && nb <= sb) return;                     // no merge: only segment 0 works
+  if (!prefill) {
+    if (cl_id > 0 && cl_id * p.CS * sb >= nb) return;  // uniform over the cluster
+    if (seg > 0 && nb <= sb) return;                     // no merge: only segment 0 works
+  }
   const int my_b0 = b_first + seg * sb;
   const int my_nb = max(0, min(b_first + nb, my_b0 + sb) - my_b0);
   const int ntile = (my_nb + TB - 1) / TB;
-  const int nseg = max(1, (nb + sb - 1) / sb);  // segments of this (sequence, head, row group)
-  const int ncl = (nseg + p.CS - 1) / p.CS;     // merge clusters
+  // segments of this (sequence, head, row group) and merge clusters
+  const int nseg = prefill ? pf_nseg : max(1, (nb + sb - 1) / sb);
+  const int ncl = (nseg + p.CS - 1) / p.CS;
   if constexpr (TC) {
     // tensor memory for the two S buffers and O; freed once the epilogue has
     // read O (every path of the CTA reaches that point)
@@ -290,7 +332,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     // no TMA issue waits on a dependent global load.
     int *pids = const_cast<int *>(flags + 4);
     int pid_base = 0;
-    const bool spec_ok = p.window == 0 && my_b0 == spec_b0;
+    const bool spec_ok = spec_on && my_b0 == spec_b0;
     auto load_pids = [&](int base) {
       __syncwarp();
       const int n = min(kBlockIds, my_nb - base);
@@ -806,10 +848,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     return obase + (int64_t)(q0 + i) * p.o_s0 + (int64_t)(h * p.G + j) * p.o_s1;
   };
   const int nrows = max(0, rr1v - rr0);  // valid rows of this CTA
-  if (p.query_start && seg == 0 && hg == 0 && s == 0) {
+  if (p.query_start && (prefill ? blockIdx.x == 0 && blockIdx.y == 0 : seg == 0 && hg == 0 && s == 0)) {
     // rows at and past the last request's end (padding of a captured batch)
     // see no key: zeros
-    const int t0 = min(max(__ldg(p.query_start + gridDim.z), 0), p.num_tokens);
+    const int t0 = min(max(__ldg(p.query_start + p.num_seqs), 0), p.num_tokens);
     const int per_row = p.Hq * (D / 8);
 #pragma unroll 1
     for (int64_t i = tid; i < (int64_t)(p.num_tokens - t0) * per_row; i += blockDim.x) {
@@ -823,8 +865,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   const int CS = p.CS;
   const int DS = D / CS;
   const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
-  const int group = (s * p.Hkv + h) * p.rg + grow;
-  const int64_t gbase = (int64_t)group * p.max_parts;
+  // split-KV counters and partial slots of this (sequence, kv head, row
+  // group), or of this prefill tile and kv head (its segments' slots are
+  // consecutive from the item's first slot)
+  const int group = prefill ? pf_split * p.Hkv + h : (s * p.Hkv + h) * p.rg + grow;
+  const int64_t gbase =
+      prefill ? (int64_t)pf_slot * p.Hkv + (int64_t)h * pf_nseg : (int64_t)group * p.max_parts;
   const int64_t slice_floats = (int64_t)NT8 * DS;
 
   if constexpr (TC) {

@@ -282,13 +282,14 @@ def make_case(
 
 def make_varlen_case(name: str, *, seed: int, q_lens: Sequence[int], pad_tokens: int = 0,
                      **kw) -> DecodeCase:
-    """A decode batch with a query length per request (q_lens[s] <= 8,
-    zero allowed) and ``pad_tokens`` rows past the last request, as in a
-    captured batch padded to a fixed token count.  The pool and block table
-    are those of ``make_case`` with ``max_query_len = max(q_lens)`` (at least
-    1); q holds sum(q_lens) + pad_tokens rows, request s at query_start[s]."""
+    """A batch with a query length per request (zero allowed; the decode
+    call takes up to 8, a prefill call any) and ``pad_tokens`` rows past the
+    last request, as in a captured batch padded to a fixed token count.  The
+    pool and block table are those of ``make_case`` with ``max_query_len =
+    max(q_lens)`` (at least 1); q holds sum(q_lens) + pad_tokens rows,
+    request s at query_start[s]."""
     q_lens = [int(m) for m in q_lens]
-    assert all(0 <= m <= 8 for m in q_lens) and len(q_lens) == len(kw["seq_lens"])
+    assert all(0 <= m for m in q_lens) and len(q_lens) == len(kw["seq_lens"])
     M = max(1, max(q_lens) if q_lens else 1)
     if kw.get("max_query_len") is None:
         kw["max_query_len"] = M
@@ -530,3 +531,34 @@ def make_rope_case(name: str, *, seed: int, dtype: torch.dtype, num_tokens: int,
                     cos_sin=rope_cos_sin_table(max_pos, rot_dim), k_cache=k_cache,
                     v_cache=v_cache, packed=packed)
     return case.to(device)
+
+
+def make_prefill_case(name: str, *, seed: int, q_lens: Sequence[int], contexts: Sequence[int],
+                      dtype: torch.dtype = torch.bfloat16, head_size: int = 128,
+                      num_q_heads: int = 32, num_kv_heads: int = 8, page_size: int = 16,
+                      layout: int = HND, window: int = 0, pad_tokens: int = 0,
+                      v_mean: float = 0.0, device: str = "cpu",
+                      gen_device: str = "cpu") -> DecodeCase:
+    """A prefill batch: request s has q_lens[s] new tokens after contexts[s]
+    cached ones (seq_lens = context + q_len, the new tokens' keys included),
+    rows as in ``make_varlen_case``."""
+    lens = [int(c) + int(m) for c, m in zip(contexts, q_lens)]
+    return make_varlen_case(name, seed=seed, q_lens=q_lens, pad_tokens=pad_tokens, dtype=dtype,
+                            head_size=head_size, num_q_heads=num_q_heads,
+                            num_kv_heads=num_kv_heads, page_size=page_size, seq_lens=lens,
+                            layout=layout, window=window, v_mean=v_mean, device=device,
+                            gen_device=gen_device)
+
+
+def prefill_flops(case) -> int:
+    """Multiply-adds x 2 of QK^T and PV over the keys each query row sees."""
+    qs, lens = case.query_start_host, case.seq_lens_host
+    total = 0
+    for s in range(case.num_seqs):
+        q_len = qs[s + 1] - qs[s]
+        ctx = max(lens[s], q_len) - q_len
+        for i in range(q_len):
+            n = ctx + i + 1
+            lo = max(0, n - case.window) if case.window else 0
+            total += n - lo
+    return 4 * case.head_size * case.num_q_heads * total

@@ -350,12 +350,12 @@ def pin_varlen_padding_zero(lib=None):
     assert np.all(o[3:] == 0.0) and np.abs(o[:3]).max() > 0
 
 
-def pin_varlen_library_sdpa(lib=None):
+def pin_varlen_library_sdpa(lib=None, q_lens=(2, 4, 0, 1, 3), lens=(19, 8, 5, 1, 30), window=5):
     """Against torch's scaled_dot_product_attention (fp64) on densely
     gathered keys, each token's request found with numpy's right-sided
     searchsorted over query_start[1:] and its key length seq_len - q_len +
     (t - query_start[r]) + 1 (the query maps of the pages)."""
-    q_lens, lens, window = [2, 4, 0, 1, 3], [19, 8, 5, 1, 30], 5
+    q_lens, lens = list(q_lens), list(lens)
     c = _varlen_case(q_lens, lens, pad=1, window=window, num_q_heads=8, head_size=32,
                      page_size=8, dtype=torch.bfloat16, seed=12)
     o = oracle.attention(c, lib=lib)
@@ -370,7 +370,7 @@ def pin_varlen_library_sdpa(lib=None):
             continue
         L = lens[r]
         klen = max(L - q_lens[r] + (t - int(qsl[r])) + 1, 0)
-        lo = max(0, klen - window)
+        lo = max(0, klen - window) if window else 0
         if klen <= lo:
             assert np.all(o[t] == 0.0)
             continue
@@ -383,11 +383,20 @@ def pin_varlen_library_sdpa(lib=None):
         np.testing.assert_allclose(o[t], ref.permute(1, 0, 2)[0].numpy(), rtol=0, atol=1e-12)
 
 
+def pin_prefill_library_sdpa(lib=None):
+    """Prefill-sized requests (query lengths past 8, one without context,
+    the new tokens' keys included in seq_len) against SDPA the same way,
+    with and without a window; the plan_prefill tiles of a request are the
+    rows of this one definition."""
+    pin_varlen_library_sdpa(lib, q_lens=(37, 1, 20, 0), lens=(60, 9, 20, 3), window=0)
+    pin_varlen_library_sdpa(lib, q_lens=(37, 1, 20, 0), lens=(60, 9, 20, 3), window=13)
+
+
 ALL_PINS = [
     pin_single_key, pin_identical_keys_mean, pin_zero_query_mean, pin_position_mean,
     pin_window_one, pin_wide_window_is_full, pin_page_permutation, pin_layouts,
     pin_split_merge, pin_causal_rows, pin_gqa_is_repeated_mha, pin_gqa_group_of_head,
     pin_one_hot_logit, pin_two_keys_logistic, pin_empty_rows_zero, pin_poison_never_read,
     pin_library_sdpa, pin_widen_exact, pin_varlen_uniform, pin_varlen_request_alone,
-    pin_varlen_padding_zero, pin_varlen_library_sdpa,
+    pin_varlen_padding_zero, pin_varlen_library_sdpa, pin_prefill_library_sdpa,
 ]

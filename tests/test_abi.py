@@ -19,7 +19,8 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = pd.declared_symbols()
-    assert len(names) == 10
+    assert len(names) == 14 and "paged_rope_cache_write" in names
+    assert {"paged_prefill_plan", "paged_prefill_scratch_bytes", "paged_prefill_attn"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -303,3 +304,70 @@ def test_plan_tensor_memory_path():
                              opts=pd.options(path=3, cluster=2, segments=4))
     with pytest.raises(pd.PagedDecodeError):   # the dot path is not built
         pd.paged_decode_plan(1, 32, 8, 128, 16, 1, 0, 256, 152, opts=pd.options(path=2))
+
+
+def test_rope_argument_checks_on_host(lib):
+    """paged_rope_cache_write's argument checks run before any device call."""
+    c = W.make_rope_case("abi", seed=1, dtype=torch.bfloat16, num_tokens=6, num_q_heads=4,
+                         num_kv_heads=2, head_size=64, rot_dim=32, page_size=16, num_pages=2)
+
+    def call(**over):
+        a = dict(q=c.q, k=c.k, v=c.v, positions=c.positions, slot_mapping=c.slot_mapping,
+                 cos_sin_cache=c.cos_sin, q_out=c.q, k_cache=c.k_cache, v_cache=c.v_cache,
+                 num_q_heads=4, num_kv_heads=2, head_size=64, rot_dim=32, page_size=16,
+                 layout=W.HND, is_neox=True)
+        a.update(over)
+        return pd.paged_rope_cache_write(**a, check=False)
+
+    assert call(head_size=96) == -3                       # head size
+    assert call(rot_dim=24) == -1                         # NeoX: rot_dim % 16
+    assert call(rot_dim=80) == -1                         # rot_dim > D
+    assert call(rot_dim=0) == -1
+    assert call(positions=c.positions.to(torch.int64)) == -2          # int32 only
+    assert call(slot_mapping=c.slot_mapping[:5]) == -1                # length
+    assert call(cos_sin_cache=c.cos_sin.to(torch.float16)) == -2      # fp32 table
+    assert call(cos_sin_cache=c.cos_sin[:, :16]) == -1                # narrower than rot_dim
+    assert call(k=c.k.to(torch.float16)) == -2                        # mixed dtypes
+    assert call(q_out=torch.empty(6, 4, 64, dtype=torch.float16)) == -2
+    assert call(num_kv_heads=1) == -1                                 # k shape
+    assert call(layout=W.NHD) == -1                                   # pool shape vs layout
+    assert call(page_size=8) == -1
+    odd = torch.empty(6, 4, 72, dtype=torch.bfloat16)[..., 4:68]      # 8-byte aligned rows
+    assert call(q=odd) == -5
+    empty = W.make_rope_case("abi0", seed=1, dtype=torch.bfloat16, num_tokens=0, num_q_heads=4,
+                             num_kv_heads=2, head_size=64, rot_dim=32, page_size=16,
+                             num_pages=2)
+    assert pd.paged_rope_cache_write(empty.q, empty.k, empty.v, empty.positions,
+                                     empty.slot_mapping, empty.cos_sin, empty.q, empty.k_cache,
+                                     empty.v_cache, 4, 2, 64, 32, 16, W.HND, True,
+                                     check=False) == 0            # nothing to do, no device
+    if not torch.cuda.is_available():
+        assert call() == -8                                           # a valid call needs the GPU
+
+
+def test_prefill_argument_checks_on_host(lib):
+    """paged_prefill_attn's checks run before any device call."""
+    c = W.make_prefill_case("abi_pf", seed=1, q_lens=[70, 20], contexts=[30, 0],
+                            num_q_heads=8, num_kv_heads=2)
+    items, info = pd.paged_prefill_plan(c.query_start_host, c.seq_lens_host, 8, 2, 0, 152)
+
+    def call(**over):
+        a = dict(q=c.q, k_cache=c.k_cache, v_cache=c.v_cache, block_table=c.block_table,
+                 seq_lens=c.seq_lens, query_start=c.query_start, work=items, info=info,
+                 out=c.q, num_q_heads=8, num_kv_heads=2, head_size=128, page_size=16,
+                 window=0, scale=0.1, layout=W.HND, scratch=None)
+        a.update(over)
+        return pd.paged_prefill_attn(**a, check=False)
+
+    assert call(head_size=96) == -3
+    assert call(num_q_heads=7) == -1
+    assert call(work=items[:-1]) == -1                      # rows != info.num_items
+    assert call(work=items[:, :4].contiguous()) == -1       # 8 int32 per item
+    assert call(query_start=c.query_start[:-1]) == -1
+    assert call(query_start=c.query_start.to(torch.int64)) == -2
+    assert call(page_size=24) == -1
+    bad = pd.PdPrefillPlanInfo.from_buffer_copy(info)
+    bad.tile_rows = 32
+    assert call(info=bad) == -1
+    if not torch.cuda.is_available():
+        assert call() == -8                                  # a valid call needs the GPU

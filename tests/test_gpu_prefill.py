@@ -1,0 +1,110 @@
+"""Paged prefill (paged_prefill_plan + paged_prefill_attn) against the fp64
+oracle through the C ABI: requests of any query length over the paged
+cache, the work list made on the host, split tiles merged in the kernel.
+The oracle is the same definition as for decode (each token t of request r
+sees seq_len - q_len + (t - query_start[r]) + 1 keys).  Bounds as for
+decode: max-abs 2e-3 (fp16) / 1e-2 (bf16) and, row by row, 2^-10 / 2^-7 of
+the row's largest oracle value."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_split_kv_02_gb300 as pd
+from paged_split_kv_02_gb300 import workloads as W
+from gpu_helpers import check, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    pd.build()
+    pd.paged_decode_device_status(reset=True)
+    yield
+    assert pd.paged_decode_device_status(reset=True) == 0
+
+
+def _run(case, num_sms=0, rows=None, expect_split=None):
+    g = case.to("cuda")
+    items, info = pd.paged_prefill_plan(case.query_start_host, case.seq_lens_host,
+                                        case.num_q_heads, case.num_kv_heads, case.window,
+                                        num_sms)
+    if expect_split is not None:
+        assert (info.num_split_tiles > 0) == expect_split
+    sms = num_sms or torch.cuda.get_device_properties(0).multi_processor_count
+    sc = pd.prefill_scratch(case.num_kv_heads, case.head_size, sms)
+    out = torch.full_like(g.q, 3.0)
+    pd.prefill_case(g, out=out, scratch=sc, plan=(items, info))
+    torch.cuda.synchronize()
+    assert pd.paged_decode_device_status(reset=True) == 0
+    assert int(sc.counters().abs().sum()) == 0, "counters not left at zero"
+    check(case, out, rows=rows)
+    return out, info
+
+
+def test_single_long_request():
+    c = W.make_prefill_case("pf_single", seed=1, q_lens=[300], contexts=[700])
+    _run(c)
+
+
+def test_mixed_batch_with_empty_request_and_padding():
+    c = W.make_prefill_case("pf_mixed", seed=2, q_lens=[1, 40, 257, 0, 100],
+                            contexts=[0, 1000, 60, 500, 2000], pad_tokens=5)
+    out, _ = _run(c)
+    assert torch.all(out[c.query_start_host[-1]:] == 0)
+
+
+def test_forced_splits_merge_in_kernel():
+    # a large resident-CTA target lowers the load: most tiles are split
+    c = W.make_prefill_case("pf_split", seed=3, q_lens=[64, 200], contexts=[3000, 1500])
+    _, info = _run(c, num_sms=4000, expect_split=True)
+    assert info.num_split_tiles >= 4
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_sliding_window(dtype):
+    c = W.make_prefill_case("pf_window", seed=4, q_lens=[400, 33], contexts=[2000, 0],
+                            dtype=dtype, head_size=256, num_q_heads=8, num_kv_heads=1,
+                            page_size=32, window=256)
+    _run(c)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,P,layout", [(64, 16, 2, 16, W.HND), (128, 8, 8, 32, W.NHD),
+                                                (512, 8, 1, 16, W.HND), (256, 16, 2, 1056, W.HND)])
+def test_head_sizes_layouts_pages(D, Hq, Hkv, P, layout):
+    c = W.make_prefill_case(f"pf_d{D}", seed=5 + D, q_lens=[97, 130], contexts=[500, 1200],
+                            dtype=torch.float16 if D == 512 else torch.bfloat16, head_size=D,
+                            num_q_heads=Hq, num_kv_heads=Hkv, page_size=P, layout=layout,
+                            v_mean=1.0 if D == 512 else 0.0)
+    _run(c)
+
+
+def test_prefill_sized_batch_sampled_rows():
+    # 4 requests x 1024 new tokens after 4k of context: sampled rows
+    c = W.make_prefill_case("pf_big", seed=6, q_lens=[1024] * 4, contexts=[4096] * 4,
+                            v_mean=1.0)
+    rows = sample_rows(c, 96, seed=6)
+    _run(c, rows=rows)
+
+
+def test_bad_work_item_is_skipped_and_reported():
+    c = W.make_prefill_case("pf_bad", seed=7, q_lens=[70], contexts=[100])
+    g = c.to("cuda")
+    items, info = pd.paged_prefill_plan(c.query_start_host, c.seq_lens_host, c.num_q_heads,
+                                        c.num_kv_heads, c.window, 0)
+    bad = items.clone()
+    bad[0, 0] = 5          # a request that does not exist
+    out = torch.full_like(g.q, 3.0)
+    pd.paged_prefill_attn(g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, g.query_start,
+                          bad.cuda(), info, out, c.num_q_heads, c.num_kv_heads, c.head_size,
+                          c.page_size, c.window, c.scale, c.layout, None)
+    torch.cuda.synchronize()
+    assert pd.paged_decode_device_status(reset=True) & pd.DEV_BAD_WORK
+    # the other items ran: rows outside the skipped tile match the oracle
+    tile = int(items[0, 1])
+    G = c.num_q_heads // c.num_kv_heads
+    rows = [(t, h) for t in range(70) for h in range(c.num_q_heads)
+            if not (tile * 64 <= t * G + h % G < (tile + 1) * 64)]
+    check(c, out, rows=rows)
