@@ -169,8 +169,9 @@ typedef struct pd_options {
   int key_groups;    /* warp groups of a CTA that take alternate KV tiles     */
   int stages;        /* shared-memory ring stages (32 KiB each)               */
   int cluster;       /* thread-block cluster size of the merge (1, 2, 4, 8)   */
-  int path;          /* 0 = auto (= 1), 1 = mma.sync, 2 = warp dot (not built:
-                        PD_EINVAL), 3 = tcgen05 MMAs with tensor memory
+  int path;          /* 0 = auto (= 1), 1 = mma.sync, 2 = warp dot products in
+                        fp32 (D <= 256, 8 packed rows per CTA, more in row
+                        groups), 3 = tcgen05 MMAs with tensor memory
                         (D <= 256, 16 packed rows per CTA)                     */
   int max_ctas_hint; /* CTAs the split aims for (0 = the SM count)            */
   int merge;         /* split-KV merge: 0 = auto, 1 = the last-arriving CTA,

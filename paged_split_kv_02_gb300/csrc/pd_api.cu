@@ -190,13 +190,13 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
     return PD_EINVAL;
   if (D != 64 && D != 128 && D != 256 && D != 512) return PD_EHEAD;
   if (M < 1 || M > 8) return PD_EQLEN;
-  // path: 0 = auto (mma.sync), 1 = mma.sync, 3 = tcgen05 with tensor memory
-  // (D <= 256); the warp-dot path (2) is not built
-  if (o.path < 0 || o.path > 3 || o.path == 2) return PD_EINVAL;
+  // path: 0 = auto (mma.sync), 1 = mma.sync, 2 = warp dot products (D <=
+  // 256, one 8-row n-tile per CTA), 3 = tcgen05 with tensor memory (D <= 256)
+  if (o.path < 0 || o.path > 3) return PD_EINVAL;
   if (o.wait_limit_us < 0) return PD_EINVAL;
-  const bool tc = o.path == 3;
-  if (tc && D > 256) return PD_EINVAL;
-  if (tc && o.cluster > 1) return PD_EINVAL;
+  const bool tc = o.path == 3, dot = o.path == 2;
+  if ((tc || dot) && D > 256) return PD_EINVAL;
+  if ((tc || dot) && o.cluster > 1) return PD_EINVAL;
   const int G = Hq / Hkv, R = G * M;
   // One sequence: at most 16 packed rows per CTA.  Every n-tile warp of a
   // warp group reads the whole stage from shared memory, so more rows per
@@ -206,7 +206,7 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   // 81 -> 52 us.  A batch runs several waves and is bound by HBM, where a
   // second read of the pages costs more than it saves: up to 64 rows.
   // (the tensor-memory path takes 16 rows per CTA, four copies of them)
-  const int64_t rows_max = (S <= 1 || tc) ? 16 : 64;
+  const int64_t rows_max = dot ? 8 : (S <= 1 || tc) ? 16 : 64;
   int rg = o.row_groups > 0
                ? o.row_groups
                : (int)std::min<int64_t>(kMaxRowGroups, std::max<int64_t>(1, cdiv(R, rows_max)));
@@ -215,7 +215,10 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   const int NT = (int)cdiv(rows_cta, 8);
   if (NT > kMaxConsumerWarps) return PD_EINVAL;
   const int TB = kStageBytes / 2 / (kBlockKeys * D * 2);
-  const int fixed = tc ? smem_bytes_tc(D, 0) : smem_bytes(D, NT, 0);
+  // (the dot path's P buffers grow with the warp groups: sized for the
+  // most it may use)
+  const int kg_dot = o.key_groups > 0 ? o.key_groups : 3;
+  const int fixed = tc ? smem_bytes_tc(D, 0) : dot ? smem_bytes_dot(D, kg_dot, 0) : smem_bytes(D, NT, 0);
   const int ns_max = std::min(8, (kSmemLimit - fixed - 16 * 8) / kStageBytes);
   // dead ring (+ Q and P tiles) available to the epilogue with NS stages
   auto epi_bytes = [&](int ns) { return tc ? epilogue_bytes_tc(D, ns) : epilogue_bytes(D, NT, ns); };
@@ -291,7 +294,7 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   // Clusters only in the one-wave regime (a batch runs several waves, where
   // the last-arriving CTA's merge overlaps other CTAs' work) and only when
   // the cooperative merge is not possible (it measured faster).
-  if (o.cluster == 0 && !tc && S <= 1 && nseg >= 8 && nseg * part_floats * 4 > (256 << 10) &&
+  if (o.cluster == 0 && !tc && !dot && S <= 1 && nseg >= 8 && nseg * part_floats * 4 > (256 << 10) &&
       !coop_possible)
     CS = 8;
   if (CS != 1 && CS != 2 && CS != 4 && CS != 8) return PD_EINVAL;
@@ -373,7 +376,7 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   if ((int64_t)Hkv * rg * nseg > INT32_MAX || (int64_t)Hkv * rg > 65535 || S > 65535)
     return PD_EINVAL;
 
-  plan->path = tc ? 3 : 1;
+  plan->path = tc ? 3 : dot ? 2 : 1;
   plan->merge = merge;
   plan->mergers = mergers;
   plan->rows = R;
@@ -389,7 +392,7 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   plan->grid_x = (int)(Hkv * rg * nseg);
   plan->grid_y = S;
   plan->block_threads = tc ? kTcThreads : 32 * (NT * KG + 1);
-  plan->smem_bytes = tc ? smem_bytes_tc(D, NS) : smem_bytes(D, NT, NS);
+  plan->smem_bytes = tc ? smem_bytes_tc(D, NS) : dot ? smem_bytes_dot(D, KG, NS) : smem_bytes(D, NT, NS);
   plan->scratch_needed = max_parts > 0 ? partial_bytes(max_parts) : 0;
   return PD_OK;
 }
@@ -512,7 +515,7 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   l.smem = plan.smem_bytes;
   l.cluster = plan.cluster;
   l.cooperative = plan.merge == 2 ? 1 : 0;
-  cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, plan.path == 3, tk, tv, p, l,
+  cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, plan.path, tk, tv, p, l,
                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();

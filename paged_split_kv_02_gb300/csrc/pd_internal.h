@@ -86,6 +86,12 @@ struct Launch {
 inline int smem_bytes(int D, int NT, int NS) {
   return kSmemAlign + NS * kStageBytes + NT * D * 16 + 2 * NS * 8 + 16 + 4 * kBlockIds;
 }
+// The warp dot-product path (one n-tile) adds, 16-byte aligned, the Q rows
+// in fp32 [8][D] and a P buffer [stage keys][8] fp32 per warp group.
+inline int smem_bytes_dot(int D, int KG, int NS) {
+  const int stage_keys = kStageBytes / 2 / (kBlockKeys * D * 2) * kBlockKeys;
+  return smem_bytes(D, 1, NS) + 16 + 8 * D * 4 + KG * stage_keys * 8 * 4;
+}
 
 // Bytes of the epilogue region (the ring and the Q tile once they are dead).
 inline int64_t epilogue_bytes(int D, int NT, int NS) {
@@ -128,7 +134,9 @@ inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
   return combine > final_merge ? combine : final_merge;
 }
 
-cudaError_t launch_mma(int D, bool bf16, bool tc, const CUtensorMap &tk, const CUtensorMap &tv,
+// path: 1 = mma.sync consumers, 2 = warp dot products (D <= 256, one 8-row
+// n-tile), 3 = tcgen05 / tensor memory (D <= 256)
+cudaError_t launch_mma(int D, bool bf16, int path, const CUtensorMap &tk, const CUtensorMap &tv,
                        const Params &p, const Launch &l, cudaStream_t stream);
 
 // The current device, checked (an sm_103 part): its SM count and the

@@ -105,10 +105,12 @@ __device__ __forceinline__ float exp2_or_zero(float x, float m) {
   return sfu_exp2(x - m);
 }
 
-template <int D, bool BF16, bool TC>
+template <int D, bool BF16, bool TC, bool DOT>
 __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     pd_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ Params p) {
+  static_assert(!(TC && DOT), "one consumer kind per instance");
+  static_assert(!DOT || D <= 256, "the warp dot-product consumer serves head sizes up to 256");
   using tag = std::integral_constant<bool, BF16>;
   using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
   constexpr int NBOX = D / 64;                  // 128-byte boxes across the head dim
@@ -143,6 +145,11 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   uint64_t *mbar_merge = fl64 + 1;                               // flags[2..3]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fl64) + 4 + kBlockIds;  // after the page ids
   uint32_t tmem_base = 0;
+  // Warp dot-product path (DOT): Q rows in fp32 [8][D], then one P buffer
+  // [stage keys][8] fp32 per warp group, 16-byte aligned after the page ids
+  float *dot_q = reinterpret_cast<float *>(
+      smem + ((reinterpret_cast<unsigned char *>(tmem_slot) - smem + 15) & ~15));
+  float *dot_p = dot_q + 8 * D;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // grid (segment, kv head x row group, sequence); a prefill launch's grid
@@ -318,6 +325,16 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
 
 
   // Consumer state (kept in registers across the main loop).
+  // (DOT: lane i holds dims [i * DPL, (i + 1) * DPL) of all 8 rows)
+  constexpr int DPL = DOT ? D / 32 : 1;
+  float dacc[DOT ? 8 : 1][DPL], dm[DOT ? 8 : 1], dl[DOT ? 8 : 1];
+#pragma unroll
+  for (int r = 0; r < (DOT ? 8 : 1); ++r) {
+    dm[r] = -INFINITY;
+    dl[r] = 0.f;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) dacc[r][j] = 0.f;
+  }
   float acc[KS][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 #pragma unroll
@@ -620,6 +637,199 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
       m0 = m_used;
       l0 = lsum_all;
     }
+    } else if constexpr (DOT) {
+    // ================= warp dot-product consumers (path 2) ================
+    // A CTA of at most 8 packed rows (one n-tile), each warp group one warp.
+    // Per stage, lane i takes keys i, i + 32, .. of the stage (KPL of them)
+    // for S = Q K^T, dot products in fp32 over 8-dim chunks of its keys'
+    // rows; the row maxima are shared by shuffles (sums stay per lane until
+    // the end); P goes to the warp's buffer in shared memory; then lane i
+    // takes dims [i * DPL, (i + 1) * DPL) of every row for O += P V, key by
+    // key.  P stays fp32 (it is not rounded to the input dtype as the
+    // tensor paths do).
+    constexpr int SKEYS = TB * kBlockKeys;  // keys per stage
+    constexpr int KPL = SKEYS / 32;         // keys per lane
+    static_assert(!DOT || KPL >= 1, "a stage has at least 32 keys");
+    const int nr = max(0, min(8, rr1v - rr0));  // real rows of this CTA
+    int rlo[8], rhi[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      rlo[r] = 0;
+      rhi[r] = 0;
+      if (r < nr) {
+        rhi[r] = max(L - ml + token_of(rr0 + r) + 1, 0);
+        rlo[r] = p.window ? max(0, rhi[r] - p.window) : 0;
+      }
+    }
+    {
+      // the CTA's Q rows, widened to fp32 once (zeros past the real rows)
+      const T *qbase = static_cast<const T *>(p.q);
+      for (int idx = tid; idx < 8 * D; idx += NC * 32) {
+        const int r = idx / D, d = idx - r * D;
+        float v = 0.f;
+        if (r < nr) {
+          const int rr = rr0 + r, i = token_of(rr), jq = rr - i * p.G;
+          const T qv = qbase[(int64_t)(q0 + i) * p.q_s0 + (int64_t)(h * p.G + jq) * p.q_s1 + d];
+          if constexpr (BF16) v = __bfloat162float(qv);
+          else v = __half2float(qv);
+        }
+        dot_q[idx] = v;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
+    }
+    float *pbuf = dot_p + g_k * SKEYS * 8;
+    int slot = g_k % NS, phase = (g_k / NS) & 1;
+    for (int j = g_k; j < ntile; j += KG) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), phase))) {
+        if (lane == 0) {
+          flags[0] = 1;
+          atomicOr(p.status, 0x1u);
+        }
+        break;
+      }
+      const int nbt = min(TB, my_nb - j * TB);
+      const unsigned char *kb = ring + slot * STAGE;
+      const unsigned char *vb = kb + TB * BLOCK_BYTES;
+      const int key_t0 = (my_b0 + j * TB) * kBlockKeys;
+      // S = Q K^T for this lane's keys
+      float sv[KPL][8];
+#pragma unroll
+      for (int i = 0; i < KPL; ++i)
+#pragma unroll
+        for (int r = 0; r < 8; ++r) sv[i][r] = 0.f;
+#pragma unroll 2
+      for (int c = 0; c < D / 8; ++c) {
+        float kf[KPL][8];
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) {
+          const int key = lane + 32 * i, b = key >> 4, kk = key & 15;
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (b < nbt)
+            w = *reinterpret_cast<const uint4 *>(kb + b * BLOCK_BYTES + (c >> 3) * 2048 + kk * 128 +
+                                                 (((c & 7) ^ (kk & 7)) << 4));
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 f;
+            if constexpr (BF16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ws[e]));
+            else f = __half22float2(*reinterpret_cast<const __half2 *>(&ws[e]));
+            kf[i][2 * e] = f.x;
+            kf[i][2 * e + 1] = f.y;
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (r < nr) {
+            const float4 qa = *reinterpret_cast<const float4 *>(dot_q + r * D + 8 * c);
+            const float4 qb = *reinterpret_cast<const float4 *>(dot_q + r * D + 8 * c + 4);
+#pragma unroll
+            for (int i = 0; i < KPL; ++i)
+              sv[i][r] += qa.x * kf[i][0] + qa.y * kf[i][1] + qa.z * kf[i][2] + qa.w * kf[i][3] +
+                          qb.x * kf[i][4] + qb.y * kf[i][5] + qb.z * kf[i][6] + qb.w * kf[i][7];
+          }
+        }
+      }
+      // scale, mask (keys past the stage, outside a row's range), row maxima
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r < nr) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < KPL; ++i) {
+            const int key = lane + 32 * i, k = key_t0 + key;
+            const bool ok = key < nbt * kBlockKeys && k >= rlo[r] && k < rhi[r];
+            sv[i][r] = ok ? sv[i][r] * p.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, sv[i][r]);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          const float mn = fmaxf(dm[r], mx);
+          const float mu = mn == -INFINITY ? 0.f : mn;
+          const float al = sfu_exp2(dm[r] - mu);  // dm = -inf -> 0
+          dm[r] = mn;
+          float ls = 0.f;
+#pragma unroll
+          for (int i = 0; i < KPL; ++i) {
+            sv[i][r] = sfu_exp2(sv[i][r] - mu);
+            ls += sv[i][r];
+          }
+          dl[r] = dl[r] * al + ls;
+#pragma unroll
+          for (int jd = 0; jd < DPL; ++jd) dacc[r][jd] *= al;
+        } else {
+#pragma unroll
+          for (int i = 0; i < KPL; ++i) sv[i][r] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) {
+        float *dst = pbuf + (lane + 32 * i) * 8;
+        *reinterpret_cast<float4 *>(dst) = make_float4(sv[i][0], sv[i][1], sv[i][2], sv[i][3]);
+        *reinterpret_cast<float4 *>(dst + 4) = make_float4(sv[i][4], sv[i][5], sv[i][6], sv[i][7]);
+      }
+      __syncwarp();
+      // O += P V: this lane's dims of every key the rows can see (keys
+      // outside every row's range hold stale or NaN values: skipped)
+      const int d0 = lane * DPL, box = d0 >> 6, chunk = (d0 & 63) >> 3, within = d0 & 7;
+      const int kbeg = max(0, u_lo - key_t0), kend = min(nbt * kBlockKeys, u_hi - key_t0);
+#pragma unroll 4
+      for (int k = kbeg; k < kend; ++k) {
+        const int b = k >> 4, kk = k & 15;
+        const unsigned char *vp =
+            vb + b * BLOCK_BYTES + box * 2048 + kk * 128 + ((chunk ^ (kk & 7)) << 4) + within * 2;
+        float vf[DPL];
+        if constexpr (DPL == 8) {
+          const uint4 w = *reinterpret_cast<const uint4 *>(vp);
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 f;
+            if constexpr (BF16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ws[e]));
+            else f = __half22float2(*reinterpret_cast<const __half2 *>(&ws[e]));
+            vf[2 * e] = f.x;
+            vf[2 * e + 1] = f.y;
+          }
+        } else if constexpr (DPL == 4) {
+          const uint2 w = *reinterpret_cast<const uint2 *>(vp);
+          const uint32_t ws[2] = {w.x, w.y};
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float2 f;
+            if constexpr (BF16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ws[e]));
+            else f = __half22float2(*reinterpret_cast<const __half2 *>(&ws[e]));
+            vf[2 * e] = f.x;
+            vf[2 * e + 1] = f.y;
+          }
+        } else {
+          const uint32_t w = *reinterpret_cast<const uint32_t *>(vp);
+          float2 f;
+          if constexpr (BF16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+          else f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+          vf[0] = f.x;
+          if constexpr (DPL > 1) vf[1] = f.y;
+        }
+        const float4 pa = *reinterpret_cast<const float4 *>(pbuf + k * 8);
+        const float4 pb = *reinterpret_cast<const float4 *>(pbuf + k * 8 + 4);
+        const float pr[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r < nr)
+#pragma unroll
+            for (int jd = 0; jd < DPL; ++jd) dacc[r][jd] += pr[r] * vf[jd];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(empty + slot));
+      slot += KG;
+      while (slot >= NS) {
+        slot -= NS;
+        phase ^= 1;
+      }
+    }
+    // full row sums (each lane summed its own keys)
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dl[r] += __shfl_xor_sync(0xffffffffu, dl[r], o);
     } else {
     // ================= consumers ==========================================
     // Visible key range of this thread's two rows (empty for padding rows).
@@ -907,7 +1117,14 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
       if (!done && lane == 0) atomicOr(p.status, 0x1u);
     }
     tc_fence_before();
-  } else if (warp < NC && lane < 4) {
+  } else if (DOT && warp < NC && lane == 0) {
+    // (the row maxima and sums are the same in every lane)
+#pragma unroll
+    for (int r = 0; r < (DOT ? 8 : 1); ++r) {
+      mrow[g_k * NT8 + r] = dm[r];
+      lrow[g_k * NT8 + r] = dl[r];
+    }
+  } else if (!DOT && warp < NC && lane < 4) {
     mrow[g_k * NT8 + r0] = m0;
     mrow[g_k * NT8 + r1] = m1;
     lrow[g_k * NT8 + r0] = l0;
@@ -920,7 +1137,16 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     // stores from the pass that forms every (row, 4 columns) item of the
     // CTA's partial: sum over the groups of acc_g * exp2(m_g - m*), then
     // normalised (one segment) or published (several).
-    if (!TC && warp < NC) {
+    if (DOT && warp < NC) {
+      float *dst = cp + (size_t)g_k * NT8 * D;
+#pragma unroll
+      for (int r = 0; r < (DOT ? 8 : 1); ++r)
+#pragma unroll
+        for (int jd = 0; jd < DPL; ++jd) {
+          const int d = lane * DPL + jd;
+          dst[r * D + psw(d, r)] = dacc[r][jd];
+        }
+    } else if (!TC && warp < NC) {
       float *dst = cp + (size_t)g_k * NT8 * D;
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
@@ -1614,10 +1840,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   }
 }
 
-template <int D, bool BF16, bool TC>
+template <int D, bool BF16, bool TC, bool DOT = false>
 cudaError_t launch_mma_t(const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
                          const Launch &l, cudaStream_t stream) {
-  auto kern = pd_decode_mma<D, BF16, TC>;
+  auto kern = pd_decode_mma<D, BF16, TC, DOT>;
   // largest dynamic shared memory opted into so far, per device
   static int configured_smem[64] = {};
   int dev = 0;

@@ -3,8 +3,12 @@
 
 namespace pd {
 
-cudaError_t launch_mma_d256(bool bf16, bool tc, const CUtensorMap &tk, const CUtensorMap &tv,
+cudaError_t launch_mma_d256(bool bf16, int path, const CUtensorMap &tk, const CUtensorMap &tv,
                            const Params &p, const Launch &l, cudaStream_t stream) {
+  if (path == 2)
+    return bf16 ? launch_mma_t<256, true, false, true>(tk, tv, p, l, stream)
+                : launch_mma_t<256, false, false, true>(tk, tv, p, l, stream);
+  const bool tc = path == 3;
   if (tc)
     return bf16 ? launch_mma_t<256, true, true>(tk, tv, p, l, stream)
                 : launch_mma_t<256, false, true>(tk, tv, p, l, stream);

@@ -306,7 +306,7 @@ PD_API int paged_prefill_attn(const pd_tensor *q, const pd_tensor *k_cache, cons
   l.cluster = 1;
   l.cooperative = 0;
   if (num_kv_heads > 65535) return PD_EINVAL;
-  cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, false, tk, tv, p, l,
+  cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, 1, tk, tv, p, l,
                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();

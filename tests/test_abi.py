@@ -302,8 +302,31 @@ def test_plan_tensor_memory_path():
     with pytest.raises(pd.PagedDecodeError):   # no clusters on this path
         pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 256, 152, scratch_desc=sd,
                              opts=pd.options(path=3, cluster=2, segments=4))
-    with pytest.raises(pd.PagedDecodeError):   # the dot path is not built
-        pd.paged_decode_plan(1, 32, 8, 128, 16, 1, 0, 256, 152, opts=pd.options(path=2))
+
+
+def test_plan_warp_dot_path():
+    """path 2: one 8-row n-tile per CTA (more rows in row groups), warp
+    groups of one warp, shared memory for fp32 Q rows and the P buffers."""
+    sd = _fake_scratch(1, 32, 8, 128, 4, 256)
+    for M, rg in [(1, 1), (2, 1), (3, 2), (4, 2)]:
+        p = pd.paged_decode_plan(1, 32, 8, 128, 16, M, 0, 2048, 152, scratch_desc=sd,
+                                 opts=pd.options(path=2))
+        assert p["path"] == 2 and p["n_tiles"] == 1 and p["row_groups"] == rg
+        assert p["rows_per_cta"] <= 8 and p["cluster"] == 1
+        KG, NS = p["key_groups"], p["stages"]
+        stage_keys = 32768 // 2 // (16 * 128 * 2) * 16
+        base = 1024 + NS * 32768 + 128 * 16 + 2 * NS * 8 + 16 + 4 * 512
+        assert p["smem_bytes"] == base + 16 + 8 * 128 * 4 + KG * stage_keys * 8 * 4
+        assert p["smem_bytes"] <= 232448
+    for D in (64, 256):
+        p = pd.paged_decode_plan(1, 8, 1, D, 16, 1, 0, 512, 152, scratch_desc=sd,
+                                 opts=pd.options(path=2))
+        assert p["path"] == 2 and p["smem_bytes"] <= 232448
+    with pytest.raises(pd.PagedDecodeError):   # head size 512 is not served
+        pd.paged_decode_plan(1, 8, 1, 512, 16, 1, 0, 64, 152, opts=pd.options(path=2))
+    with pytest.raises(pd.PagedDecodeError):   # no clusters on this path
+        pd.paged_decode_plan(1, 32, 8, 128, 16, 1, 0, 256, 152, scratch_desc=sd,
+                             opts=pd.options(path=2, cluster=2, segments=4))
 
 
 def test_rope_argument_checks_on_host(lib):

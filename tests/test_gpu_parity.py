@@ -332,3 +332,43 @@ def test_varlen_out_of_order_query_start_is_clamped_and_reported():
     assert torch.all(out_full[g.q.shape[0]:] == 7.0), "a row past out was written"
     assert torch.isfinite(out.float()).all()
     assert pd.paged_decode_device_status(reset=True) == pd.DEV_BAD_QSTART
+
+
+# ---- the warp dot-product consumer (path 2) --------------------------------
+
+def _dot(case, **kw):
+    return _parity(case, opts=pd.options(path=2, **kw))
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("L", [128, 1024, 4096])
+def test_warp_dot_spec_decode(M, L):
+    """bf16 D=128 32/8: 4 and 8 packed rows in one CTA, 12 and 16 in two
+    row groups."""
+    _dot(W.spec_decode_hnd(M, L, seed=40 + M))
+
+
+def test_warp_dot_single_seq_nhd():
+    _dot(W.single_seq_nhd(seed=41))
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("M", [1, 4])
+def test_warp_dot_sliding_window(dtype, M):
+    _dot(W.sliding_window(dtype, M, 4096, seed=42))
+
+
+@pytest.mark.parametrize("D", [64, 256])
+def test_warp_dot_head_sizes(D):
+    _dot(W.make_case(f"dot_d{D}", seed=43, dtype=torch.float16, head_size=D, num_q_heads=8,
+                     num_kv_heads=2, page_size=32, max_query_len=2, seq_lens=[1777],
+                     layout=W.NHD))
+
+
+def test_warp_dot_batch_varlen_and_splits():
+    _dot(W.batched_hybrid_pages(seed=44, num_seqs=8, max_len=3000))
+    _dot(W.make_varlen_case("dot_varlen", seed=45, q_lens=[2, 1, 0, 2], pad_tokens=3,
+                            dtype=torch.bfloat16, head_size=128, num_q_heads=16,
+                            num_kv_heads=4, page_size=16, seq_lens=[900, 50, 7, 2100]))
+    _dot(W.spec_decode_hnd(2, 4096, seed=46), segments=7, merge=1)
+    _dot(W.spec_decode_hnd(1, 8192, seed=47, v_mean=1.0))
