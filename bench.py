@@ -862,8 +862,9 @@ def run_prefill(args, world, rank, local):
         "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
                      "traffic_basis": "no ncu capture of this launch", "peak_kind": peak_kind,
-                     "note": "products on mma.sync m16n8k16 (keys on the M side, 8-row "
-                             "n-tiles), against the measured tcgen05-class bf16 peak"},
+                     "note": "products on mma.sync m16n8k16 (rows on the M side, 16 rows "
+                             "per warp, two warp groups; D > 128: keys on the M side), "
+                             "against the measured tcgen05-class bf16 peak"},
         "clocks": clk.summary(),
         "e2e": None,
         "cpu_baseline": cpu,

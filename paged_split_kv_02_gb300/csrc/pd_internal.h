@@ -135,7 +135,8 @@ inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
 }
 
 // path: 1 = mma.sync consumers, 2 = warp dot products (D <= 256, one 8-row
-// n-tile), 3 = tcgen05 / tensor memory (D <= 256)
+// n-tile), 3 = tcgen05 / tensor memory (D <= 256), 4 = mma.sync with the
+// rows on the M side, 16 rows per warp (prefill tiles, D <= 128)
 cudaError_t launch_mma(int D, bool bf16, int path, const CUtensorMap &tk, const CUtensorMap &tv,
                        const Params &p, const Launch &l, cudaStream_t stream);
 

@@ -105,11 +105,12 @@ __device__ __forceinline__ float exp2_or_zero(float x, float m) {
   return sfu_exp2(x - m);
 }
 
-template <int D, bool BF16, bool TC, bool DOT>
+template <int D, bool BF16, bool TC, bool DOT, bool RM>
 __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     pd_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ Params p) {
-  static_assert(!(TC && DOT), "one consumer kind per instance");
+  static_assert((int)TC + (int)DOT + (int)RM <= 1, "one consumer kind per instance");
+  static_assert(!RM || D <= 128, "the rows-on-M consumer keeps Q and O of 16 rows in registers");
   static_assert(!DOT || D <= 256, "the warp dot-product consumer serves head sizes up to 256");
   using tag = std::integral_constant<bool, BF16>;
   using T = std::conditional_t<BF16, __nv_bfloat16, __half>;
@@ -129,7 +130,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   constexpr int SC = TB * kBlockKeys;
   constexpr int PTILE = tc_p_tile_bytes(D);
   constexpr int TMEM_COLS = tc_tmem_cols(D);
-  const int NS = p.NS, NT = p.NT, KG = p.KG, NC = TC ? kTcConsumerWarps : NT * KG;
+  // (RM: one warp per 16 packed rows, the n-tiles taken in pairs)
+  const int NS = p.NS, NT = p.NT, KG = p.KG,
+            NC = TC ? kTcConsumerWarps : RM ? (NT >> 1) * KG : NT * KG;
   const int NT8 = NT * 8;
   const int NTQ = TC ? kTcRows / 8 : NT;  // 8-row groups of the Q tile
   unsigned char *ring = smem;
@@ -166,7 +169,8 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   if (warp == 0) {
     if (lane < NS) {
       mbar_init(smem_u32(full + lane), 1);
-      mbar_init(smem_u32(empty + lane), TC ? 1 : NT);  // TC: freed by the PV MMAs' commit
+      // (TC: freed by the PV MMAs' commit; RM: by its NT / 2 warps)
+      mbar_init(smem_u32(empty + lane), TC ? 1 : RM ? NT >> 1 : NT);
     }
     if constexpr (TC) {
       if (lane < kTcBarriers)
@@ -194,8 +198,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   auto token_of = [&](int rr) { return lg_g >= 0 ? rr >> lg_g : rr / p.G; };  // packed row -> token
   int tok0 = token_of(rr0), tok1 = token_of(rr1 - 1);  // tokens of the first and last row
   const int lg_nt = (NT & (NT - 1)) == 0 ? __ffs(NT) - 1 : -1;
-  const int t_n = lg_nt >= 0 ? warp & (NT - 1) : warp % NT;  // consumer n-tile
-  const int g_k = lg_nt >= 0 ? warp >> lg_nt : warp / NT;    // consumer warp group
+  // consumer n-tile and warp group (RM: warp w of a group takes rows 16w ..)
+  const int t_n = RM ? warp % (NT >> 1) : lg_nt >= 0 ? warp & (NT - 1) : warp % NT;
+  const int g_k = RM ? warp / (NT >> 1) : lg_nt >= 0 ? warp >> lg_nt : warp / NT;
   int cl_id = seg / p.CS;
   const int bpp = p.P / kBlockKeys;  // 16-key blocks per page
   const int lg_bpp = (bpp & (bpp - 1)) == 0 ? __ffs(bpp) - 1 : -1;
@@ -335,6 +340,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
 #pragma unroll
     for (int j = 0; j < DPL; ++j) dacc[r][j] = 0.f;
   }
+  // (RM: O of this warp's 16 rows, D/8 n-tiles of 8 dims)
+  float racc[RM ? D / 8 : 1][4];
+#pragma unroll
+  for (int i = 0; i < (RM ? D / 8 : 1); ++i) racc[i][0] = racc[i][1] = racc[i][2] = racc[i][3] = 0.f;
   float acc[KS][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 #pragma unroll
@@ -830,6 +839,190 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     for (int r = 0; r < 8; ++r)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dl[r] += __shfl_xor_sync(0xffffffffu, dl[r], o);
+    } else if constexpr (RM) {
+    // ================= rows-on-M consumers (prefill tiles) =================
+    // Warp w owns the packed rows 16w .. 16w + 15 (two n-tiles of the Q
+    // tile) and every key of every stage, with the rows on the MMA's M side:
+    //   S[16 rows x 8 keys]  = Q[16 x D] . K^T       (Q fragments in registers)
+    //   O[16 rows x 8 dims] += P[16 x 16 keys] . V   (P straight from S's
+    //                                                 accumulators)
+    // so each stage is read from shared memory once per 16 rows, not once
+    // per 8.  A row lives in the four lanes of one lane >> 2 class: two
+    // xor-shuffles give its maximum.
+    const int gq = lane >> 2, tq = lane & 3;  // fragment row and column pair
+    const int ra = 16 * t_n + gq, rb = ra + 8;  // this lane's two rows
+    int lo_a = 0, hi_a = 0, lo_b = 0, hi_b = 0;
+    if (rr0 + ra < rr1v) {
+      hi_a = max(L - ml + token_of(rr0 + ra) + 1, 0);
+      lo_a = p.window ? max(0, hi_a - p.window) : 0;
+    }
+    if (rr0 + rb < rr1v) {
+      hi_b = max(L - ml + token_of(rr0 + rb) + 1, 0);
+      lo_b = p.window ? max(0, hi_b - p.window) : 0;
+    }
+    {
+      // the Q tile, as for the other consumers
+      const T *qbase = static_cast<const T *>(p.q);
+      for (int idx = tid; idx < NT8 * (D / 8); idx += NC * 32) {
+        const int r = idx / (D / 8), c = idx % (D / 8);
+        const int rr = rr0 + r;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (rr < rr1v) {
+          const int i = token_of(rr), jq = rr - i * p.G;
+          v = __ldg(reinterpret_cast<const uint4 *>(qbase + (int64_t)(q0 + i) * p.q_s0 +
+                                                    (int64_t)(h * p.G + jq) * p.q_s1 + c * 8));
+        }
+        const int tn = r >> 3, rw = r & 7, box = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4 *>(qs + (tn * NBOX + box) * 1024 + rw * 128 + ((cc ^ rw) << 4)) = v;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
+    }
+    // Q as the A operand (16 rows x 16 dims per k-step): matrices (rows 0-7 |
+    // 8-15) x (dims 0-7 | 8-15) of the k-step
+    uint32_t qa[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int j = lane >> 3, row = lane & 7;
+      const int tn = 2 * t_n + (j & 1), chunk = 2 * ks + (j >> 1);
+      ldsm_x4(smem_u32(qs) + (tn * NBOX + (chunk >> 3)) * 1024 + row * 128 +
+                  (((chunk & 7) ^ row) << 4),
+              qa[ks]);
+    }
+    // warp group g_k takes the stages g_k, g_k + KG, ..
+    int slot = g_k % NS, phase = (g_k / NS) & 1;
+    for (int j = g_k; j < ntile; j += KG) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), phase))) {
+        if (lane == 0) {
+          flags[0] = 1;
+          atomicOr(p.status, 0x1u);
+        }
+        break;
+      }
+      const int nbt = min(TB, my_nb - j * TB);
+      const uint32_t kbase = smem_u32(ring + slot * STAGE);
+      const uint32_t vbase = kbase + TB * BLOCK_BYTES;
+      const int key_t0 = (my_b0 + j * TB) * kBlockKeys;
+      constexpr int KN = TB * 2;  // 8-key n-tiles of the stage
+      float sc[KN][4];
+#pragma unroll
+      for (int kn = 0; kn < KN; ++kn) sc[kn][0] = sc[kn][1] = sc[kn][2] = sc[kn][3] = 0.f;
+      // S = Q K^T: K rows are [key][dims], the col-major B of the MMA;
+      // one ldmatrix.x4 serves two n-tiles of one k-step
+#pragma unroll
+      for (int kn = 0; kn < KN; kn += 2) {
+        if ((kn >> 1) < nbt) {  // both n-tiles of block kn / 2
+          const int jm = lane >> 3, kk = (jm >> 1) * 8 + (lane & 7);  // key in the block
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            const int chunk = 2 * ks + (jm & 1);
+            uint32_t b[4];
+            ldsm_x4(kbase + (kn >> 1) * BLOCK_BYTES + (chunk >> 3) * 2048 + kk * 128 +
+                        (((chunk & 7) ^ (kk & 7)) << 4),
+                    b);
+            mma_16816<BF16>(sc[kn], qa[ks], b[0], b[1]);
+            mma_16816<BF16>(sc[kn + 1], qa[ks], b[2], b[3]);
+          }
+        }
+      }
+      // scale, mask, running max of rows ra and rb
+      float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+      for (int kn = 0; kn < KN; ++kn) {
+        const int k0 = key_t0 + kn * 8 + 2 * tq;
+        const bool blk = (kn >> 1) < nbt;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = k0 + (e & 1);
+          const bool ok = blk && ((e < 2) ? (k >= lo_a && k < hi_a) : (k >= lo_b && k < hi_b));
+          sc[kn][e] = ok ? sc[kn][e] * p.scale_log2 : -INFINITY;
+        }
+        mxa = fmaxf(mxa, fmaxf(sc[kn][0], sc[kn][1]));
+        mxb = fmaxf(mxb, fmaxf(sc[kn][2], sc[kn][3]));
+      }
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, o));
+        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, o));
+      }
+      const float mna = fmaxf(m0, mxa), mnb = fmaxf(m1, mxb);
+      const float mua = mna == -INFINITY ? 0.f : mna, mub = mnb == -INFINITY ? 0.f : mnb;
+      const float ala = sfu_exp2(m0 - mua), alb = sfu_exp2(m1 - mub);  // m = -inf -> 0
+      m0 = mna;
+      m1 = mnb;
+      if (__any_sync(0xffffffffu, ala != 1.f || alb != 1.f)) {
+#pragma unroll
+        for (int dn = 0; dn < D / 8; ++dn) {
+          racc[dn][0] *= ala;
+          racc[dn][1] *= ala;
+          racc[dn][2] *= alb;
+          racc[dn][3] *= alb;
+        }
+      }
+      l0 *= ala;
+      l1 *= alb;
+      // P = exp2(S - m) as the A operand of PV, 16 keys (two n-tiles) at a
+      // time; V^T fragments by ldmatrix.trans, V of keys outside every row's
+      // range zeroed (stale or NaN slots)
+#pragma unroll
+      for (int kb = 0; kb < TB; ++kb) {
+        if (kb < nbt) {
+          float pv[2][4];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            pv[u][0] = sfu_exp2(sc[2 * kb + u][0] - mua);
+            pv[u][1] = sfu_exp2(sc[2 * kb + u][1] - mua);
+            pv[u][2] = sfu_exp2(sc[2 * kb + u][2] - mub);
+            pv[u][3] = sfu_exp2(sc[2 * kb + u][3] - mub);
+            l0 += pv[u][0] + pv[u][1];
+            l1 += pv[u][2] + pv[u][3];
+          }
+          uint32_t pa[4];
+          pa[0] = pack2(pv[0][0], pv[0][1], tag{});
+          pa[1] = pack2(pv[0][2], pv[0][3], tag{});
+          pa[2] = pack2(pv[1][0], pv[1][1], tag{});
+          pa[3] = pack2(pv[1][2], pv[1][3], tag{});
+          const int key0 = key_t0 + kb * kBlockKeys;
+          const bool vmask = !(key0 >= u_lo && key0 + kBlockKeys <= u_hi);
+          uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+          if (vmask) {
+            const int ke = key0 + 2 * tq;
+            mlo = ((ke >= u_lo && ke < u_hi) ? 0x0000ffffu : 0u) |
+                  ((ke + 1 >= u_lo && ke + 1 < u_hi) ? 0xffff0000u : 0u);
+            mhi = ((ke + 8 >= u_lo && ke + 8 < u_hi) ? 0x0000ffffu : 0u) |
+                  ((ke + 9 >= u_lo && ke + 9 < u_hi) ? 0xffff0000u : 0u);
+          }
+          const int jm = lane >> 3, kk = (jm & 1) * 8 + (lane & 7);  // key of the block
+          const uint32_t vb = vbase + kb * BLOCK_BYTES + kk * 128;
+#pragma unroll
+          for (int dn = 0; dn < D / 8; dn += 2) {
+            const int chunk = dn + (jm >> 1);
+            uint32_t b[4];
+            ldsm_x4_trans(vb + (chunk >> 3) * 2048 + (((chunk & 7) ^ (kk & 7)) << 4), b);
+            if (vmask) {
+              b[0] &= mlo;
+              b[1] &= mhi;
+              b[2] &= mlo;
+              b[3] &= mhi;
+            }
+            mma_16816<BF16>(racc[dn], pa, b[0], b[1]);
+            mma_16816<BF16>(racc[dn + 1], pa, b[2], b[3]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(empty + slot));
+      slot += KG;
+      while (slot >= NS) {
+        slot -= NS;
+        phase ^= 1;
+      }
+    }
+    // full row sums over the four lanes of a row
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
     } else {
     // ================= consumers ==========================================
     // Visible key range of this thread's two rows (empty for padding rows).
@@ -1124,7 +1317,13 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
       mrow[g_k * NT8 + r] = dm[r];
       lrow[g_k * NT8 + r] = dl[r];
     }
-  } else if (!DOT && warp < NC && lane < 4) {
+  } else if (RM && warp < NC && (lane & 3) == 0) {
+    const int ra = g_k * NT8 + 16 * t_n + (lane >> 2);
+    mrow[ra] = m0;
+    mrow[ra + 8] = m1;
+    lrow[ra] = l0;
+    lrow[ra + 8] = l1;
+  } else if (!DOT && !RM && warp < NC && lane < 4) {
     mrow[g_k * NT8 + r0] = m0;
     mrow[g_k * NT8 + r1] = m1;
     lrow[g_k * NT8 + r0] = l0;
@@ -1146,6 +1345,17 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
           const int d = lane * DPL + jd;
           dst[r * D + psw(d, r)] = dacc[r][jd];
         }
+    } else if (RM && warp < NC) {
+      float *dst = cp + (size_t)g_k * NT8 * D;
+      const int ra = 16 * t_n + (lane >> 2), rb = ra + 8;
+#pragma unroll
+      for (int dn = 0; dn < (RM ? D / 8 : 1); ++dn) {
+        const int d = dn * 8 + 2 * (lane & 3);
+        dst[ra * D + psw(d, ra)] = racc[dn][0];
+        dst[ra * D + psw(d + 1, ra)] = racc[dn][1];
+        dst[rb * D + psw(d, rb)] = racc[dn][2];
+        dst[rb * D + psw(d + 1, rb)] = racc[dn][3];
+      }
     } else if (!TC && warp < NC) {
       float *dst = cp + (size_t)g_k * NT8 * D;
 #pragma unroll
@@ -1840,10 +2050,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   }
 }
 
-template <int D, bool BF16, bool TC, bool DOT = false>
+template <int D, bool BF16, bool TC, bool DOT = false, bool RM = false>
 cudaError_t launch_mma_t(const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
                          const Launch &l, cudaStream_t stream) {
-  auto kern = pd_decode_mma<D, BF16, TC, DOT>;
+  auto kern = pd_decode_mma<D, BF16, TC, DOT, RM>;
   // largest dynamic shared memory opted into so far, per device
   static int configured_smem[64] = {};
   int dev = 0;

@@ -99,21 +99,26 @@ int plan_tiles(const int32_t *query_start, const int32_t *seq_lens, int S, int H
 }
 
 // Launch shape of a prefill tile: 8 n-tiles of 8 rows, one warp group,
-// as many 32 KiB ring stages as fit next to the Q tile.
+// as many 32 KiB ring stages as fit next to the Q tile.  Up to D = 128 the
+// rows sit on the MMA's M side, one warp per 16 rows (path 4: each stage is
+// read from shared memory once per 16 rows); larger heads keep the keys on
+// the M side, one warp per 8 rows (path 1).
 struct PrefillShape {
-  int NT, KG, NS, smem, threads;
+  int NT, KG, NS, smem, threads, path;
 };
 
 int prefill_shape(int D, PrefillShape *sh) {
   sh->NT = kTileRows / 8;
-  sh->KG = 1;
+  sh->path = D <= 128 ? 4 : 1;
+  // path 4: two warp groups of four warps take alternate stages
+  sh->KG = sh->path == 4 ? 2 : 1;
   const int fixed = smem_bytes(D, sh->NT, 0);
-  sh->NS = std::min(8, (kSmemLimit - fixed - 16 * 8) / kStageBytes);
+  sh->NS = std::min(8, (kSmemLimit - fixed - 16 * 8) / kStageBytes) / sh->KG * sh->KG;
   if (sh->NS < 2) return PD_EINVAL;
   if (epilogue_floats(D, sh->NT, sh->KG, 1, kMaxSegments) * 4 > epilogue_bytes(D, sh->NT, sh->NS))
     return PD_EINVAL;
   sh->smem = smem_bytes(D, sh->NT, sh->NS);
-  sh->threads = 32 * (sh->NT * sh->KG + 1);
+  sh->threads = 32 * ((sh->path == 4 ? sh->NT / 2 : sh->NT) * sh->KG + 1);
   return PD_OK;
 }
 
@@ -306,7 +311,7 @@ PD_API int paged_prefill_attn(const pd_tensor *q, const pd_tensor *k_cache, cons
   l.cluster = 1;
   l.cooperative = 0;
   if (num_kv_heads > 65535) return PD_EINVAL;
-  cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, 1, tk, tv, p, l,
+  cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, sh.path, tk, tv, p, l,
                              static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
