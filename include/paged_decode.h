@@ -333,7 +333,7 @@ typedef struct pd_prefill_item {
 } pd_prefill_item;
 
 typedef struct pd_prefill_plan_info {
-  int64_t num_items;       /* work items (launch rows x kv heads)             */
+  int64_t num_items;       /* work items (each runs once per kv head)         */
   int32_t num_split_tiles; /* tiles cut into segments                         */
   int32_t num_slots;       /* partial slots of their segments (per kv head)  */
   int32_t tile_rows;       /* PD_PREFILL_TILE_ROWS                            */
