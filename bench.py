@@ -802,7 +802,7 @@ def run_prefill(args, world, rank, local):
     c0 = reps[0]
     sms = torch.cuda.get_device_properties(local).multi_processor_count
     plan = pd.paged_prefill_plan(c0.query_start_host, c0.seq_lens_host, c0.num_q_heads,
-                                 c0.num_kv_heads, c0.window, sms)
+                                 c0.num_kv_heads, c0.head_size, c0.window, sms)
     items, info = plan
     work = items.to(device)
     sc = pd.prefill_scratch(c0.num_kv_heads, c0.head_size, sms, device=device)
@@ -862,9 +862,9 @@ def run_prefill(args, world, rank, local):
         "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
                      "traffic_basis": "no ncu capture of this launch", "peak_kind": peak_kind,
-                     "note": "products on mma.sync m16n8k16 (rows on the M side, 16 rows "
-                             "per warp, two warp groups; D > 128: keys on the M side), "
-                             "against the measured tcgen05-class bf16 peak"},
+                     "note": "products on tcgen05 (128-row tiles, M = 128; Q, S, P and O "
+                             "in tensor memory; four softmax warps, one MMA-issuing thread), "
+                             "against the measured cuBLAS bf16 peak"},
         "clocks": clk.summary(),
         "e2e": None,
         "cpu_baseline": cpu,

@@ -312,18 +312,21 @@ PD_API int paged_rope_cache_write(const pd_tensor *q, const pd_tensor *k, const 
  * q and out, and its token i sees the keys [lo, seq_lens[s] - q_len_s + i +
  * 1) (lo as in paged_decode_attn).  A launch runs a host-made work list: a
  * request's query tokens are packed token-major into rows (token i, q head
- * h*G + j -> row i*G + j), cut into tiles of PD_PREFILL_TILE_ROWS rows, and
+ * h*G + j -> row i*G + j), cut into tiles of PD_PREFILL_TILE_ROWS rows
+ * (PD_PREFILL_TILE_ROWS_D128 at head size 128, whose tiles run on the
+ * 5th-generation tensor cores with one row per tensor-memory lane), and
  * a tile whose keys (from its window start rounded down to 16 keys, to the
  * last key its last token sees) exceed the mean load per resident CTA is cut
  * into segments, merged in the kernel by the last-arriving segment.  Items
  * are ordered heaviest first.  Each item runs once per kv head. */
 #define PD_PREFILL_TILE_ROWS 64
+#define PD_PREFILL_TILE_ROWS_D128 128
 #define PD_PREFILL_MAX_SEGMENTS 32
 
 /* One work item: a segment of the keys of one tile of one request. */
 typedef struct pd_prefill_item {
   int32_t seq;      /* request of the batch                                   */
-  int32_t tile;     /* tile of PD_PREFILL_TILE_ROWS packed rows of it          */
+  int32_t tile;     /* tile of info.tile_rows packed rows of it               */
   int32_t seg;      /* segment of the tile's keys, 0 .. nseg - 1               */
   int32_t nseg;     /* segments of the tile (1: not split)                    */
   int32_t split;    /* index of the split tile, -1 when nseg == 1             */
@@ -336,7 +339,8 @@ typedef struct pd_prefill_plan_info {
   int64_t num_items;       /* work items (each runs once per kv head)         */
   int32_t num_split_tiles; /* tiles cut into segments                         */
   int32_t num_slots;       /* partial slots of their segments (per kv head)  */
-  int32_t tile_rows;       /* PD_PREFILL_TILE_ROWS                            */
+  int32_t tile_rows;       /* packed rows per tile: PD_PREFILL_TILE_ROWS, or  *
+                            * PD_PREFILL_TILE_ROWS_D128 at head size 128     */
   int32_t max_segments;    /* PD_PREFILL_MAX_SEGMENTS                         */
   int32_t target_ctas;     /* CTAs resident at once the split aims at         */
   int32_t reserved;
@@ -346,14 +350,15 @@ typedef struct pd_prefill_plan_info {
 
 /* The work list of a prefill launch, computed on the host from host copies
  * of query_start [num_seqs + 1] and seq_lens [num_seqs] (each length, or an
- * upper bound).  num_sms: CTAs resident at once (0 = the current device's
- * SM count; this kernel runs one CTA per SM).  items NULL: fill `info` only
- * (a size query); else items[0 .. info->num_items) are written and
- * `capacity` must hold them.  Returns PD_EINVAL on a malformed query_start
- * (negative or decreasing). */
+ * upper bound).  head_size (64, 128, 256 or 512; else PD_EHEAD) sets the
+ * tile rows.  num_sms: CTAs resident at once (0 = the current device's SM
+ * count; this kernel runs one CTA per SM).  items NULL: fill `info` only (a
+ * size query); else items[0 .. info->num_items) are written and `capacity`
+ * must hold them.  Returns PD_EINVAL on a malformed query_start (negative
+ * or decreasing). */
 PD_API int paged_prefill_plan(const int32_t *query_start, const int32_t *seq_lens, int num_seqs,
-                              int num_q_heads, int num_kv_heads, int window, int num_sms,
-                              pd_prefill_item *items, int64_t capacity,
+                              int num_q_heads, int num_kv_heads, int head_size, int window,
+                              int num_sms, pd_prefill_item *items, int64_t capacity,
                               pd_prefill_plan_info *info);
 
 /* Scratch bytes that serve every prefill plan made with this num_sms.
@@ -367,7 +372,7 @@ PD_API size_t paged_prefill_scratch_bytes(int num_kv_heads, int head_size, int n
  *   k_cache, v_cache, block_table, seq_lens: as paged_decode_attn
  *   query_start  [S + 1] int32 device array (the plan's, on the device)
  *   work         [num_items, 8] int32 device copy of the plan's items
- *   info         the plan's info (host)
+ *   info         the plan's info (host), made for this head_size
  *   scratch      needed when info->num_split_tiles > 0 (else may be NULL)
  * Items that do not fit the launch (a request, tile, segment or slot out of
  * range) are skipped and reported as PD_DEV_BAD_WORK. */

@@ -148,7 +148,7 @@ def lib():
         L.paged_decode_version.restype = i32
         L.paged_rope_cache_write.argtypes = [T] * 9 + [i32] * 7 + [vp]
         L.paged_rope_cache_write.restype = i32
-        L.paged_prefill_plan.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, i64,
+        L.paged_prefill_plan.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, i64,
                                          ctypes.POINTER(PdPrefillPlanInfo)]
         L.paged_prefill_plan.restype = i32
         L.paged_prefill_scratch_bytes.argtypes = [i32, i32, i32]
@@ -350,9 +350,11 @@ def rope_case(case, q_out=None, stream=None):
     return q_out
 
 
-def paged_prefill_plan(query_start, seq_lens, num_q_heads, num_kv_heads, window, num_sms=0):
-    """The work list of a prefill launch, made on the host (see the C
-    header): returns (items int32 [n, 8] as a CPU tensor, PdPrefillPlanInfo)."""
+def paged_prefill_plan(query_start, seq_lens, num_q_heads, num_kv_heads, head_size, window,
+                       num_sms=0):
+    """The work list of a prefill launch for this head size, made on the host
+    (see the C header): returns (items int32 [n, 8] as a CPU tensor,
+    PdPrefillPlanInfo)."""
     qs = torch.as_tensor(query_start, dtype=torch.int32).contiguous()
     sl = torch.as_tensor(seq_lens, dtype=torch.int32).contiguous()
     S = int(sl.shape[0])
@@ -361,13 +363,13 @@ def paged_prefill_plan(query_start, seq_lens, num_q_heads, num_kv_heads, window,
     info = PdPrefillPlanInfo()
     L = lib()
     rc = L.paged_prefill_plan(qs.data_ptr(), sl.data_ptr(), S, int(num_q_heads),
-                              int(num_kv_heads), int(window), int(num_sms), None, 0,
-                              ctypes.byref(info))
+                              int(num_kv_heads), int(head_size), int(window), int(num_sms), None,
+                              0, ctypes.byref(info))
     if rc != PD_OK:
         raise PagedDecodeError(rc, "paged_prefill_plan")
     items = torch.zeros((int(info.num_items), 8), dtype=torch.int32)
     rc = L.paged_prefill_plan(qs.data_ptr(), sl.data_ptr(), S, int(num_q_heads),
-                              int(num_kv_heads), int(window), int(num_sms),
+                              int(num_kv_heads), int(head_size), int(window), int(num_sms),
                               items.data_ptr() if items.numel() else None, int(info.num_items),
                               ctypes.byref(info))
     if rc != PD_OK:
@@ -412,7 +414,7 @@ def prefill_case(case, out=None, scratch=None, stream=None, num_sms=0, plan=None
     call on a ``workloads.DecodeCase`` with ``query_start``; returns out."""
     if plan is None:
         plan = paged_prefill_plan(case.query_start_host, case.seq_lens_host, case.num_q_heads,
-                                  case.num_kv_heads, case.window, num_sms)
+                                  case.num_kv_heads, case.head_size, case.window, num_sms)
     items, info = plan
     work = items.to(case.q.device)
     if out is None:

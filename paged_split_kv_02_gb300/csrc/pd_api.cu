@@ -18,7 +18,7 @@ __device__ unsigned int g_status;  // PD_DEV_* bits; read by paged_decode_device
 
 namespace {
 
-constexpr int kVersion = 10100;  // 1.1.0
+constexpr int kVersion = 10200;  // 1.2.0
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block on sm_100-class parts
 constexpr int kMaxDevices = 64;
 

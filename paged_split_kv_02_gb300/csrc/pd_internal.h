@@ -122,6 +122,26 @@ inline int64_t epilogue_bytes_tc(int D, int NS) {
   return (int64_t)NS * kStageBytes + (int64_t)kTcRows * D * 2 + 2LL * tc_p_tile_bytes(D);
 }
 
+// Tensor-memory prefill path (TP, head size 128): 128 packed rows per tile,
+// one per tensor-memory lane.  Columns: Q (two 16-bit elements per column),
+// two S buffers of a stage's keys (fp32), two P buffers (16-bit pairs), O
+// (fp32), rounded up to a power of two.
+constexpr int kTpRows = 128;
+constexpr int tp_s_col(int D) { return D / 2; }
+constexpr int tp_p_col(int D) { return D / 2 + 2 * tc_stage_keys(D); }
+constexpr int tp_o_col(int D) { return D / 2 + 3 * tc_stage_keys(D); }
+constexpr int tp_tmem_cols(int D) {
+  return tp_o_col(D) + D <= 128 ? 128 : tp_o_col(D) + D <= 256 ? 256 : 512;
+}
+static_assert(tp_o_col(128) + 128 <= 512, "tensor memory of a prefill tile");
+// Dynamic shared memory of a tensor-memory prefill launch: ring + barriers
+// + flags + staged page ids + tensor-memory address (Q and P live in tensor
+// memory); its epilogue region is the dead ring.
+inline int smem_bytes_tp(int NS) {
+  return kSmemAlign + NS * kStageBytes + 2 * NS * 8 + kTcBarriers * 8 + 16 + 4 * kBlockIds + 16;
+}
+inline int64_t epilogue_bytes_tp(int NS) { return (int64_t)NS * kStageBytes; }
+
 // Floats the epilogue needs: combine phase and final-merge phase.
 inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
   const int64_t nt8 = 8LL * NT;
@@ -136,7 +156,9 @@ inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
 
 // path: 1 = mma.sync consumers, 2 = warp dot products (D <= 256, one 8-row
 // n-tile), 3 = tcgen05 / tensor memory (D <= 256), 4 = mma.sync with the
-// rows on the M side, 16 rows per warp (prefill tiles, D <= 128)
+// rows on the M side, 16 rows per warp (prefill tiles, D <= 128), 5 =
+// tcgen05 prefill tiles of 128 rows with Q, S, P and O in tensor memory
+// (D = 128)
 cudaError_t launch_mma(int D, bool bf16, int path, const CUtensorMap &tk, const CUtensorMap &tv,
                        const Params &p, const Launch &l, cudaStream_t stream);
 

@@ -28,7 +28,9 @@
 //
 // A second consumer (TC = true) runs the products on the 5th-generation
 // tensor cores instead: tcgen05 MMAs issued by one thread, accumulators in
-// tensor memory, four softmax warps (see the TC branch below).
+// tensor memory, four softmax warps (see the TC branch below).  A third
+// (TP = true) does the same for prefill tiles of 128 packed rows, one row
+// per tensor-memory lane, with Q and P read by the MMAs from tensor memory.
 //
 // Epilogue: the warp groups' (acc, m, l) are combined in shared memory into
 // the CTA's partial.  A sequence cut into several segments publishes the
@@ -58,6 +60,14 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, std::true_type /*b
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, std::false_type /*fp16*/) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
+}
+// lo + hi of a packed pair, widened back to fp32
+__device__ __forceinline__ float sum2(uint32_t w, std::true_type /*bf16*/) {
+  return __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+}
+__device__ __forceinline__ float sum2(uint32_t w, std::false_type /*fp16*/) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+  return f.x + f.y;
 }
 
 // Column swizzle of the fp32 partial tiles in shared memory: rows 2x and 2x+1
@@ -105,11 +115,12 @@ __device__ __forceinline__ float exp2_or_zero(float x, float m) {
   return sfu_exp2(x - m);
 }
 
-template <int D, bool BF16, bool TC, bool DOT, bool RM>
-__global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
+template <int D, bool BF16, bool TC, bool DOT, bool RM, bool TP>
+__global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
     pd_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ Params p) {
-  static_assert((int)TC + (int)DOT + (int)RM <= 1, "one consumer kind per instance");
+  static_assert((int)TC + (int)DOT + (int)RM + (int)TP <= 1, "one consumer kind per instance");
+  static_assert(!TP || D == 128, "the tensor-memory prefill consumer serves head size 128");
   static_assert(!RM || D <= 128, "the rows-on-M consumer keeps Q and O of 16 rows in registers");
   static_assert(!DOT || D <= 256, "the warp dot-product consumer serves head sizes up to 256");
   using tag = std::integral_constant<bool, BF16>;
@@ -129,12 +140,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   // Tensor-memory path (TC): keys per stage, P tile bytes, TMEM columns.
   constexpr int SC = TB * kBlockKeys;
   constexpr int PTILE = tc_p_tile_bytes(D);
-  constexpr int TMEM_COLS = tc_tmem_cols(D);
+  constexpr int TMEM_COLS = TP ? tp_tmem_cols(D) : tc_tmem_cols(D);
   // (RM: one warp per 16 packed rows, the n-tiles taken in pairs)
   const int NS = p.NS, NT = p.NT, KG = p.KG,
-            NC = TC ? kTcConsumerWarps : RM ? (NT >> 1) * KG : NT * KG;
+            NC = TC || TP ? kTcConsumerWarps : RM ? (NT >> 1) * KG : NT * KG;
   const int NT8 = NT * 8;
-  const int NTQ = TC ? kTcRows / 8 : NT;  // 8-row groups of the Q tile
+  const int NTQ = TC ? kTcRows / 8 : TP ? 0 : NT;  // 8-row groups of the Q tile (TP: none)
   unsigned char *ring = smem;
   unsigned char *qs = ring + NS * STAGE;
   unsigned char *pts = qs + NTQ * D * 16;  // TC: two P tiles
@@ -143,7 +154,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   // TC barriers: [0,1] S full, [2,3] S read, [4,5] P written, [6,7] PV done,
   // [8] every MMA done
   uint64_t *tcb = empty + NS;
-  uint64_t *fl64 = tcb + (TC ? kTcBarriers : 0);
+  uint64_t *fl64 = tcb + (TC || TP ? kTcBarriers : 0);
   volatile int *flags = reinterpret_cast<volatile int *>(fl64);  // [0] abort, [1] last
   uint64_t *mbar_merge = fl64 + 1;                               // flags[2..3]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fl64) + 4 + kBlockIds;  // after the page ids
@@ -169,10 +180,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   if (warp == 0) {
     if (lane < NS) {
       mbar_init(smem_u32(full + lane), 1);
-      // (TC: freed by the PV MMAs' commit; RM: by its NT / 2 warps)
-      mbar_init(smem_u32(empty + lane), TC ? 1 : RM ? NT >> 1 : NT);
+      // (TC, TP: freed by the PV MMAs' commit; RM: by its NT / 2 warps)
+      mbar_init(smem_u32(empty + lane), TC || TP ? 1 : RM ? NT >> 1 : NT);
     }
-    if constexpr (TC) {
+    if constexpr (TC || TP) {
       if (lane < kTcBarriers)
         mbar_init(smem_u32(tcb + lane), (lane >= 2 && lane <= 5) ? 4 : 1);
     }
@@ -318,9 +329,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   // segments of this (sequence, head, row group) and merge clusters
   const int nseg = prefill ? pf_nseg : max(1, (nb + sb - 1) / sb);
   const int ncl = (nseg + p.CS - 1) / p.CS;
-  if constexpr (TC) {
-    // tensor memory for the two S buffers and O; freed once the epilogue has
-    // read O (every path of the CTA reaches that point)
+  if constexpr (TC || TP) {
+    // tensor memory for the two S buffers and O (TP: and Q and two P
+    // buffers); freed once the epilogue has read O (every path of the CTA
+    // reaches that point)
     if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -423,7 +435,224 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         if (!mbar_wait_bounded(smem_u32(full + j % NS), (j / NS) & 1)) atomicOr(p.status, 0x1u);
     }
   } else {
-    if constexpr (TC) {
+    if constexpr (TP) {
+    // ================= tensor-memory prefill consumers ====================
+    // The tile's 128 packed rows are the M = 128 side of every MMA, row r in
+    // tensor-memory lane r; softmax warp w (w < 4) owns lanes 32 w .. 32 w +
+    // 31, one row per thread.  Warp 4 issues the MMAs from one thread:
+    //   S[128 x stage keys] = Q . K^T  (A = Q from tensor memory; B = one
+    //                                   16-key K block, K-major; N = 16)
+    //   O[128 x D]         += P . V    (A = P from tensor memory; B = one V
+    //                                   block, MN-major as the copies land)
+    // Two S buffers let the MMAs of stage j + 1 run during the softmax of
+    // stage j; two P buffers let the softmax write P of stage j + 1 while the
+    // PV MMAs of stage j run.  O is rescaled in tensor memory only when a
+    // row's max grows more than 8 past the reference its P values use (so
+    // P <= 2^8), the online-softmax update in exp2 form.
+    static_assert(!TP || SC == 64, "a stage holds 64 keys at head size 128");
+    const uint32_t tQ = tmem_base, tS = tmem_base + tp_s_col(D), tPb = tmem_base + tp_p_col(D),
+                   tO = tmem_base + tp_o_col(D);
+    const int r_tp = 32 * warp + lane, rr_tp = rr0 + r_tp;  // this thread's row (softmax warps)
+    const bool live = warp < kTcConsumerWarps - 1 && rr_tp < rr1v;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    if (warp < kTcConsumerWarps - 1) {
+      // Q row -> tensor memory, 16-bit pairs in memory order (zeros for rows
+      // past the request's tokens)
+      const uint4 *src = nullptr;
+      if (live) {
+        const int i = token_of(rr_tp), jq = rr_tp - i * p.G;
+        src = reinterpret_cast<const uint4 *>(static_cast<const T *>(p.q) +
+                                              (int64_t)(q0 + i) * p.q_s0 +
+                                              (int64_t)(h * p.G + jq) * p.q_s1);
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t w[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 v = live ? __ldg(src + c0 / 4 + u) : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * u] = v.x;
+          w[4 * u + 1] = v.y;
+          w[4 * u + 2] = v.z;
+          w[4 * u + 3] = v.w;
+        }
+        tmem_st32(tQ + lane_base + c0, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");  // Q is in tensor memory
+    if (warp == kTcConsumerWarps - 1) {
+      if (lane == 0) {
+        // ---- MMA issue (one thread) ----
+        tc_fence_after();
+        const uint32_t idS = umma_idesc_f16(kTpRows, kBlockKeys, BF16, 0, 0);
+        const uint32_t idO = umma_idesc_f16(kTpRows, D, BF16, 0, 1);
+        const uint32_t ring_u = smem_u32(ring);
+        bool ok = true;
+        for (int j = 0; j <= ntile; ++j) {
+          if (j < ntile) {
+            const int slot = j % NS;
+            ok = mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1);
+            // S buffer j & 1 was read by the softmax of stage j - 2
+            if (ok && j >= 2) ok = mbar_wait_bounded(smem_u32(tcb + 2 + (j & 1)), ((j - 2) >> 1) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const int nbt = min(TB, my_nb - j * TB);
+            const uint64_t dk = umma_desc_sw128(ring_u + slot * STAGE, 16, 1024);
+            for (int b = 0; b < nbt; ++b) {
+              const uint64_t dkb = dk + (uint64_t)(b * BLOCK_BYTES / 16);
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks)
+                umma_f16_ts(tS + (j & 1) * SC + kBlockKeys * b, tQ + 8 * ks,
+                            dkb + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) / 16), idS,
+                            ks > 0 ? 1u : 0u);
+            }
+            umma_commit(smem_u32(tcb + (j & 1)));  // S of stage j is ready
+          }
+          if (j >= 1) {
+            const int jj = j - 1, slot = jj % NS;
+            ok = mbar_wait_bounded(smem_u32(tcb + 4 + (jj & 1)), (jj >> 1) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const int nbt = min(TB, my_nb - jj * TB);
+            const uint64_t dv = umma_desc_sw128(ring_u + slot * STAGE + TB * BLOCK_BYTES, 2048, 1024);
+            for (int b = 0; b < nbt; ++b)
+              umma_f16_ts(tO, tPb + (jj & 1) * (SC / 2) + 8 * b, dv + (uint64_t)(b * BLOCK_BYTES / 16),
+                          idO, (jj > 0 || b > 0) ? 1u : 0u);
+            umma_commit(smem_u32(empty + slot));        // the stage may be refilled
+            umma_commit(smem_u32(tcb + 6 + (jj & 1)));  // P buffer jj & 1 is free, O is current
+          }
+        }
+        if (!ok) {
+          flags[0] = 1;
+          atomicOr(p.status, 0x1u);
+        }
+        umma_commit(smem_u32(tcb + 8));  // every MMA issued above has completed
+      }
+      __syncwarp();
+    } else {
+      // ---- softmax: one row per thread ----
+      int lo = 0, hi = 0;
+      if (live) {
+        hi = max(L - ml + token_of(rr_tp) + 1, 0);
+        lo = p.window ? max(0, hi - p.window) : 0;
+      }
+      float m_used = -INFINITY, lsum = 0.f;
+      for (int j = 0; j < ntile; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + (j & 1)), (j >> 1) & 1))) {
+          if (lane == 0) {
+            flags[0] = 1;
+            atomicOr(p.status, 0x1u);
+          }
+          break;
+        }
+        tc_fence_after();
+        float sv[SC];
+        {
+          uint32_t x0[32], x1[32];
+          tmem_ld32(tS + lane_base + (j & 1) * SC, x0);
+          tmem_ld32(tS + lane_base + (j & 1) * SC + 32, x1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            sv[i] = __uint_as_float(x0[i]);
+            sv[32 + i] = __uint_as_float(x1[i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(tcb + 2 + (j & 1)));  // S buffer read
+        const int nbt = min(TB, my_nb - j * TB);
+        const int key_t0 = (my_b0 + j * TB) * kBlockKeys;
+        const int slot = j % NS;
+        // every row of the tile sees every key of the stage
+        const bool fast = nbt == TB && key_t0 >= v_lo && key_t0 + SC <= v_hi;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < SC; ++c) {
+          float x = sv[c] * p.scale_log2;
+          const int k = key_t0 + c;
+          if (!live || (!fast && !(c < nbt * kBlockKeys && k >= lo && k < hi))) x = -INFINITY;
+          sv[c] = x;
+          mx = fmaxf(mx, x);
+        }
+        const float m_new = fmaxf(m_used, mx);
+        const bool need = m_used != -INFINITY && m_new > m_used + 8.f;
+        bool ok = true;
+        if (__any_sync(0xffffffffu, need)) {
+          // O must be current: the PV MMAs of stage j - 1 have completed
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_bounded(smem_u32(tcb + 6 + ((j - 1) & 1)), ((j - 1) >> 1) & 1));
+          if (ok) {
+            tc_fence_after();
+            const float alpha = need ? sfu_exp2(m_used - m_new) : 1.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32(tO + lane_base + c0, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(tO + lane_base + c0, o);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            if (need) {
+              lsum *= alpha;
+              m_used = m_new;
+            }
+          }
+        }
+        if (m_used == -INFINITY) m_used = m_new;
+        // P buffer j & 1 is free once the PV MMAs of stage j - 2 have completed
+        if (ok && j >= 2)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_bounded(smem_u32(tcb + 6 + (j & 1)), ((j - 2) >> 1) & 1));
+        if (!ok) {
+          if (lane == 0) {
+            flags[0] = 1;
+            atomicOr(p.status, 0x1u);
+          }
+          break;
+        }
+        {
+          // the row sum takes P as rounded for the MMA, so O is normalised by
+          // the weights it was formed with
+          const float mu = m_used == -INFINITY ? 0.f : m_used;
+          uint32_t w[SC / 2];
+          float ls = 0.f;
+#pragma unroll
+          for (int c = 0; c < SC; c += 2) {
+            w[c >> 1] = pack2(sfu_exp2(sv[c] - mu), sfu_exp2(sv[c + 1] - mu), tag{});
+            ls += sum2(w[c >> 1], tag{});
+          }
+          lsum += ls;
+          tmem_st32(tPb + lane_base + (j & 1) * (SC / 2), w);
+        }
+        // zero V of keys no row sees (outside the union, stale or NaN slots)
+        if (!(nbt == TB && key_t0 >= u_lo && key_t0 + SC <= u_hi)) {
+          unsigned char *vb = ring + slot * STAGE + TB * BLOCK_BYTES;
+          for (int c = 32 * warp + lane; c < nbt * kBlockKeys; c += 128) {
+            const int k = key_t0 + c;
+            if (k < u_lo || k >= u_hi) {
+#pragma unroll 1
+              for (int x = 0; x < NBOX * 8; ++x)
+                *reinterpret_cast<uint4 *>(vb + (c >> 4) * BLOCK_BYTES + (x >> 3) * 2048 +
+                                           (c & 15) * 128 + (x & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();  // the zeroed V reaches the tensor core
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(tcb + 4 + (j & 1)));  // P of stage j written
+      }
+      m0 = m_used;
+      l0 = lsum;
+    }
+    } else if constexpr (TC) {
     // ================= tensor-memory consumers ============================
     // The CTA's packed rows (<= 16) are copied four times into the 64 rows
     // of the Q tile (row 16 q + r = packed row r), so the M = 64 MMAs give
@@ -1276,7 +1505,40 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
       prefill ? (int64_t)pf_slot * p.Hkv + (int64_t)h * pf_nseg : (int64_t)group * p.max_parts;
   const int64_t slice_floats = (int64_t)NT8 * DS;
 
-  if constexpr (TC) {
+  if constexpr (TP) {
+    // O (tensor memory) -> the CTA's partial in shared memory (KG = 1): row
+    // 32 w + lane of softmax warp w, once every MMA has completed
+    if (warp < kTcConsumerWarps - 1) {
+      const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8), 0));
+      tc_fence_after();
+      const int r = 32 * warp + lane;
+      const bool keep = r < NT8;
+      const bool have = ntile > 0 && done;
+      const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+      float *dst = cp + (size_t)r * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tmem_base + tp_o_col(D) + lane_base + c0, o);
+        tmem_wait_ld();
+        if (keep) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 v = have ? make_float4(__uint_as_float(o[i]), __uint_as_float(o[i + 1]),
+                                                __uint_as_float(o[i + 2]), __uint_as_float(o[i + 3]))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4 *>(dst + psw(c0 + i, r)) = v;
+          }
+        }
+      }
+      if (keep) {
+        mrow[r] = have ? m0 : -INFINITY;
+        lrow[r] = have ? l0 : 0.f;
+      }
+      if (!done && lane == 0) atomicOr(p.status, 0x1u);
+    }
+    tc_fence_before();
+  } else if constexpr (TC) {
     // O (tensor memory) -> the CTA's partial in shared memory (one warp group,
     // KG = 1), one row per thread, once every MMA has completed
     if (warp < kTcConsumerWarps - 1) {
@@ -1356,7 +1618,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
         dst[rb * D + psw(d, rb)] = racc[dn][2];
         dst[rb * D + psw(d + 1, rb)] = racc[dn][3];
       }
-    } else if (!TC && warp < NC) {
+    } else if (!TC && !TP && warp < NC) {
       float *dst = cp + (size_t)g_k * NT8 * D;
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
@@ -1368,7 +1630,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
       }
     }
     __syncthreads();
-    if constexpr (TC) {
+    if constexpr (TC || TP) {
       // every read of tensor memory is done
       if (warp == 0) {
         tc_fence_after();
@@ -1459,14 +1721,14 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
     if (nseg == 1) return;
   } else {
   __syncthreads();
-  if constexpr (TC) {
-    // (clusters are not planned on the tensor-memory path; free it anyway)
+  if constexpr (TC || TP) {
+    // (clusters are not planned on the tensor-memory paths; free it anyway)
     if (warp == 0) {
       tc_fence_after();
       tmem_dealloc(tmem_base, TMEM_COLS);
     }
   }
-  if (!TC && warp < NC) {
+  if (!TC && !TP && warp < NC) {
     float ms0 = -INFINITY, ms1 = -INFINITY;
 #pragma unroll 1
     for (int gg = 0; gg < KG; ++gg) {
@@ -1669,8 +1931,11 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
             // poison the group's arrival count so that the next launch on
             // this scratch sees it out of range (and reports it) instead of
             // electing mergers from a stale count; the scratch must be
-            // initialised again before it serves another call
-            atomicAdd(p.counters + 2 * group, 1 << 24);
+            // initialised again before it serves another call.  The sign bit
+            // keeps the count below ncl, so a merger of this launch still
+            // polling keeps waiting (and gives up in turn) rather than take
+            // the poison for the last arrival.
+            atomicOr(p.counters + 2 * group, (int)0x80000000u);
             break;
           }
         }
@@ -2050,10 +2315,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : kMaxThreads, 1)
   }
 }
 
-template <int D, bool BF16, bool TC, bool DOT = false, bool RM = false>
+template <int D, bool BF16, bool TC, bool DOT = false, bool RM = false, bool TP = false>
 cudaError_t launch_mma_t(const CUtensorMap &tk, const CUtensorMap &tv, const Params &p,
                          const Launch &l, cudaStream_t stream) {
-  auto kern = pd_decode_mma<D, BF16, TC, DOT, RM>;
+  auto kern = pd_decode_mma<D, BF16, TC, DOT, RM, TP>;
   // largest dynamic shared memory opted into so far, per device
   static int configured_smem[64] = {};
   int dev = 0;

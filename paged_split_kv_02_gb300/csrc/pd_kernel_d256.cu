@@ -5,6 +5,7 @@ namespace pd {
 
 cudaError_t launch_mma_d256(bool bf16, int path, const CUtensorMap &tk, const CUtensorMap &tv,
                            const Params &p, const Launch &l, cudaStream_t stream) {
+  if (path == 5) return cudaErrorInvalidValue;  // tensor-memory prefill: head size 128
   if (path == 4) return cudaErrorInvalidValue;  // rows-on-M: head sizes up to 128
   if (path == 2)
     return bf16 ? launch_mma_t<256, true, false, true>(tk, tv, p, l, stream)

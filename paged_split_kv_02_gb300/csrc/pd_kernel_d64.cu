@@ -5,6 +5,7 @@ namespace pd {
 
 cudaError_t launch_mma_d64(bool bf16, int path, const CUtensorMap &tk, const CUtensorMap &tv,
                            const Params &p, const Launch &l, cudaStream_t stream) {
+  if (path == 5) return cudaErrorInvalidValue;  // tensor-memory prefill: head size 128
   if (path == 4)
     return bf16 ? launch_mma_t<64, true, false, false, true>(tk, tv, p, l, stream)
                 : launch_mma_t<64, false, false, false, true>(tk, tv, p, l, stream);

@@ -5,7 +5,8 @@
 //
 // A request's query tokens are packed token-major into rows (token i, q
 // head h*G + j -> row i*G + j) and cut into tiles of PD_PREFILL_TILE_ROWS
-// rows; a tile's keys run from its window start (rounded down to a 16-key
+// rows (PD_PREFILL_TILE_ROWS_D128 at head size 128, the tensor-memory
+// tiles); a tile's keys run from its window start (rounded down to a 16-key
 // block) to the last key its last token sees.  A tile heavier than the mean
 // load per resident CTA is cut into segments, merged in the kernel by the
 // last-arriving segment.  Items are ordered heaviest first, so the longest
@@ -20,7 +21,11 @@
 namespace pd {
 namespace {
 
-constexpr int kTileRows = PD_PREFILL_TILE_ROWS;
+// packed rows of a tile: 128 (one per tensor-memory lane) where the
+// tensor-memory consumer serves the head size, else 64
+int tile_rows_for(int D) { return D == 128 ? PD_PREFILL_TILE_ROWS_D128 : PD_PREFILL_TILE_ROWS; }
+static_assert(PD_PREFILL_TILE_ROWS_D128 == kTpRows, "a tensor-memory prefill tile");
+bool head_size_ok(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 constexpr int kMaxSegments = PD_PREFILL_MAX_SEGMENTS;
 // a segment reads at least this many 16-key blocks (two ring stages at
 // D = 128), so that its partial stays small next to the keys it read
@@ -37,8 +42,9 @@ struct Tile {
 
 // The plan shared by paged_prefill_plan and paged_prefill_attn's checks.
 int plan_tiles(const int32_t *query_start, const int32_t *seq_lens, int S, int Hq, int Hkv,
-               int window, int target, std::vector<Tile> *tiles, pd_prefill_plan_info *info) {
-  if (S < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || window < 0 || target <= 0)
+               int rows, int window, int target, std::vector<Tile> *tiles,
+               pd_prefill_plan_info *info) {
+  if (S < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || window < 0 || target <= 0 || rows <= 0)
     return PD_EINVAL;
   if (S > 0 && (!query_start || !seq_lens)) return PD_EINVAL;
   const int G = Hq / Hkv;
@@ -52,12 +58,12 @@ int plan_tiles(const int32_t *query_start, const int32_t *seq_lens, int S, int H
     // as the query length: no context)
     const int64_t L = std::max<int64_t>(seq_lens[s], q_len);
     const int64_t context = L - q_len;
-    const int64_t ntiles = cdiv(q_len * G, kTileRows);
+    const int64_t ntiles = cdiv(q_len * G, rows);
     if (ntiles > INT32_MAX) return PD_EINVAL;
     // the request's last tile first (it sees the most keys)
     for (int64_t t = ntiles - 1; t >= 0; --t) {
-      const int64_t first = t * kTileRows / G;
-      const int64_t last = std::min(q_len - 1, ((t + 1) * kTileRows - 1) / G);
+      const int64_t first = t * rows / G;
+      const int64_t last = std::min(q_len - 1, ((t + 1) * rows - 1) / G);
       const int64_t key_end = context + last + 1;
       const int64_t key_begin =
           window ? std::max<int64_t>(0, context + first - window + 1) / kBlockKeys * kBlockKeys : 0;
@@ -90,7 +96,7 @@ int plan_tiles(const int32_t *query_start, const int32_t *seq_lens, int S, int H
   info->num_items = items;
   info->num_split_tiles = n_split;
   info->num_slots = n_slots;
-  info->tile_rows = kTileRows;
+  info->tile_rows = rows;
   info->max_segments = kMaxSegments;
   info->total_blocks = total;
   info->load_blocks = load;
@@ -98,17 +104,32 @@ int plan_tiles(const int32_t *query_start, const int32_t *seq_lens, int S, int H
   return PD_OK;
 }
 
-// Launch shape of a prefill tile: 8 n-tiles of 8 rows, one warp group,
-// as many 32 KiB ring stages as fit next to the Q tile.  Up to D = 128 the
-// rows sit on the MMA's M side, one warp per 16 rows (path 4: each stage is
-// read from shared memory once per 16 rows); larger heads keep the keys on
-// the M side, one warp per 8 rows (path 1).
+// Launch shape of a prefill tile.  At D = 128: 128 rows on the tensor
+// cores (path 5: Q, S, P and O in tensor memory, four softmax warps and one
+// MMA warp), as many 32 KiB ring stages as fit.  Otherwise 8 n-tiles of 8
+// rows, as many stages as fit next to the Q tile; at D = 64 the rows sit on
+// the MMA's M side, one warp per 16 rows (path 4: each stage is read from
+// shared memory once per 16 rows); larger heads keep the keys on the M side,
+// one warp per 8 rows (path 1).
 struct PrefillShape {
   int NT, KG, NS, smem, threads, path;
+  int64_t epi;  // bytes of the epilogue region
 };
 
 int prefill_shape(int D, PrefillShape *sh) {
-  sh->NT = kTileRows / 8;
+  if (D == 128) {
+    sh->path = 5;
+    sh->NT = kTpRows / 8;
+    sh->KG = 1;
+    sh->NS = std::min(8, (kSmemLimit - smem_bytes_tp(0)) / (kStageBytes + 16));
+    if (sh->NS < 2) return PD_EINVAL;
+    sh->smem = smem_bytes_tp(sh->NS);
+    sh->epi = epilogue_bytes_tp(sh->NS);
+    if (epilogue_floats(D, sh->NT, sh->KG, 1, kMaxSegments) * 4 > sh->epi) return PD_EINVAL;
+    sh->threads = kTcThreads;
+    return PD_OK;
+  }
+  sh->NT = PD_PREFILL_TILE_ROWS / 8;
   sh->path = D <= 128 ? 4 : 1;
   // path 4: two warp groups of four warps take alternate stages
   sh->KG = sh->path == 4 ? 2 : 1;
@@ -118,6 +139,7 @@ int prefill_shape(int D, PrefillShape *sh) {
   if (epilogue_floats(D, sh->NT, sh->KG, 1, kMaxSegments) * 4 > epilogue_bytes(D, sh->NT, sh->NS))
     return PD_EINVAL;
   sh->smem = smem_bytes(D, sh->NT, sh->NS);
+  sh->epi = epilogue_bytes(D, sh->NT, sh->NS);
   sh->threads = 32 * ((sh->path == 4 ? sh->NT / 2 : sh->NT) * sh->KG + 1);
   return PD_OK;
 }
@@ -132,17 +154,18 @@ using namespace pd;
 extern "C" {
 
 PD_API int paged_prefill_plan(const int32_t *query_start, const int32_t *seq_lens, int num_seqs,
-                              int num_q_heads, int num_kv_heads, int window, int num_sms,
-                              pd_prefill_item *items, int64_t capacity,
+                              int num_q_heads, int num_kv_heads, int head_size, int window,
+                              int num_sms, pd_prefill_item *items, int64_t capacity,
                               pd_prefill_plan_info *info) {
   if (!info) return PD_EINVAL;
+  if (!head_size_ok(head_size)) return PD_EHEAD;
   if (num_sms <= 0) {
     int rc = device_check(&num_sms, nullptr);
     if (rc != PD_OK) return rc;
   }
   std::vector<Tile> tiles;
-  int rc = plan_tiles(query_start, seq_lens, num_seqs, num_q_heads, num_kv_heads, window,
-                      num_sms, &tiles, info);
+  int rc = plan_tiles(query_start, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                      tile_rows_for(head_size), window, num_sms, &tiles, info);
   if (rc != PD_OK) return rc;
   if (!items) return PD_OK;  // a size query
   if (capacity < info->num_items) return PD_EINVAL;
@@ -170,15 +193,16 @@ PD_API int paged_prefill_plan(const int32_t *query_start, const int32_t *seq_len
 
 PD_API size_t paged_prefill_scratch_bytes(int num_kv_heads, int head_size, int num_sms) {
   if (num_kv_heads <= 0 || num_sms <= 0) return 0;
-  if (head_size != 64 && head_size != 128 && head_size != 256 && head_size != 512) return 0;
+  if (!head_size_ok(head_size)) return 0;
+  const int rows = tile_rows_for(head_size);
   // counters of paged_decode_scratch_init(.., max_num_seqs = num_sms,
   // num_kv_heads = 1, ..) and partials of 2 x num_sms slots: a plan splits
   // fewer than num_sms tiles x kv heads into fewer than 2 x num_sms
   // segments x kv heads
   const int64_t counters = round256((int64_t)num_sms * PD_COUNTERS_PER_PAIR * 4);
   const int64_t slots = 2LL * num_sms;
-  const int64_t acc = round256(slots * kTileRows * head_size * 4);
-  const int64_t ml = round256(slots * kTileRows * 2 * 4);
+  const int64_t acc = round256(slots * rows * head_size * 4);
+  const int64_t ml = round256(slots * rows * 2 * 4);
   return (size_t)(counters + acc + ml);
 }
 
@@ -192,7 +216,8 @@ PD_API int paged_prefill_attn(const pd_tensor *q, const pd_tensor *k_cache, cons
       !info || !out)
     return PD_EINVAL;
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return PD_EINVAL;
-  if (head_size != 64 && head_size != 128 && head_size != 256 && head_size != 512) return PD_EHEAD;
+  if (!head_size_ok(head_size)) return PD_EHEAD;
+  const int rows = tile_rows_for(head_size);
   if (page_size <= 0 || page_size % kBlockKeys != 0 || window < 0 || !std::isfinite(scale))
     return PD_EINVAL;
   if (layout != PD_NHD && layout != PD_HND) return PD_EINVAL;
@@ -226,7 +251,7 @@ PD_API int paged_prefill_attn(const pd_tensor *q, const pd_tensor *k_cache, cons
   for (int i = 0; i < 4; ++i)
     if (k_cache->shape[i] != v_cache->shape[i]) return PD_EINVAL;
   // the plan: its work list on the device, its sizes from paged_prefill_plan
-  if (info->num_items < 0 || info->num_items > INT32_MAX || info->tile_rows != kTileRows ||
+  if (info->num_items < 0 || info->num_items > INT32_MAX || info->tile_rows != rows ||
       info->num_split_tiles < 0 || info->num_slots < 0 || info->max_segments != kMaxSegments)
     return PD_EINVAL;
   if (work->ndim != 2 || work->shape[0] != info->num_items || work->shape[1] != 8 ||
@@ -248,8 +273,8 @@ PD_API int paged_prefill_attn(const pd_tensor *q, const pd_tensor *k_cache, cons
     if (!scratch || !scratch->data) return PD_ESCRATCH;
     const int64_t cbytes = round256(scratch->counter_slots * 4);
     const int64_t parts = (int64_t)info->num_slots * num_kv_heads;
-    const int64_t acc = round256(parts * kTileRows * head_size * 4);
-    const int64_t ml = round256(parts * kTileRows * 2 * 4);
+    const int64_t acc = round256(parts * rows * head_size * 4);
+    const int64_t ml = round256(parts * rows * 2 * 4);
     if (scratch->counter_slots < 2LL * info->num_split_tiles * num_kv_heads ||
         (int64_t)scratch->bytes < cbytes + acc + ml)
       return PD_ESCRATCH;
@@ -286,7 +311,7 @@ PD_API int paged_prefill_attn(const pd_tensor *q, const pd_tensor *k_cache, cons
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.R = 1 << 30;
   p.rg = 1;
-  p.rows_cta = kTileRows;
+  p.rows_cta = rows;
   p.NT = sh.NT;
   p.KG = sh.KG;
   p.NS = sh.NS;
@@ -295,7 +320,7 @@ PD_API int paged_prefill_attn(const pd_tensor *q, const pd_tensor *k_cache, cons
   p.CS = 1;
   p.max_parts = kMaxSegments;
   p.status = status;
-  p.epi_floats = epilogue_bytes(head_size, sh.NT, sh.NS) / 4;
+  p.epi_floats = sh.epi / 4;
   p.coop = 0;
   p.mergers = 1;
   p.wait_limit_ns = 1000000000ull;

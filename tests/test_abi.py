@@ -26,7 +26,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert pd.paged_decode_version() == 10100
+    assert pd.paged_decode_version() == 10200
     for code in range(0, -9, -1):
         assert lib.paged_decode_strerror(code)
     assert b"unknown" in lib.paged_decode_strerror(-99)
@@ -372,7 +372,7 @@ def test_prefill_argument_checks_on_host(lib):
     """paged_prefill_attn's checks run before any device call."""
     c = W.make_prefill_case("abi_pf", seed=1, q_lens=[70, 20], contexts=[30, 0],
                             num_q_heads=8, num_kv_heads=2)
-    items, info = pd.paged_prefill_plan(c.query_start_host, c.seq_lens_host, 8, 2, 0, 152)
+    items, info = pd.paged_prefill_plan(c.query_start_host, c.seq_lens_host, 8, 2, 128, 0, 152)
 
     def call(**over):
         a = dict(q=c.q, k_cache=c.k_cache, v_cache=c.v_cache, block_table=c.block_table,
@@ -392,5 +392,9 @@ def test_prefill_argument_checks_on_host(lib):
     bad = pd.PdPrefillPlanInfo.from_buffer_copy(info)
     bad.tile_rows = 32
     assert call(info=bad) == -1
+    # a plan made for another head size (64-row tiles) does not fit head size 128
+    items64, info64 = pd.paged_prefill_plan(c.query_start_host, c.seq_lens_host, 8, 2, 64, 0, 152)
+    assert info64.tile_rows == 64 and info.tile_rows == 128
+    assert call(work=items64, info=info64) == -1
     if not torch.cuda.is_available():
         assert call() == -8                                  # a valid call needs the GPU

@@ -29,8 +29,8 @@ def _built():
 def _run(case, num_sms=0, rows=None, expect_split=None):
     g = case.to("cuda")
     items, info = pd.paged_prefill_plan(case.query_start_host, case.seq_lens_host,
-                                        case.num_q_heads, case.num_kv_heads, case.window,
-                                        num_sms)
+                                        case.num_q_heads, case.num_kv_heads, case.head_size,
+                                        case.window, num_sms)
     if expect_split is not None:
         assert (info.num_split_tiles > 0) == expect_split
     sms = num_sms or torch.cuda.get_device_properties(0).multi_processor_count
@@ -81,6 +81,37 @@ def test_head_sizes_layouts_pages(D, Hq, Hkv, P, layout):
     _run(c)
 
 
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 1), (16, 16), (12, 4)])
+def test_tensor_memory_tiles_d128(dtype, Hq, Hkv):
+    # head size 128 runs 128-row tiles on the tensor cores: G = 4, 8, 1 and 3
+    # (a tile then ends inside a token), ragged query lengths, a request with
+    # no context and one shorter than a tile; values shifted so the outputs
+    # are O(1)
+    c = W.make_prefill_case(f"pf_tp_{Hq}_{Hkv}", seed=11 + Hq + Hkv, q_lens=[131, 7, 300, 64],
+                            contexts=[500, 33, 0, 1999], dtype=dtype, head_size=128,
+                            num_q_heads=Hq, num_kv_heads=Hkv, page_size=16, v_mean=1.0)
+    _, info = _run(c)
+    assert info.tile_rows == 128
+
+
+@pytest.mark.parametrize("window", [1, 100, 129])
+def test_tensor_memory_tiles_d128_windows(window):
+    c = W.make_prefill_case(f"pf_tp_w{window}", seed=21 + window, q_lens=[200, 45],
+                            contexts=[700, 0], head_size=128, num_q_heads=16, num_kv_heads=4,
+                            page_size=32, window=window)
+    _run(c)
+
+
+def test_tensor_memory_tiles_d128_split_nhd():
+    # split tiles (a large resident-CTA target) merged in the kernel, NHD pages
+    c = W.make_prefill_case("pf_tp_split", seed=31, q_lens=[256, 100], contexts=[4000, 900],
+                            head_size=128, num_q_heads=32, num_kv_heads=8, page_size=16,
+                            layout=W.NHD, v_mean=1.0)
+    _, info = _run(c, num_sms=4000, expect_split=True)
+    assert info.num_split_tiles >= 4
+
+
 def test_prefill_sized_batch_sampled_rows():
     # 4 requests x 1024 new tokens after 4k of context: sampled rows
     c = W.make_prefill_case("pf_big", seed=6, q_lens=[1024] * 4, contexts=[4096] * 4,
@@ -93,7 +124,7 @@ def test_bad_work_item_is_skipped_and_reported():
     c = W.make_prefill_case("pf_bad", seed=7, q_lens=[70], contexts=[100])
     g = c.to("cuda")
     items, info = pd.paged_prefill_plan(c.query_start_host, c.seq_lens_host, c.num_q_heads,
-                                        c.num_kv_heads, c.window, 0)
+                                        c.num_kv_heads, c.head_size, c.window, 0)
     bad = items.clone()
     bad[0, 0] = 5          # a request that does not exist
     out = torch.full_like(g.q, 3.0)
@@ -103,8 +134,8 @@ def test_bad_work_item_is_skipped_and_reported():
     torch.cuda.synchronize()
     assert pd.paged_decode_device_status(reset=True) & pd.DEV_BAD_WORK
     # the other items ran: rows outside the skipped tile match the oracle
-    tile = int(items[0, 1])
+    tile, TR = int(items[0, 1]), info.tile_rows
     G = c.num_q_heads // c.num_kv_heads
     rows = [(t, h) for t in range(70) for h in range(c.num_q_heads)
-            if not (tile * 64 <= t * G + h % G < (tile + 1) * 64)]
+            if not (tile * TR <= t * G + h % G < (tile + 1) * TR)]
     check(c, out, rows=rows)

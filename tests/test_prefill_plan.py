@@ -1,7 +1,7 @@
 """The prefill work-list planner on the CPU (host code of the C ABI, no
 device): the rules of plan_prefill and prefill_target_workgroups on the
 vllm.v1.attention.ops.rocm_rdna_hip page, restated for this kernel (64
-packed rows per tile, 16-key blocks, one CTA per SM):
+packed rows per tile, 128 at head size 128; 16-key blocks, one CTA per SM):
 
 * a request's tiles cover its q_len x G packed rows, token-major;
 * a tile's keys run from its window start, rounded down to a 16-key block,
@@ -20,17 +20,21 @@ import pytest
 
 import paged_split_kv_02_gb300 as pd
 
-ROWS, FLOOR, MAX_SEG, BLOCK = 64, 8, 32, 16
+FLOOR, MAX_SEG, BLOCK = 8, 32, 16
 
 
-def _plan(q_lens, ctx, Hq=32, Hkv=8, window=0, sms=152):
+def rows_for(D):
+    return 128 if D == 128 else 64
+
+
+def _plan(q_lens, ctx, Hq=32, Hkv=8, window=0, sms=152, D=64):
     qs = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
     lens = (np.asarray(ctx) + np.asarray(q_lens)).astype(np.int32)
-    items, info = pd.paged_prefill_plan(qs, lens, Hq, Hkv, window, sms)
+    items, info = pd.paged_prefill_plan(qs, lens, Hq, Hkv, D, window, sms)
     return items.numpy(), info, qs, lens
 
 
-def _expected_tiles(q_lens, ctx, G, window):
+def _expected_tiles(q_lens, ctx, G, window, ROWS):
     """(seq, tile) -> (first token, last token, key_begin, key_end, blocks)."""
     out = {}
     for s, (m, c) in enumerate(zip(q_lens, ctx)):
@@ -57,6 +61,21 @@ def test_hand_worked_single_request():
     assert np.all(split[:, 3] == 2)
 
 
+def test_hand_worked_single_request_128_row_tiles():
+    # the same request at head size 128: 16 tiles of 32 tokens, tile t sees
+    # 32 (t + 1) keys = 2 (t + 1) blocks; 272 blocks x 8 / 152 = 14.3 per
+    # CTA; tiles of 16 .. 28 blocks split in two, of 30 and 32 in three
+    # (min(ceil(30 / 14.3), 30 // 8) = 3); 7 + 7 x 2 + 2 x 3 = 27 items.
+    # Heaviest per segment first: the 28-block tile's halves (14), then the
+    # unsplit 14-block tile
+    items, info, _, _ = _plan([512], [0], D=128)
+    assert info.tile_rows == 128 and info.total_blocks == 272
+    assert info.num_items == 27 and info.num_split_tiles == 9 and info.num_slots == 20
+    assert [tuple(r) for r in items[:3, :4]] == [(0, 13, 0, 2), (0, 13, 1, 2), (0, 6, 0, 1)]
+    assert sorted(items[items[:, 3] == 3][:, 1].tolist()) == [14] * 3 + [15] * 3
+
+
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("q_lens,ctx,Hq,Hkv,window,sms", [
     ([512], [0], 32, 8, 0, 152),
     ([1, 40, 257, 0, 100], [0, 1000, 60, 500, 3000], 32, 8, 0, 152),
@@ -66,10 +85,11 @@ def test_hand_worked_single_request():
     ([5, 9, 1], [0, 0, 0], 4, 4, 0, 152),                           # tiny
     ([2048], [30000], 64, 8, 4096, 152),
 ])
-def test_plan_rules(q_lens, ctx, Hq, Hkv, window, sms):
+def test_plan_rules(q_lens, ctx, Hq, Hkv, window, sms, D):
     G = Hq // Hkv
-    items, info, qs, lens = _plan(q_lens, ctx, Hq, Hkv, window, sms)
-    exp = _expected_tiles(q_lens, ctx, G, window)
+    ROWS = rows_for(D)
+    items, info, qs, lens = _plan(q_lens, ctx, Hq, Hkv, window, sms, D)
+    exp = _expected_tiles(q_lens, ctx, G, window, ROWS)
     total = sum(v[4] for v in exp.values())
     assert info.total_blocks == total and info.tile_rows == ROWS and info.target_ctas == sms
     load = max(Hkv * total / sms, FLOOR)
@@ -115,25 +135,30 @@ def test_plan_size_query_and_capacity():
     info2 = pd.PdPrefillPlanInfo()
     import ctypes
     L = pd.lib()
-    assert L.paged_prefill_plan(qs.ctypes.data, lens.ctypes.data, 2, 32, 8, 0, 152, None, 0,
+    assert L.paged_prefill_plan(qs.ctypes.data, lens.ctypes.data, 2, 32, 8, 64, 0, 152, None, 0,
                                 ctypes.byref(info2)) == 0
     assert info2.num_items == info.num_items
     buf = (pd.PdPrefillItem * max(1, int(info.num_items) - 1))()
-    assert L.paged_prefill_plan(qs.ctypes.data, lens.ctypes.data, 2, 32, 8, 0, 152, buf,
+    assert L.paged_prefill_plan(qs.ctypes.data, lens.ctypes.data, 2, 32, 8, 64, 0, 152, buf,
                                 int(info.num_items) - 1, ctypes.byref(info2)) == -1
+    # a head size the kernels do not serve
+    assert L.paged_prefill_plan(qs.ctypes.data, lens.ctypes.data, 2, 32, 8, 96, 0, 152, None, 0,
+                                ctypes.byref(info2)) == -3
 
 
 def test_plan_rejects_malformed_query_start():
     with pytest.raises(pd.PagedDecodeError):
-        pd.paged_prefill_plan([0, 10, 5], [10, 10], 32, 8, 0, 152)   # decreasing
+        pd.paged_prefill_plan([0, 10, 5], [10, 10], 32, 8, 128, 0, 152)   # decreasing
     with pytest.raises(pd.PagedDecodeError):
-        pd.paged_prefill_plan([0, 10], [10], 30, 8, 0, 152)          # Hq % Hkv
-    items, info = pd.paged_prefill_plan([0, 0, 0], [5, 0], 32, 8, 0, 152)
+        pd.paged_prefill_plan([0, 10], [10], 30, 8, 128, 0, 152)          # Hq % Hkv
+    items, info = pd.paged_prefill_plan([0, 0, 0], [5, 0], 32, 8, 128, 0, 152)
     assert info.num_items == 0 and items.shape == (0, 8)
 
 
-def test_prefill_scratch_bytes_cover_every_plan():
-    D, Hkv, sms = 128, 8, 152
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_prefill_scratch_bytes_cover_every_plan(D):
+    Hkv, sms = 8, 152
+    ROWS = rows_for(D)
     n = pd.paged_prefill_scratch_bytes(Hkv, D, sms)
     counters = -(-sms * pd.COUNTERS_PER_PAIR * 4 // 256) * 256
     acc = -(-2 * sms * ROWS * D * 4 // 256) * 256
@@ -142,7 +167,7 @@ def test_prefill_scratch_bytes_cover_every_plan():
     # a plan's split tiles and slots fit: (tiles x kv heads) counters in
     # pairs, (slots x kv heads) partials
     for q_lens, ctx in [([512], [0]), ([64] * 8, [8000] * 8), ([2048], [30000])]:
-        _, info, _, _ = _plan(q_lens, ctx, Hkv=Hkv, sms=sms)
+        _, info, _, _ = _plan(q_lens, ctx, Hkv=Hkv, sms=sms, D=D)
         assert 2 * info.num_split_tiles * Hkv <= sms * pd.COUNTERS_PER_PAIR
         assert info.num_slots * Hkv <= 2 * sms
     assert pd.paged_prefill_scratch_bytes(8, 96, 152) == 0
