@@ -72,10 +72,12 @@ std::once_flag g_encode_once;
 struct MapKey {
   const void *ptr;
   int layout;
+  int one_box;
   int64_t dims[4];
   int64_t strides[3];
   bool operator==(const MapKey &o) const {
-    return ptr == o.ptr && layout == o.layout && std::memcmp(dims, o.dims, sizeof dims) == 0 &&
+    return ptr == o.ptr && layout == o.layout && one_box == o.one_box &&
+           std::memcmp(dims, o.dims, sizeof dims) == 0 &&
            std::memcmp(strides, o.strides, sizeof strides) == 0;
   }
 };
@@ -96,7 +98,7 @@ std::mutex g_map_mu;
 // consumers' ldmatrix reads.  A TMA copy has a fixed per-copy cost (2 KiB
 // boxes stream at ~33 GB/s per SM on GB300); one copy per block is 32*D
 // bytes (4 KiB at D = 128, 16 KiB at D = 512).
-int encode_cache_map(const pd_tensor *t, int layout, CUtensorMap *out) {
+int encode_cache_map(const pd_tensor *t, int layout, CUtensorMap *out, bool one_box = false) {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
     void *fn = nullptr;
@@ -115,6 +117,7 @@ int encode_cache_map(const pd_tensor *t, int layout, CUtensorMap *out) {
   MapKey key{};
   key.ptr = t->data;
   key.layout = layout;
+  key.one_box = one_box ? 1 : 0;
   for (int i = 0; i < 4; ++i) key.dims[i] = t->shape[i];
   for (int i = 0; i < 3; ++i) key.strides[i] = t->stride[i];
   std::lock_guard<std::mutex> lock(g_map_mu);
@@ -128,7 +131,9 @@ int encode_cache_map(const pd_tensor *t, int layout, CUtensorMap *out) {
                         (cuuint64_t)t->shape[hi], (cuuint64_t)t->shape[0]};
   cuuint64_t strides[4] = {(cuuint64_t)t->stride[ti] * 2, 128, (cuuint64_t)t->stride[hi] * 2,
                            (cuuint64_t)t->stride[0] * 2};  // bytes
-  cuuint32_t box[5] = {64, (cuuint32_t)kBlockKeys, (cuuint32_t)(D / 64), 1, 1};
+  // a copy lands a 16-key block with all of its D/64 128-byte rows, or
+  // (one_box) one 64-dim box of it
+  cuuint32_t box[5] = {64, (cuuint32_t)kBlockKeys, one_box ? 1u : (cuuint32_t)(D / 64), 1, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUtensorMap m;
   CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, t->data, dims, strides, box, estr,
@@ -543,8 +548,8 @@ int check_rows(const pd_tensor *t, int64_t rows, int Hq, int D) {
   return check_rows_tensor(t, rows, Hq, D);
 }
 
-int cache_tensor_map(const pd_tensor *t, int layout, CUtensorMap *out) {
-  return encode_cache_map(t, layout, out);
+int cache_tensor_map(const pd_tensor *t, int layout, CUtensorMap *out, bool one_box) {
+  return encode_cache_map(t, layout, out, one_box);
 }
 
 }  // namespace pd

@@ -123,17 +123,22 @@ inline int64_t epilogue_bytes_tc(int D, int NS) {
 }
 
 // Tensor-memory prefill path (TP, head size 128): 128 packed rows per tile,
-// one per tensor-memory lane.  Columns: Q (two 16-bit elements per column),
-// two S buffers of a stage's keys (fp32), two P buffers (16-bit pairs), O
-// (fp32), rounded up to a power of two.
+// one per tensor-memory lane; two groups of four softmax warps take the
+// even and the odd stages, each with its own O; one warp issues the MMAs.
+// Columns: Q (two 16-bit elements per column), two S buffers of a stage's
+// keys (fp32), two P buffers (16-bit pairs), two O (fp32), rounded up to a
+// power of two.
 constexpr int kTpRows = 128;
+constexpr int kTpSoftmaxWarps = 8;
+constexpr int kTpConsumerWarps = kTpSoftmaxWarps + 1;
+constexpr int kTpThreads = 32 * (kTpConsumerWarps + 1);
 constexpr int tp_s_col(int D) { return D / 2; }
 constexpr int tp_p_col(int D) { return D / 2 + 2 * tc_stage_keys(D); }
 constexpr int tp_o_col(int D) { return D / 2 + 3 * tc_stage_keys(D); }
 constexpr int tp_tmem_cols(int D) {
-  return tp_o_col(D) + D <= 128 ? 128 : tp_o_col(D) + D <= 256 ? 256 : 512;
+  return tp_o_col(D) + 2 * D <= 128 ? 128 : tp_o_col(D) + 2 * D <= 256 ? 256 : 512;
 }
-static_assert(tp_o_col(128) + 128 <= 512, "tensor memory of a prefill tile");
+static_assert(tp_o_col(128) + 2 * 128 <= 512, "tensor memory of a prefill tile");
 // Dynamic shared memory of a tensor-memory prefill launch: ring + barriers
 // + flags + staged page ids + tensor-memory address (Q and P live in tensor
 // memory); its epilogue region is the dead ring.
@@ -150,7 +155,8 @@ inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {
                           (CS > 1 ? nt8 * (D / CS) + 2 * nt8 + (int64_t)CS * nt8 : 0) + 16;
   // weights and sums of every part, then a chunk buffer of >= one row chunk
   // of one part (rows * D/CS <= 16 floats per thread)
-  const int64_t final_merge = 2LL * ncl_max * nt8 + nt8 + 16 + 16LL * kMaxThreads + D;
+  const int64_t final_merge = 2LL * ncl_max * nt8 + nt8 + 16 +
+                              16LL * (kMaxThreads > kTpThreads ? kMaxThreads : kTpThreads) + D;
   return combine > final_merge ? combine : final_merge;
 }
 
@@ -170,7 +176,9 @@ int device_check(int *num_sms, unsigned int **status);
 // token-row descriptor, and the TMA tensor map of a pool (pd_api.cu).
 int check_cache_tensor(const pd_tensor *t, int layout, int Hkv, int P, int D);
 int check_rows(const pd_tensor *t, int64_t rows, int Hq, int D);
-int cache_tensor_map(const pd_tensor *t, int layout, CUtensorMap *out);
+// one_box: a copy lands one 64-dim box of a 16-key block instead of all of
+// them (the tensor-memory prefill's K, landed box-major).
+int cache_tensor_map(const pd_tensor *t, int layout, CUtensorMap *out, bool one_box = false);
 
 // The rotary embedding + paged KV-cache write (pd_rope.cu).
 struct RopeParams {

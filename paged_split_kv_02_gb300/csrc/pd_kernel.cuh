@@ -116,7 +116,7 @@ __device__ __forceinline__ float exp2_or_zero(float x, float m) {
 }
 
 template <int D, bool BF16, bool TC, bool DOT, bool RM, bool TP>
-__global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
+__global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThreads, 1)
     pd_decode_mma(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ Params p) {
   static_assert((int)TC + (int)DOT + (int)RM + (int)TP <= 1, "one consumer kind per instance");
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
   constexpr int TMEM_COLS = TP ? tp_tmem_cols(D) : tc_tmem_cols(D);
   // (RM: one warp per 16 packed rows, the n-tiles taken in pairs)
   const int NS = p.NS, NT = p.NT, KG = p.KG,
-            NC = TC || TP ? kTcConsumerWarps : RM ? (NT >> 1) * KG : NT * KG;
+            NC = TC ? kTcConsumerWarps : TP ? kTpConsumerWarps : RM ? (NT >> 1) * KG : NT * KG;
   const int NT8 = NT * 8;
   const int NTQ = TC ? kTcRows / 8 : TP ? 0 : NT;  // 8-row groups of the Q tile (TP: none)
   unsigned char *ring = smem;
@@ -409,9 +409,25 @@ __global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
       const int nbt = min(TB, my_nb - j * TB);
       if (lane == 0) mbar_arrive_expect_tx(smem_u32(full + slot), nbt * 2 * BLOCK_BYTES);
       __syncwarp();
-      if (lane < 2 * nbt) {
-        // one copy per 16-key block of K or V (all D/64 swizzle rows at once)
-        const int kv = lane >= nbt, b = lane - kv * nbt;
+      if (TP && lane < nbt * NBOX) {
+        // TP's K: one copy per (16-key block, 64-dim box), box-major in the
+        // stage ([box][block][16 keys][128 B]) so that one box's keys are
+        // consecutive 128-byte rows (one MMA descriptor spans the stage)
+        const int b = lane / NBOX, x = lane - b * NBOX;
+        const int blk = my_b0 + j * TB + b;
+        const int key_in_page = (lg_bpp >= 0 ? blk & (bpp - 1) : blk % bpp) * kBlockKeys;
+        int phys = pids[j * TB + b - pid_base];
+        if ((unsigned)phys >= (unsigned)p.num_pool_blocks) {
+          atomicOr(p.status, 0x2u);  // a page id outside the pool: report, read page 0
+          phys = 0;
+        }
+        const uint32_t dst = smem_u32(ring + slot * STAGE + x * (TB * BLOCK_BYTES / NBOX) +
+                                      b * (BLOCK_BYTES / NBOX));
+        tma_load_5d(dst, &tmK, smem_u32(full + slot), 0, key_in_page, x, h, phys, pol);
+      } else if (TP ? lane >= nbt * NBOX && lane < nbt * (NBOX + 1) : lane < 2 * nbt) {
+        // one copy per 16-key block of K or V (all D/64 swizzle rows at once;
+        // TP: V only)
+        const int kv = TP ? 1 : lane >= nbt, b = TP ? lane - nbt * NBOX : lane - kv * nbt;
         const int blk = my_b0 + j * TB + b;
         const int key_in_page = (lg_bpp >= 0 ? blk & (bpp - 1) : blk % bpp) * kBlockKeys;
         int phys = pids[j * TB + b - pid_base];
@@ -438,24 +454,29 @@ __global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
     if constexpr (TP) {
     // ================= tensor-memory prefill consumers ====================
     // The tile's 128 packed rows are the M = 128 side of every MMA, row r in
-    // tensor-memory lane r; softmax warp w (w < 4) owns lanes 32 w .. 32 w +
-    // 31, one row per thread.  Warp 4 issues the MMAs from one thread:
-    //   S[128 x stage keys] = Q . K^T  (A = Q from tensor memory; B = one
-    //                                   16-key K block, K-major; N = 16)
+    // tensor-memory lane r.  Softmax warp w (w < 8) owns lanes 32 (w % 4) ..
+    // 32 (w % 4) + 31, one row per thread, and the stages of parity w / 4:
+    // two groups of four warps, each an independent online softmax over its
+    // stages with its own O in tensor memory (merged in the epilogue like
+    // warp groups).  Warp 8 issues the MMAs from one thread:
+    //   S[128 x stage keys] = Q . K^T  (A = Q from tensor memory; B = the
+    //                                   stage's K, landed box-major, K-major;
+    //                                   N = 64, one MMA per 16 dims)
     //   O[128 x D]         += P . V    (A = P from tensor memory; B = one V
     //                                   block, MN-major as the copies land)
-    // Two S buffers let the MMAs of stage j + 1 run during the softmax of
-    // stage j; two P buffers let the softmax write P of stage j + 1 while the
-    // PV MMAs of stage j run.  O is rescaled in tensor memory only when a
-    // row's max grows more than 8 past the reference its P values use (so
-    // P <= 2^8), the online-softmax update in exp2 form.
+    // S, P and O of stage j are the buffers of its parity: the MMAs of stage
+    // j + 1 run during the softmax of stage j, and the two groups' softmaxes
+    // overlap.  O is rescaled in tensor memory only when a row's max grows
+    // more than 8 past the reference its P values use (so P <= 2^8), the
+    // online-softmax update in exp2 form.
     static_assert(!TP || SC == 64, "a stage holds 64 keys at head size 128");
     const uint32_t tQ = tmem_base, tS = tmem_base + tp_s_col(D), tPb = tmem_base + tp_p_col(D),
                    tO = tmem_base + tp_o_col(D);
-    const int r_tp = 32 * warp + lane, rr_tp = rr0 + r_tp;  // this thread's row (softmax warps)
-    const bool live = warp < kTcConsumerWarps - 1 && rr_tp < rr1v;
+    const int r_tp = 32 * (warp & 3) + lane, rr_tp = rr0 + r_tp;  // this thread's row
+    const int g_tp = warp >> 2;                                   // softmax group: stage parity
+    const bool live = warp < kTpSoftmaxWarps && rr_tp < rr1v;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    if (warp < kTcConsumerWarps - 1) {
+    if (warp < 4) {
       // Q row -> tensor memory, 16-bit pairs in memory order (zeros for rows
       // past the request's tokens)
       const uint4 *src = nullptr;
@@ -482,64 +503,64 @@ __global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
       tc_fence_before();
     }
     asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");  // Q is in tensor memory
-    if (warp == kTcConsumerWarps - 1) {
-      if (lane == 0) {
-        // ---- MMA issue (one thread) ----
-        tc_fence_after();
-        const uint32_t idS = umma_idesc_f16(kTpRows, kBlockKeys, BF16, 0, 0);
-        const uint32_t idO = umma_idesc_f16(kTpRows, D, BF16, 0, 1);
-        const uint32_t ring_u = smem_u32(ring);
-        bool ok = true;
-        for (int j = 0; j <= ntile; ++j) {
-          if (j < ntile) {
-            const int slot = j % NS;
-            ok = mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1);
-            // S buffer j & 1 was read by the softmax of stage j - 2
-            if (ok && j >= 2) ok = mbar_wait_bounded(smem_u32(tcb + 2 + (j & 1)), ((j - 2) >> 1) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            const int nbt = min(TB, my_nb - j * TB);
-            const uint64_t dk = umma_desc_sw128(ring_u + slot * STAGE, 16, 1024);
-            for (int b = 0; b < nbt; ++b) {
-              const uint64_t dkb = dk + (uint64_t)(b * BLOCK_BYTES / 16);
+    if (warp == kTpConsumerWarps - 1) {
+      // ---- MMA issue: the whole warp runs the loop (every operand is
+      // warp-uniform), one elected lane issues each MMA and commit ----
+      tc_fence_after();
+      const uint32_t idS = umma_idesc_f16(kTpRows, SC, BF16, 0, 0);
+      const uint32_t idO = umma_idesc_f16(kTpRows, D, BF16, 0, 1);
+      const uint32_t ring_u = smem_u32(ring);
+      bool ok = true;
+      for (int j = 0; j <= ntile; ++j) {
+        if (j < ntile) {
+          const int slot = j % NS;
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1));
+          // S buffer j & 1 was read by the softmax of stage j - 2
+          if (ok && j >= 2)
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_bounded(smem_u32(tcb + 2 + (j & 1)), ((j - 2) >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          // all SC keys of the stage at once (keys of blocks a short stage
+          // did not load give scores the softmax masks)
+          const uint32_t kst = ring_u + slot * STAGE;
 #pragma unroll
-              for (int ks = 0; ks < KS; ++ks)
-                umma_f16_ts(tS + (j & 1) * SC + kBlockKeys * b, tQ + 8 * ks,
-                            dkb + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) / 16), idS,
-                            ks > 0 ? 1u : 0u);
-            }
-            umma_commit(smem_u32(tcb + (j & 1)));  // S of stage j is ready
-          }
-          if (j >= 1) {
-            const int jj = j - 1, slot = jj % NS;
-            ok = mbar_wait_bounded(smem_u32(tcb + 4 + (jj & 1)), (jj >> 1) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            const int nbt = min(TB, my_nb - jj * TB);
-            const uint64_t dv = umma_desc_sw128(ring_u + slot * STAGE + TB * BLOCK_BYTES, 2048, 1024);
-            for (int b = 0; b < nbt; ++b)
-              umma_f16_ts(tO, tPb + (jj & 1) * (SC / 2) + 8 * b, dv + (uint64_t)(b * BLOCK_BYTES / 16),
-                          idO, (jj > 0 || b > 0) ? 1u : 0u);
-            umma_commit(smem_u32(empty + slot));        // the stage may be refilled
-            umma_commit(smem_u32(tcb + 6 + (jj & 1)));  // P buffer jj & 1 is free, O is current
-          }
+          for (int ks = 0; ks < KS; ++ks)
+            umma_f16_ts_warp(tS + (j & 1) * SC, tQ + 8 * ks,
+                             umma_desc_sw128(kst + (ks >> 2) * (TB * BLOCK_BYTES / NBOX) + (ks & 3) * 32,
+                                             16, 1024),
+                             idS, ks > 0 ? 1u : 0u);
+          umma_commit_warp(smem_u32(tcb + (j & 1)));  // S of stage j is ready
         }
-        if (!ok) {
-          flags[0] = 1;
-          atomicOr(p.status, 0x1u);
+        if (j >= 1) {
+          const int jj = j - 1, slot = jj % NS;
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 4 + (jj & 1)), (jj >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const int nbt = min(TB, my_nb - jj * TB);
+          const uint64_t dv = umma_desc_sw128(ring_u + slot * STAGE + TB * BLOCK_BYTES, 2048, 1024);
+          for (int b = 0; b < nbt; ++b)
+            umma_f16_ts_warp(tO + (jj & 1) * D, tPb + (jj & 1) * (SC / 2) + 8 * b,
+                             dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (jj > 1 || b > 0) ? 1u : 0u);
+          umma_commit_warp(smem_u32(empty + slot));        // the stage may be refilled
+          umma_commit_warp(smem_u32(tcb + 6 + (jj & 1)));  // P buffer jj & 1 is free, its O current
         }
-        umma_commit(smem_u32(tcb + 8));  // every MMA issued above has completed
       }
-      __syncwarp();
+      if (!ok && lane == 0) {
+        flags[0] = 1;
+        atomicOr(p.status, 0x1u);
+      }
+      umma_commit_warp(smem_u32(tcb + 8));  // every MMA issued above has completed
     } else {
-      // ---- softmax: one row per thread ----
+      // ---- softmax: one row per thread, the stages of this group's parity ----
       int lo = 0, hi = 0;
       if (live) {
         hi = max(L - ml + token_of(rr_tp) + 1, 0);
         lo = p.window ? max(0, hi - p.window) : 0;
       }
+      const uint32_t tOg = tO + g_tp * D;
       float m_used = -INFINITY, lsum = 0.f;
-      for (int j = 0; j < ntile; ++j) {
+      for (int j = g_tp; j < ntile; j += 2) {
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + (j & 1)), (j >> 1) & 1))) {
           if (lane == 0) {
             flags[0] = 1;
@@ -548,7 +569,7 @@ __global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
           break;
         }
         tc_fence_after();
-        float sv[SC];
+        uint32_t sr[SC];  // the row's scores of the stage (fp32 bits)
         {
           uint32_t x0[32], x1[32];
           tmem_ld32(tS + lane_base + (j & 1) * SC, x0);
@@ -556,8 +577,8 @@ __global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            sv[i] = __uint_as_float(x0[i]);
-            sv[32 + i] = __uint_as_float(x1[i]);
+            sr[i] = x0[i];
+            sr[32 + i] = x1[i];
           }
         }
         tc_fence_before();
@@ -566,49 +587,79 @@ __global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
         const int nbt = min(TB, my_nb - j * TB);
         const int key_t0 = (my_b0 + j * TB) * kBlockKeys;
         const int slot = j % NS;
-        // every row of the tile sees every key of the stage
+        // every row of the tile sees every key of the stage: no mask, and the
+        // scale is applied inside the exponent (rows past the request's
+        // tokens have Q = 0, finite scores, and are never stored)
         const bool fast = nbt == TB && key_t0 >= v_lo && key_t0 + SC <= v_hi;
-        float mx = -INFINITY;
+        const float sl2 = p.scale_log2;
+        float mx;
+        if (fast) {
+          // the largest scaled score: the largest (scale >= 0) or smallest
+          // raw score, eight independent chains
+          float a[8];
 #pragma unroll
-        for (int c = 0; c < SC; ++c) {
-          float x = sv[c] * p.scale_log2;
-          const int k = key_t0 + c;
-          if (!live || (!fast && !(c < nbt * kBlockKeys && k >= lo && k < hi))) x = -INFINITY;
-          sv[c] = x;
-          mx = fmaxf(mx, x);
+          for (int u = 0; u < 8; ++u) a[u] = __uint_as_float(sr[u]);
+          if (sl2 >= 0.f) {
+#pragma unroll
+            for (int c = 8; c < SC; ++c) a[c & 7] = fmaxf(a[c & 7], __uint_as_float(sr[c]));
+#pragma unroll
+            for (int u = 4; u >= 1; u >>= 1)
+#pragma unroll
+              for (int v = 0; v < u; ++v) a[v] = fmaxf(a[v], a[v + u]);
+          } else {
+#pragma unroll
+            for (int c = 8; c < SC; ++c) a[c & 7] = fminf(a[c & 7], __uint_as_float(sr[c]));
+#pragma unroll
+            for (int u = 4; u >= 1; u >>= 1)
+#pragma unroll
+              for (int v = 0; v < u; ++v) a[v] = fminf(a[v], a[v + u]);
+          }
+          mx = a[0] * sl2;
+        } else {
+          // scaled scores with the mask applied (-inf), kept as fp32 bits
+          float a[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) a[u] = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < SC; ++c) {
+            const int k = key_t0 + c;
+            float x = __uint_as_float(sr[c]) * sl2;
+            if (!live || !(c < nbt * kBlockKeys && k >= lo && k < hi)) x = -INFINITY;
+            sr[c] = __float_as_uint(x);
+            a[c & 7] = fmaxf(a[c & 7], x);
+          }
+#pragma unroll
+          for (int u = 4; u >= 1; u >>= 1)
+#pragma unroll
+            for (int v = 0; v < u; ++v) a[v] = fmaxf(a[v], a[v + u]);
+          mx = a[0];
         }
         const float m_new = fmaxf(m_used, mx);
         const bool need = m_used != -INFINITY && m_new > m_used + 8.f;
-        bool ok = true;
-        if (__any_sync(0xffffffffu, need)) {
-          // O must be current: the PV MMAs of stage j - 1 have completed
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait_bounded(smem_u32(tcb + 6 + ((j - 1) & 1)), ((j - 1) >> 1) & 1));
-          if (ok) {
-            tc_fence_after();
-            const float alpha = need ? sfu_exp2(m_used - m_new) : 1.f;
+        // the PV MMAs of this group's previous stage (j - 2) have completed:
+        // its P buffer is free and its O current
+        bool ok = j < 2 || __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 6 + (j & 1)),
+                                                                     ((j - 2) >> 1) & 1));
+        tc_fence_after();
+        if (ok && __any_sync(0xffffffffu, need)) {
+          const float alpha = need ? sfu_exp2(m_used - m_new) : 1.f;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t o[32];
-              tmem_ld32(tO + lane_base + c0, o);
-              tmem_wait_ld();
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tOg + lane_base + c0, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(tO + lane_base + c0, o);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            if (need) {
-              lsum *= alpha;
-              m_used = m_new;
-            }
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tOg + lane_base + c0, o);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          if (need) {
+            lsum *= alpha;
+            m_used = m_new;
           }
         }
         if (m_used == -INFINITY) m_used = m_new;
-        // P buffer j & 1 is free once the PV MMAs of stage j - 2 have completed
-        if (ok && j >= 2)
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait_bounded(smem_u32(tcb + 6 + (j & 1)), ((j - 2) >> 1) & 1));
         if (!ok) {
           if (lane == 0) {
             flags[0] = 1;
@@ -617,23 +668,32 @@ __global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
           break;
         }
         {
-          // the row sum takes P as rounded for the MMA, so O is normalised by
-          // the weights it was formed with
+          // P = 2^(x - m) rounded to the input type; the row sum takes P as
+          // rounded for the MMA (four chains), so O is normalised by the
+          // weights it was formed with
           const float mu = m_used == -INFINITY ? 0.f : m_used;
           uint32_t w[SC / 2];
-          float ls = 0.f;
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+          if (fast) {
 #pragma unroll
-          for (int c = 0; c < SC; c += 2) {
-            w[c >> 1] = pack2(sfu_exp2(sv[c] - mu), sfu_exp2(sv[c + 1] - mu), tag{});
-            ls += sum2(w[c >> 1], tag{});
+            for (int c = 0; c < SC; c += 2)
+              w[c >> 1] = pack2(sfu_exp2(fmaf(__uint_as_float(sr[c]), sl2, -mu)),
+                                sfu_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -mu)), tag{});
+          } else {
+#pragma unroll
+            for (int c = 0; c < SC; c += 2)
+              w[c >> 1] = pack2(sfu_exp2(__uint_as_float(sr[c]) - mu),
+                                sfu_exp2(__uint_as_float(sr[c + 1]) - mu), tag{});
           }
-          lsum += ls;
+#pragma unroll
+          for (int c = 0; c < SC / 2; ++c) ls[c & 3] += sum2(w[c], tag{});
+          lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
           tmem_st32(tPb + lane_base + (j & 1) * (SC / 2), w);
         }
         // zero V of keys no row sees (outside the union, stale or NaN slots)
         if (!(nbt == TB && key_t0 >= u_lo && key_t0 + SC <= u_hi)) {
           unsigned char *vb = ring + slot * STAGE + TB * BLOCK_BYTES;
-          for (int c = 32 * warp + lane; c < nbt * kBlockKeys; c += 128) {
+          for (int c = 32 * (warp & 3) + lane; c < nbt * kBlockKeys; c += 128) {
             const int k = key_t0 + c;
             if (k < u_lo || k >= u_hi) {
 #pragma unroll 1
@@ -1506,20 +1566,21 @@ __global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
   const int64_t slice_floats = (int64_t)NT8 * DS;
 
   if constexpr (TP) {
-    // O (tensor memory) -> the CTA's partial in shared memory (KG = 1): row
-    // 32 w + lane of softmax warp w, once every MMA has completed
-    if (warp < kTcConsumerWarps - 1) {
+    // O of each softmax group (tensor memory) -> the group's partial in
+    // shared memory (KG = 2): row 32 (w % 4) + lane of softmax warp w, once
+    // every MMA has completed
+    if (warp < kTpSoftmaxWarps) {
       const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8), 0));
       tc_fence_after();
-      const int r = 32 * warp + lane;
+      const int g = warp >> 2, r = 32 * (warp & 3) + lane;
       const bool keep = r < NT8;
-      const bool have = ntile > 0 && done;
-      const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-      float *dst = cp + (size_t)r * D;
+      const bool have = ntile > g && done;  // the group took at least one stage
+      const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+      float *dst = cp + ((size_t)g * NT8 + r) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
-        tmem_ld32(tmem_base + tp_o_col(D) + lane_base + c0, o);
+        tmem_ld32(tmem_base + tp_o_col(D) + g * D + lane_base + c0, o);
         tmem_wait_ld();
         if (keep) {
 #pragma unroll
@@ -1532,8 +1593,8 @@ __global__ void __launch_bounds__(TC || TP ? kTcThreads : kMaxThreads, 1)
         }
       }
       if (keep) {
-        mrow[r] = have ? m0 : -INFINITY;
-        lrow[r] = have ? l0 : 0.f;
+        mrow[g * NT8 + r] = have ? m0 : -INFINITY;
+        lrow[g * NT8 + r] = have ? l0 : 0.f;
       }
       if (!done && lane == 0) atomicOr(p.status, 0x1u);
     }

@@ -105,8 +105,8 @@ int plan_tiles(const int32_t *query_start, const int32_t *seq_lens, int S, int H
 }
 
 // Launch shape of a prefill tile.  At D = 128: 128 rows on the tensor
-// cores (path 5: Q, S, P and O in tensor memory, four softmax warps and one
-// MMA warp), as many 32 KiB ring stages as fit.  Otherwise 8 n-tiles of 8
+// cores (path 5: Q, S, P and O in tensor memory, two groups of four softmax
+// warps and one MMA warp), as many 32 KiB ring stages as fit.  Otherwise 8 n-tiles of 8
 // rows, as many stages as fit next to the Q tile; at D = 64 the rows sit on
 // the MMA's M side, one warp per 16 rows (path 4: each stage is read from
 // shared memory once per 16 rows); larger heads keep the keys on the M side,
@@ -120,13 +120,13 @@ int prefill_shape(int D, PrefillShape *sh) {
   if (D == 128) {
     sh->path = 5;
     sh->NT = kTpRows / 8;
-    sh->KG = 1;
+    sh->KG = 2;  // two softmax groups, merged like warp groups
     sh->NS = std::min(8, (kSmemLimit - smem_bytes_tp(0)) / (kStageBytes + 16));
     if (sh->NS < 2) return PD_EINVAL;
     sh->smem = smem_bytes_tp(sh->NS);
     sh->epi = epilogue_bytes_tp(sh->NS);
     if (epilogue_floats(D, sh->NT, sh->KG, 1, kMaxSegments) * 4 > sh->epi) return PD_EINVAL;
-    sh->threads = kTcThreads;
+    sh->threads = kTpThreads;
     return PD_OK;
   }
   sh->NT = PD_PREFILL_TILE_ROWS / 8;
@@ -285,7 +285,7 @@ PD_API int paged_prefill_attn(const pd_tensor *q, const pd_tensor *k_cache, cons
   }
 
   CUtensorMap tk, tv;
-  if ((rc = cache_tensor_map(k_cache, layout, &tk)) != PD_OK) return rc;
+  if ((rc = cache_tensor_map(k_cache, layout, &tk, sh.path == 5)) != PD_OK) return rc;
   if ((rc = cache_tensor_map(v_cache, layout, &tv)) != PD_OK) return rc;
 
   p.q = q->data;
