@@ -337,7 +337,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    // (broadcast from lane 0 so the compiler knows it is warp-uniform: the
+    // tensor-memory operands then stay in uniform registers)
+    tmem_base = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile uint32_t *>(tmem_slot), 0);
   }
 
 
@@ -510,41 +512,50 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
       const uint32_t idS = umma_idesc_f16(kTpRows, SC, BF16, 0, 0);
       const uint32_t idO = umma_idesc_f16(kTpRows, D, BF16, 0, 1);
       const uint32_t ring_u = smem_u32(ring);
-      bool ok = true;
-      for (int j = 0; j <= ntile; ++j) {
-        if (j < ntile) {
-          const int slot = j % NS;
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1));
-          // S buffer j & 1 was read by the softmax of stage j - 2
-          if (ok && j >= 2)
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait_bounded(smem_u32(tcb + 2 + (j & 1)), ((j - 2) >> 1) & 1));
-          if (!ok) break;
-          tc_fence_after();
-          // all SC keys of the stage at once (keys of blocks a short stage
-          // did not load give scores the softmax masks)
-          const uint32_t kst = ring_u + slot * STAGE;
+      // S of stage j into S buffer j & 1, once its stage has landed and (j >= 2)
+      // the softmax of stage j - 2 has read that buffer
+      auto issue_s = [&](int j) -> bool {
+        const int slot = j % NS;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1)))
+          return false;
+        if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 2 + (j & 1)),
+                                                                 ((j - 2) >> 1) & 1)))
+          return false;
+        tc_fence_after();
+        // all SC keys of the stage at once (keys of blocks a short stage did
+        // not load give scores the softmax masks)
+        const uint32_t kst = ring_u + slot * STAGE;
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks)
-            umma_f16_ts_warp(tS + (j & 1) * SC, tQ + 8 * ks,
-                             umma_desc_sw128(kst + (ks >> 2) * (TB * BLOCK_BYTES / NBOX) + (ks & 3) * 32,
-                                             16, 1024),
-                             idS, ks > 0 ? 1u : 0u);
-          umma_commit_warp(smem_u32(tcb + (j & 1)));  // S of stage j is ready
-        }
-        if (j >= 1) {
-          const int jj = j - 1, slot = jj % NS;
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 4 + (jj & 1)), (jj >> 1) & 1));
-          if (!ok) break;
-          tc_fence_after();
-          const int nbt = min(TB, my_nb - jj * TB);
-          const uint64_t dv = umma_desc_sw128(ring_u + slot * STAGE + TB * BLOCK_BYTES, 2048, 1024);
-          for (int b = 0; b < nbt; ++b)
-            umma_f16_ts_warp(tO + (jj & 1) * D, tPb + (jj & 1) * (SC / 2) + 8 * b,
-                             dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (jj > 1 || b > 0) ? 1u : 0u);
-          umma_commit_warp(smem_u32(empty + slot));        // the stage may be refilled
-          umma_commit_warp(smem_u32(tcb + 6 + (jj & 1)));  // P buffer jj & 1 is free, its O current
-        }
+        for (int ks = 0; ks < KS; ++ks)
+          umma_f16_ts_warp(tS + (j & 1) * SC, tQ + 8 * ks,
+                           umma_desc_sw128(kst + (ks >> 2) * (TB * BLOCK_BYTES / NBOX) + (ks & 3) * 32,
+                                           16, 1024),
+                           idS, ks > 0 ? 1u : 0u);
+        umma_commit_warp(smem_u32(tcb + (j & 1)));  // S of stage j is ready
+        return true;
+      };
+      // Order: S of stages 0 and 1, then per stage k: S of stage k + 2 (as
+      // soon as the softmax of k has read its S buffer), then PV of stage k
+      // (once its P is written).  S of the next stage of each softmax group
+      // is so in flight while the group is still on its current stage, and
+      // neither group waits for the other.
+      bool ok = true;
+      for (int j = 0; j < 2 && j < ntile && ok; ++j) ok = issue_s(j);
+      for (int k = 0; k < ntile && ok; ++k) {
+        if (k + 2 < ntile && !(ok = issue_s(k + 2))) break;
+        const int slot = k % NS;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 4 + (k & 1)), (k >> 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        const int nbt = min(TB, my_nb - k * TB);
+        const uint64_t dv = umma_desc_sw128(ring_u + slot * STAGE + TB * BLOCK_BYTES, 2048, 1024);
+#pragma unroll
+        for (int b = 0; b < TB; ++b)
+          if (b < nbt)
+            umma_f16_ts_warp(tO + (k & 1) * D, tPb + (k & 1) * (SC / 2) + 8 * b,
+                             dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (k > 1 || b > 0) ? 1u : 0u);
+        umma_commit_warp(smem_u32(empty + slot));       // the stage may be refilled
+        umma_commit_warp(smem_u32(tcb + 6 + (k & 1)));  // P buffer k & 1 is free, its O current
       }
       if (!ok && lane == 0) {
         flags[0] = 1;
