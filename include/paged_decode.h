@@ -314,13 +314,14 @@ PD_API int paged_rope_cache_write(const pd_tensor *q, const pd_tensor *k, const 
  * request's query tokens are packed token-major into rows (token i, q head
  * h*G + j -> row i*G + j), cut into tiles of PD_PREFILL_TILE_ROWS rows
  * (PD_PREFILL_TILE_ROWS_D128 at head size 128, whose tiles run on the
- * 5th-generation tensor cores with one row per tensor-memory lane), and
+ * 5th-generation tensor cores as two halves of one row per tensor-memory
+ * lane), and
  * a tile whose keys (from its window start rounded down to 16 keys, to the
  * last key its last token sees) exceed the mean load per resident CTA is cut
  * into segments, merged in the kernel by the last-arriving segment.  Items
  * are ordered heaviest first.  Each item runs once per kv head. */
 #define PD_PREFILL_TILE_ROWS 64
-#define PD_PREFILL_TILE_ROWS_D128 128
+#define PD_PREFILL_TILE_ROWS_D128 256
 #define PD_PREFILL_MAX_SEGMENTS 32
 
 /* One work item: a segment of the keys of one tile of one request. */

@@ -122,12 +122,12 @@ inline int64_t epilogue_bytes_tc(int D, int NS) {
   return (int64_t)NS * kStageBytes + (int64_t)kTcRows * D * 2 + 2LL * tc_p_tile_bytes(D);
 }
 
-// Tensor-memory prefill path (TP, head size 128): 128 packed rows per tile,
-// one per tensor-memory lane; two groups of four softmax warps take the
-// even and the odd stages, each with its own O; one warp issues the MMAs.
-// Columns: Q (two 16-bit elements per column), two S buffers of a stage's
-// keys (fp32), two P buffers (16-bit pairs), two O (fp32), rounded up to a
-// power of two.
+// Tensor-memory prefill path (TP, head size 128): two tiles of 128 packed
+// rows share each K/V stage, one row of a tile per tensor-memory lane, each
+// tile with its own four softmax warps; one warp issues the MMAs.  Columns:
+// the first tile's Q (two 16-bit elements per column; the second tile's Q
+// is in shared memory), one S buffer per tile (fp32), one P buffer per tile
+// (16-bit pairs), one O per tile (fp32), rounded up to a power of two.
 constexpr int kTpRows = 128;
 constexpr int kTpSoftmaxWarps = 8;
 constexpr int kTpConsumerWarps = kTpSoftmaxWarps + 1;
@@ -139,13 +139,16 @@ constexpr int tp_tmem_cols(int D) {
   return tp_o_col(D) + 2 * D <= 128 ? 128 : tp_o_col(D) + 2 * D <= 256 ? 256 : 512;
 }
 static_assert(tp_o_col(128) + 2 * 128 <= 512, "tensor memory of a prefill tile");
-// Dynamic shared memory of a tensor-memory prefill launch: ring + barriers
-// + flags + staged page ids + tensor-memory address (Q and P live in tensor
-// memory); its epilogue region is the dead ring.
-inline int smem_bytes_tp(int NS) {
-  return kSmemAlign + NS * kStageBytes + 2 * NS * 8 + kTcBarriers * 8 + 16 + 4 * kBlockIds + 16;
+// Dynamic shared memory of a tensor-memory prefill launch: ring + the second
+// tile's Q + barriers + flags + staged page ids + tensor-memory address;
+// its epilogue region is the dead ring and Q tile.
+inline int smem_bytes_tp(int D, int NS) {
+  return kSmemAlign + NS * kStageBytes + kTpRows * D * 2 + 2 * NS * 8 + kTcBarriers * 8 + 16 +
+         4 * kBlockIds + 16;
 }
-inline int64_t epilogue_bytes_tp(int NS) { return (int64_t)NS * kStageBytes; }
+inline int64_t epilogue_bytes_tp(int D, int NS) {
+  return (int64_t)NS * kStageBytes + (int64_t)kTpRows * D * 2;
+}
 
 // Floats the epilogue needs: combine phase and final-merge phase.
 inline int64_t epilogue_floats(int D, int NT, int KG, int CS, int ncl_max) {

@@ -145,7 +145,8 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
   const int NS = p.NS, NT = p.NT, KG = p.KG,
             NC = TC ? kTcConsumerWarps : TP ? kTpConsumerWarps : RM ? (NT >> 1) * KG : NT * KG;
   const int NT8 = NT * 8;
-  const int NTQ = TC ? kTcRows / 8 : TP ? 0 : NT;  // 8-row groups of the Q tile (TP: none)
+  // 8-row groups of the Q tile in shared memory (TP: the second tile's)
+  const int NTQ = TC ? kTcRows / 8 : TP ? kTpRows / 8 : NT;
   unsigned char *ring = smem;
   unsigned char *qs = ring + NS * STAGE;
   unsigned char *pts = qs + NTQ * D * 16;  // TC: two P tiles
@@ -455,32 +456,35 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
   } else {
     if constexpr (TP) {
     // ================= tensor-memory prefill consumers ====================
-    // The tile's 128 packed rows are the M = 128 side of every MMA, row r in
-    // tensor-memory lane r.  Softmax warp w (w < 8) owns lanes 32 (w % 4) ..
-    // 32 (w % 4) + 31, one row per thread, and the stages of parity w / 4:
-    // two groups of four warps, each an independent online softmax over its
-    // stages with its own O in tensor memory (merged in the epilogue like
-    // warp groups).  Warp 8 issues the MMAs from one thread:
-    //   S[128 x stage keys] = Q . K^T  (A = Q from tensor memory; B = the
-    //                                   stage's K, landed box-major, K-major;
-    //                                   N = 64, one MMA per 16 dims)
-    //   O[128 x D]         += P . V    (A = P from tensor memory; B = one V
-    //                                   block, MN-major as the copies land)
-    // S, P and O of stage j are the buffers of its parity: the MMAs of stage
-    // j + 1 run during the softmax of stage j, and the two groups' softmaxes
-    // overlap.  O is rescaled in tensor memory only when a row's max grows
-    // more than 8 past the reference its P values use (so P <= 2^8), the
-    // online-softmax update in exp2 form.
+    // Two tiles of 128 packed rows share every K/V stage: tile X (X = 0, 1)
+    // is rows 128 X .. 128 X + 127, one row per tensor-memory lane, and its
+    // own four softmax warps 4 X .. 4 X + 3 (warp w owns lanes 32 (w % 4) ..
+    // 32 (w % 4) + 31, one row per thread).  Warp 8 issues the MMAs:
+    //   S_X[128 x stage keys] = Q_X . K^T  (A = Q_0 from tensor memory, Q_1
+    //                                     from shared memory; B = the stage's
+    //                                     K, landed box-major, K-major; N = 64,
+    //                                     one MMA per 16 dims)
+    //   O_X[128 x D]         += P_X . V    (A = P_X from tensor memory; B = one
+    //                                     V block, MN-major as the copies land)
+    // S of stage j + 1 is computed while the softmax of stage j runs (its S
+    // buffer is free once the softmax has read it); P of stage j + 1 is
+    // written once the PV MMAs of stage j are done.  O_X is rescaled in
+    // tensor memory only when a row's max grows more than 8 past the
+    // reference its P values use (so P <= 2^8), the online-softmax update in
+    // exp2 form.  Two tiles per stage halve the K/V copies per row: the
+    // per-SM copy rate bounds a 128-row tile.
     static_assert(!TP || SC == 64, "a stage holds 64 keys at head size 128");
-    const uint32_t tQ = tmem_base, tS = tmem_base + tp_s_col(D), tPb = tmem_base + tp_p_col(D),
-                   tO = tmem_base + tp_o_col(D);
-    const int r_tp = 32 * (warp & 3) + lane, rr_tp = rr0 + r_tp;  // this thread's row
-    const int g_tp = warp >> 2;                                   // softmax group: stage parity
+    const int X = (warp >> 2) & 1;             // this softmax warp's tile
+    const int r_tp = 32 * (warp & 3) + lane;   // its row in the tile
+    const int rr_tp = rr0 + kTpRows * X + r_tp;
     const bool live = warp < kTpSoftmaxWarps && rr_tp < rr1v;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    if (warp < 4) {
-      // Q row -> tensor memory, 16-bit pairs in memory order (zeros for rows
-      // past the request's tokens)
+    const uint32_t tQ = tmem_base, tS = tmem_base + tp_s_col(D), tPb = tmem_base + tp_p_col(D),
+                   tO = tmem_base + tp_o_col(D);
+    if (warp < kTpSoftmaxWarps) {
+      // Q rows: tile 0 into tensor memory (16-bit pairs in memory order),
+      // tile 1 into the 128-byte-swizzled K-major tile in shared memory
+      // ([64-dim box][128 rows][128 B]); zeros for rows past the requests
       const uint4 *src = nullptr;
       if (live) {
         const int i = token_of(rr_tp), jq = rr_tp - i * p.G;
@@ -488,74 +492,93 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
                                               (int64_t)(q0 + i) * p.q_s0 +
                                               (int64_t)(h * p.G + jq) * p.q_s1);
       }
+      if (X == 0) {
 #pragma unroll
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
-        uint32_t w[32];
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t w[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 v = live ? __ldg(src + c0 / 4 + u) : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * u] = v.x;
-          w[4 * u + 1] = v.y;
-          w[4 * u + 2] = v.z;
-          w[4 * u + 3] = v.w;
+          for (int u = 0; u < 8; ++u) {
+            const uint4 v = live ? __ldg(src + c0 / 4 + u) : make_uint4(0u, 0u, 0u, 0u);
+            w[4 * u] = v.x;
+            w[4 * u + 1] = v.y;
+            w[4 * u + 2] = v.z;
+            w[4 * u + 3] = v.w;
+          }
+          tmem_st32(tQ + lane_base + c0, w);
         }
-        tmem_st32(tQ + lane_base + c0, w);
+        tmem_wait_st();
+        tc_fence_before();
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(qs + (c >> 3) * (kTpRows * 128) + r_tp * 128 +
+                                     (((c & 7) ^ (r_tp & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();  // the tensor core reads the tile
       }
-      tmem_wait_st();
-      tc_fence_before();
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");  // Q is in tensor memory
+    asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");  // both Q tiles are in place
     if (warp == kTpConsumerWarps - 1) {
       // ---- MMA issue: the whole warp runs the loop (every operand is
       // warp-uniform), one elected lane issues each MMA and commit ----
       tc_fence_after();
       const uint32_t idS = umma_idesc_f16(kTpRows, SC, BF16, 0, 0);
       const uint32_t idO = umma_idesc_f16(kTpRows, D, BF16, 0, 1);
-      const uint32_t ring_u = smem_u32(ring);
-      // S of stage j into S buffer j & 1, once its stage has landed and (j >= 2)
-      // the softmax of stage j - 2 has read that buffer
+      const uint32_t ring_u = smem_u32(ring), qb_u = smem_u32(qs);
+      // S of both tiles for stage j, once its stage has landed and (j >= 1)
+      // each tile's softmax has read its S buffer
       auto issue_s = [&](int j) -> bool {
         const int slot = j % NS;
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1)))
           return false;
-        if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 2 + (j & 1)),
-                                                                 ((j - 2) >> 1) & 1)))
-          return false;
-        tc_fence_after();
-        // all SC keys of the stage at once (keys of blocks a short stage did
-        // not load give scores the softmax masks)
         const uint32_t kst = ring_u + slot * STAGE;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
-          umma_f16_ts_warp(tS + (j & 1) * SC, tQ + 8 * ks,
-                           umma_desc_sw128(kst + (ks >> 2) * (TB * BLOCK_BYTES / NBOX) + (ks & 3) * 32,
-                                           16, 1024),
-                           idS, ks > 0 ? 1u : 0u);
-        umma_commit_warp(smem_u32(tcb + (j & 1)));  // S of stage j is ready
+        for (int x = 0; x < 2; ++x) {
+          if (j >= 1 &&
+              !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 2 + x), (j - 1) & 1)))
+            return false;
+          tc_fence_after();
+          // all SC keys of the stage at once (keys of blocks a short stage
+          // did not load give scores the softmax masks)
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            const uint64_t bk =
+                umma_desc_sw128(kst + (ks >> 2) * (TB * BLOCK_BYTES / NBOX) + (ks & 3) * 32, 16, 1024);
+            if (x == 0)
+              umma_f16_ts_warp(tS, tQ + 8 * ks, bk, idS, ks > 0 ? 1u : 0u);
+            else
+              umma_f16_warp(tS + SC,
+                            umma_desc_sw128(qb_u + (ks >> 2) * (kTpRows * 128) + (ks & 3) * 32, 16, 1024),
+                            bk, idS, ks > 0 ? 1u : 0u);
+          }
+          umma_commit_warp(smem_u32(tcb + x));  // S_x of stage j is ready
+        }
         return true;
       };
-      // Order: S of stages 0 and 1, then per stage k: S of stage k + 2 (as
-      // soon as the softmax of k has read its S buffer), then PV of stage k
-      // (once its P is written).  S of the next stage of each softmax group
-      // is so in flight while the group is still on its current stage, and
-      // neither group waits for the other.
-      bool ok = true;
-      for (int j = 0; j < 2 && j < ntile && ok; ++j) ok = issue_s(j);
+      // Order: S of stage 0, then per stage k: S of stage k + 1 (as soon as
+      // the softmaxes have read the S of stage k), PV of stage k (as soon as
+      // its P is written), tile by tile.
+      bool ok = ntile == 0 || issue_s(0);
       for (int k = 0; k < ntile && ok; ++k) {
-        if (k + 2 < ntile && !(ok = issue_s(k + 2))) break;
+        if (k + 1 < ntile && !(ok = issue_s(k + 1))) break;
         const int slot = k % NS;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 4 + (k & 1)), (k >> 1) & 1));
-        if (!ok) break;
-        tc_fence_after();
         const int nbt = min(TB, my_nb - k * TB);
         const uint64_t dv = umma_desc_sw128(ring_u + slot * STAGE + TB * BLOCK_BYTES, 2048, 1024);
 #pragma unroll
-        for (int b = 0; b < TB; ++b)
-          if (b < nbt)
-            umma_f16_ts_warp(tO + (k & 1) * D, tPb + (k & 1) * (SC / 2) + 8 * b,
-                             dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (k > 1 || b > 0) ? 1u : 0u);
-        umma_commit_warp(smem_u32(empty + slot));       // the stage may be refilled
-        umma_commit_warp(smem_u32(tcb + 6 + (k & 1)));  // P buffer k & 1 is free, its O current
+        for (int x = 0; x < 2; ++x) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 4 + x), k & 1));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int b = 0; b < TB; ++b)
+            if (b < nbt)
+              umma_f16_ts_warp(tO + x * D, tPb + x * (SC / 2) + 8 * b,
+                               dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (k > 0 || b > 0) ? 1u : 0u);
+          umma_commit_warp(smem_u32(tcb + 6 + x));  // P_x is free, O_x current
+        }
+        if (!ok) break;
+        umma_commit_warp(smem_u32(empty + slot));  // the stage may be refilled
       }
       if (!ok && lane == 0) {
         flags[0] = 1;
@@ -563,16 +586,16 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
       }
       umma_commit_warp(smem_u32(tcb + 8));  // every MMA issued above has completed
     } else {
-      // ---- softmax: one row per thread, the stages of this group's parity ----
+      // ---- softmax: one row per thread, every stage, this tile ----
       int lo = 0, hi = 0;
       if (live) {
         hi = max(L - ml + token_of(rr_tp) + 1, 0);
         lo = p.window ? max(0, hi - p.window) : 0;
       }
-      const uint32_t tOg = tO + g_tp * D;
+      const uint32_t tSx = tS + X * SC, tPx = tPb + X * (SC / 2), tOx = tO + X * D;
       float m_used = -INFINITY, lsum = 0.f;
-      for (int j = g_tp; j < ntile; j += 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + (j & 1)), (j >> 1) & 1))) {
+      for (int j = 0; j < ntile; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + X), j & 1))) {
           if (lane == 0) {
             flags[0] = 1;
             atomicOr(p.status, 0x1u);
@@ -583,8 +606,8 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         uint32_t sr[SC];  // the row's scores of the stage (fp32 bits)
         {
           uint32_t x0[32], x1[32];
-          tmem_ld32(tS + lane_base + (j & 1) * SC, x0);
-          tmem_ld32(tS + lane_base + (j & 1) * SC + 32, x1);
+          tmem_ld32(tSx + lane_base, x0);
+          tmem_ld32(tSx + lane_base + 32, x1);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -594,12 +617,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(tcb + 2 + (j & 1)));  // S buffer read
+        if (lane == 0) mbar_arrive(smem_u32(tcb + 2 + X));  // S buffer read
         const int nbt = min(TB, my_nb - j * TB);
         const int key_t0 = (my_b0 + j * TB) * kBlockKeys;
         const int slot = j % NS;
-        // every row of the tile sees every key of the stage: no mask, and the
-        // scale is applied inside the exponent (rows past the request's
+        // every row of the CTA sees every key of the stage: no mask, and the
+        // scale is applied inside the exponent (rows past the requests'
         // tokens have Q = 0, finite scores, and are never stored)
         const bool fast = nbt == TB && key_t0 >= v_lo && key_t0 + SC <= v_hi;
         const float sl2 = p.scale_log2;
@@ -647,21 +670,21 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         }
         const float m_new = fmaxf(m_used, mx);
         const bool need = m_used != -INFINITY && m_new > m_used + 8.f;
-        // the PV MMAs of this group's previous stage (j - 2) have completed:
-        // its P buffer is free and its O current
-        bool ok = j < 2 || __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 6 + (j & 1)),
-                                                                     ((j - 2) >> 1) & 1));
+        // the PV MMAs of the previous stage have completed: P_X is free and
+        // O_X current
+        bool ok = j < 1 || __all_sync(0xffffffffu,
+                                      mbar_wait_bounded(smem_u32(tcb + 6 + X), (j - 1) & 1));
         tc_fence_after();
         if (ok && __any_sync(0xffffffffu, need)) {
           const float alpha = need ? sfu_exp2(m_used - m_new) : 1.f;
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
-            tmem_ld32(tOg + lane_base + c0, o);
+            tmem_ld32(tOx + lane_base + c0, o);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tOg + lane_base + c0, o);
+            tmem_st32(tOx + lane_base + c0, o);
           }
           tmem_wait_st();
           tc_fence_before();
@@ -699,10 +722,11 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
 #pragma unroll
           for (int c = 0; c < SC / 2; ++c) ls[c & 3] += sum2(w[c], tag{});
           lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-          tmem_st32(tPb + lane_base + (j & 1) * (SC / 2), w);
+          tmem_st32(tPx + lane_base, w);
         }
-        // zero V of keys no row sees (outside the union, stale or NaN slots)
-        if (!(nbt == TB && key_t0 >= u_lo && key_t0 + SC <= u_hi)) {
+        // zero V of keys no row sees (outside the union, stale or NaN slots);
+        // tile 0 does it, and both tiles' PV MMAs are issued after its P
+        if (X == 0 && !(nbt == TB && key_t0 >= u_lo && key_t0 + SC <= u_hi)) {
           unsigned char *vb = ring + slot * STAGE + TB * BLOCK_BYTES;
           for (int c = 32 * (warp & 3) + lane; c < nbt * kBlockKeys; c += 128) {
             const int k = key_t0 + c;
@@ -718,7 +742,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         fence_proxy_async_smem();  // the zeroed V reaches the tensor core
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(tcb + 4 + (j & 1)));  // P of stage j written
+        if (lane == 0) mbar_arrive(smem_u32(tcb + 4 + X));  // P of stage j written
       }
       m0 = m_used;
       l0 = lsum;
@@ -1577,17 +1601,17 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
   const int64_t slice_floats = (int64_t)NT8 * DS;
 
   if constexpr (TP) {
-    // O of each softmax group (tensor memory) -> the group's partial in
-    // shared memory (KG = 2): row 32 (w % 4) + lane of softmax warp w, once
-    // every MMA has completed
+    // O of each tile (tensor memory) -> the CTA's partial in shared memory
+    // (KG = 1): row 128 X + 32 (w % 4) + lane of softmax warp w of tile X,
+    // once every MMA has completed
     if (warp < kTpSoftmaxWarps) {
       const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8), 0));
       tc_fence_after();
-      const int g = warp >> 2, r = 32 * (warp & 3) + lane;
+      const int g = warp >> 2, r = kTpRows * g + 32 * (warp & 3) + lane;
       const bool keep = r < NT8;
-      const bool have = ntile > g && done;  // the group took at least one stage
+      const bool have = ntile > 0 && done;
       const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-      float *dst = cp + ((size_t)g * NT8 + r) * D;
+      float *dst = cp + (size_t)r * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
@@ -1604,8 +1628,8 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         }
       }
       if (keep) {
-        mrow[g * NT8 + r] = have ? m0 : -INFINITY;
-        lrow[g * NT8 + r] = have ? l0 : 0.f;
+        mrow[r] = have ? m0 : -INFINITY;
+        lrow[r] = have ? l0 : 0.f;
       }
       if (!done && lane == 0) atomicOr(p.status, 0x1u);
     }

@@ -21,10 +21,10 @@
 namespace pd {
 namespace {
 
-// packed rows of a tile: 128 (one per tensor-memory lane) where the
-// tensor-memory consumer serves the head size, else 64
+// packed rows of a tile: 256 (two tiles of one row per tensor-memory lane)
+// where the tensor-memory consumer serves the head size, else 64
 int tile_rows_for(int D) { return D == 128 ? PD_PREFILL_TILE_ROWS_D128 : PD_PREFILL_TILE_ROWS; }
-static_assert(PD_PREFILL_TILE_ROWS_D128 == kTpRows, "a tensor-memory prefill tile");
+static_assert(PD_PREFILL_TILE_ROWS_D128 == 2 * kTpRows, "two tensor-memory tiles per CTA");
 bool head_size_ok(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 constexpr int kMaxSegments = PD_PREFILL_MAX_SEGMENTS;
 // a segment reads at least this many 16-key blocks (two ring stages at
@@ -104,9 +104,10 @@ int plan_tiles(const int32_t *query_start, const int32_t *seq_lens, int S, int H
   return PD_OK;
 }
 
-// Launch shape of a prefill tile.  At D = 128: 128 rows on the tensor
-// cores (path 5: Q, S, P and O in tensor memory, two groups of four softmax
-// warps and one MMA warp), as many 32 KiB ring stages as fit.  Otherwise 8 n-tiles of 8
+// Launch shape of a prefill tile.  At D = 128: 256 rows on the tensor
+// cores (path 5: two tiles of 128 rows sharing each K/V stage, S, P and O
+// in tensor memory, four softmax warps per tile and one MMA warp), as many
+// 32 KiB ring stages as fit next to the second tile's Q.  Otherwise 8 n-tiles of 8
 // rows, as many stages as fit next to the Q tile; at D = 64 the rows sit on
 // the MMA's M side, one warp per 16 rows (path 4: each stage is read from
 // shared memory once per 16 rows); larger heads keep the keys on the M side,
@@ -119,12 +120,12 @@ struct PrefillShape {
 int prefill_shape(int D, PrefillShape *sh) {
   if (D == 128) {
     sh->path = 5;
-    sh->NT = kTpRows / 8;
-    sh->KG = 2;  // two softmax groups, merged like warp groups
-    sh->NS = std::min(8, (kSmemLimit - smem_bytes_tp(0)) / (kStageBytes + 16));
+    sh->NT = 2 * kTpRows / 8;
+    sh->KG = 1;
+    sh->NS = std::min(8, (kSmemLimit - smem_bytes_tp(D, 0)) / (kStageBytes + 16));
     if (sh->NS < 2) return PD_EINVAL;
-    sh->smem = smem_bytes_tp(sh->NS);
-    sh->epi = epilogue_bytes_tp(sh->NS);
+    sh->smem = smem_bytes_tp(D, sh->NS);
+    sh->epi = epilogue_bytes_tp(D, sh->NS);
     if (epilogue_floats(D, sh->NT, sh->KG, 1, kMaxSegments) * 4 > sh->epi) return PD_EINVAL;
     sh->threads = kTpThreads;
     return PD_OK;

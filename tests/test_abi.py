@@ -394,7 +394,7 @@ def test_prefill_argument_checks_on_host(lib):
     assert call(info=bad) == -1
     # a plan made for another head size (64-row tiles) does not fit head size 128
     items64, info64 = pd.paged_prefill_plan(c.query_start_host, c.seq_lens_host, 8, 2, 64, 0, 152)
-    assert info64.tile_rows == 64 and info.tile_rows == 128
+    assert info64.tile_rows == 64 and info.tile_rows == 256
     assert call(work=items64, info=info64) == -1
     if not torch.cuda.is_available():
         assert call() == -8                                  # a valid call needs the GPU

@@ -84,15 +84,15 @@ def test_head_sizes_layouts_pages(D, Hq, Hkv, P, layout):
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 1), (16, 16), (12, 4)])
 def test_tensor_memory_tiles_d128(dtype, Hq, Hkv):
-    # head size 128 runs 128-row tiles on the tensor cores: G = 4, 8, 1 and 3
-    # (a tile then ends inside a token), ragged query lengths, a request with
-    # no context and one shorter than a tile; values shifted so the outputs
-    # are O(1)
+    # head size 128 runs 256-row tiles (two halves of 128) on the tensor
+    # cores: G = 4, 8, 1 and 3 (a tile then ends inside a token), ragged query
+    # lengths, a request with no context and one shorter than a half; values
+    # shifted so the outputs are O(1)
     c = W.make_prefill_case(f"pf_tp_{Hq}_{Hkv}", seed=11 + Hq + Hkv, q_lens=[131, 7, 300, 64],
                             contexts=[500, 33, 0, 1999], dtype=dtype, head_size=128,
                             num_q_heads=Hq, num_kv_heads=Hkv, page_size=16, v_mean=1.0)
     _, info = _run(c)
-    assert info.tile_rows == 128
+    assert info.tile_rows == 256
 
 
 @pytest.mark.parametrize("window", [1, 100, 129])

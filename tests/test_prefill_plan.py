@@ -1,7 +1,7 @@
 """The prefill work-list planner on the CPU (host code of the C ABI, no
 device): the rules of plan_prefill and prefill_target_workgroups on the
 vllm.v1.attention.ops.rocm_rdna_hip page, restated for this kernel (64
-packed rows per tile, 128 at head size 128; 16-key blocks, one CTA per SM):
+packed rows per tile, 256 at head size 128; 16-key blocks, one CTA per SM):
 
 * a request's tiles cover its q_len x G packed rows, token-major;
 * a tile's keys run from its window start, rounded down to a 16-key block,
@@ -24,7 +24,7 @@ FLOOR, MAX_SEG, BLOCK = 8, 32, 16
 
 
 def rows_for(D):
-    return 128 if D == 128 else 64
+    return 256 if D == 128 else 64
 
 
 def _plan(q_lens, ctx, Hq=32, Hkv=8, window=0, sms=152, D=64):
@@ -61,18 +61,21 @@ def test_hand_worked_single_request():
     assert np.all(split[:, 3] == 2)
 
 
-def test_hand_worked_single_request_128_row_tiles():
-    # the same request at head size 128: 16 tiles of 32 tokens, tile t sees
-    # 32 (t + 1) keys = 2 (t + 1) blocks; 272 blocks x 8 / 152 = 14.3 per
-    # CTA; tiles of 16 .. 28 blocks split in two, of 30 and 32 in three
-    # (min(ceil(30 / 14.3), 30 // 8) = 3); 7 + 7 x 2 + 2 x 3 = 27 items.
-    # Heaviest per segment first: the 28-block tile's halves (14), then the
-    # unsplit 14-block tile
+def test_hand_worked_single_request_256_row_tiles():
+    # the same request at head size 128: 8 tiles of 64 tokens, tile t sees
+    # 64 (t + 1) keys = 4 (t + 1) blocks; 144 blocks x 8 / 152 = 7.6 per CTA,
+    # below the floor of 8; a tile of b > 8 blocks is cut into
+    # min(ceil(b / 8), b // 8) segments: 12 -> 1, 16 -> 2, 20 -> 2, 24 -> 3,
+    # 28 -> 3, 32 -> 4; 3 + 14 = 17 items.  Heaviest per segment first: the
+    # unsplit 12-block tile, the 20-block tile's halves (10), the 28-block
+    # tile's thirds (9.3), then the 8-block segments in tile order
     items, info, _, _ = _plan([512], [0], D=128)
-    assert info.tile_rows == 128 and info.total_blocks == 272
-    assert info.num_items == 27 and info.num_split_tiles == 9 and info.num_slots == 20
-    assert [tuple(r) for r in items[:3, :4]] == [(0, 13, 0, 2), (0, 13, 1, 2), (0, 6, 0, 1)]
-    assert sorted(items[items[:, 3] == 3][:, 1].tolist()) == [14] * 3 + [15] * 3
+    assert info.tile_rows == 256 and info.total_blocks == 144
+    assert info.load_blocks == pytest.approx(8)
+    assert info.num_items == 17 and info.num_split_tiles == 5 and info.num_slots == 14
+    assert [tuple(r) for r in items[:6, :4]] == [(0, 2, 0, 1), (0, 4, 0, 2), (0, 4, 1, 2),
+                                                 (0, 6, 0, 3), (0, 6, 1, 3), (0, 6, 2, 3)]
+    assert [int(t) for t in items[6:, 1]] == [7] * 4 + [5] * 3 + [3] * 2 + [1, 0]
 
 
 @pytest.mark.parametrize("D", [64, 128])
