@@ -124,14 +124,16 @@ inline int64_t epilogue_bytes_tc(int D, int NS) {
 
 // Tensor-memory prefill path (TP, head size 128): two tiles of 128 packed
 // rows share each K/V stage, one row of a tile per tensor-memory lane, each
-// tile with its own four softmax warps; one warp issues the MMAs.  Columns:
+// tile with its own four softmax warps; one warp issues the S MMAs of both
+// tiles, one warp per tile the PV MMAs.  Columns:
 // the first tile's Q (two 16-bit elements per column; the second tile's Q
 // is in shared memory), one S buffer per tile (fp32), one P buffer per tile
 // (16-bit pairs), one O per tile (fp32), rounded up to a power of two.
 constexpr int kTpRows = 128;
 constexpr int kTpSoftmaxWarps = 8;
-constexpr int kTpConsumerWarps = kTpSoftmaxWarps + 1;
-constexpr int kTpThreads = 32 * (kTpConsumerWarps + 1);
+constexpr int kTpConsumerWarps = kTpSoftmaxWarps + 1;  // + the warp that issues S
+// warps: softmax 0..7, S issue 8, producer 9, PV issue 10 (tile 0) and 11
+constexpr int kTpThreads = 32 * (kTpConsumerWarps + 3);
 constexpr int tp_s_col(int D) { return D / 2; }
 constexpr int tp_p_col(int D) { return D / 2 + 2 * tc_stage_keys(D); }
 constexpr int tp_o_col(int D) { return D / 2 + 3 * tc_stage_keys(D); }

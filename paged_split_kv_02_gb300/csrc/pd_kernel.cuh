@@ -181,12 +181,14 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
   if (warp == 0) {
     if (lane < NS) {
       mbar_init(smem_u32(full + lane), 1);
-      // (TC, TP: freed by the PV MMAs' commit; RM: by its NT / 2 warps)
-      mbar_init(smem_u32(empty + lane), TC || TP ? 1 : RM ? NT >> 1 : NT);
+      // (TC: freed by the PV MMAs' commit; TP: by both tiles' PV commits;
+      // RM: by its NT / 2 warps)
+      mbar_init(smem_u32(empty + lane), TC ? 1 : TP ? 2 : RM ? NT >> 1 : NT);
     }
     if constexpr (TC || TP) {
+      // (TP: every MMA done = the S warp's and both PV warps' last commits)
       if (lane < kTcBarriers)
-        mbar_init(smem_u32(tcb + lane), (lane >= 2 && lane <= 5) ? 4 : 1);
+        mbar_init(smem_u32(tcb + lane), (lane >= 2 && lane <= 5) ? 4 : (TP && lane == 8) ? 3 : 1);
     }
     if (lane == 31) {
       mbar_init(smem_u32(mbar_merge), 1);
@@ -459,7 +461,8 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     // Two tiles of 128 packed rows share every K/V stage: tile X (X = 0, 1)
     // is rows 128 X .. 128 X + 127, one row per tensor-memory lane, and its
     // own four softmax warps 4 X .. 4 X + 3 (warp w owns lanes 32 (w % 4) ..
-    // 32 (w % 4) + 31, one row per thread).  Warp 8 issues the MMAs:
+    // 32 (w % 4) + 31, one row per thread).  Warp 8 issues the S MMAs, warp
+    // 10 + X the PV MMAs of tile X, each as soon as its inputs are ready:
     //   S_X[128 x stage keys] = Q_X . K^T  (A = Q_0 from tensor memory, Q_1
     //                                     from shared memory; B = the stage's
     //                                     K, landed box-major, K-major; N = 64,
@@ -518,13 +521,13 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         fence_proxy_async_smem();  // the tensor core reads the tile
       }
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");  // both Q tiles are in place
+    // both Q tiles are in place (softmax warps and the S warp)
+    if (warp < kTpConsumerWarps) asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
     if (warp == kTpConsumerWarps - 1) {
-      // ---- MMA issue: the whole warp runs the loop (every operand is
+      // ---- S issue: the whole warp runs the loop (every operand is
       // warp-uniform), one elected lane issues each MMA and commit ----
       tc_fence_after();
       const uint32_t idS = umma_idesc_f16(kTpRows, SC, BF16, 0, 0);
-      const uint32_t idO = umma_idesc_f16(kTpRows, D, BF16, 0, 1);
       const uint32_t ring_u = smem_u32(ring), qb_u = smem_u32(qs);
       // S of both tiles for stage j, once its stage has landed and (j >= 1)
       // each tile's softmax has read its S buffer
@@ -556,35 +559,43 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         }
         return true;
       };
-      // Order: S of stage 0, then per stage k: S of stage k + 1 (as soon as
-      // the softmaxes have read the S of stage k), PV of stage k (as soon as
-      // its P is written), tile by tile.
+      // S of stage 0, then of each next stage as soon as both softmaxes have
+      // read the S of the stage before (the PV MMAs are the PV warps')
       bool ok = ntile == 0 || issue_s(0);
-      for (int k = 0; k < ntile && ok; ++k) {
-        if (k + 1 < ntile && !(ok = issue_s(k + 1))) break;
+      for (int k = 1; k < ntile && ok; ++k) ok = issue_s(k);
+      if (!ok && lane == 0) {
+        flags[0] = 1;
+        atomicOr(p.status, 0x1u);
+      }
+      umma_commit_warp(smem_u32(tcb + 8));  // this warp's MMAs have completed
+    } else if (warp >= kTpConsumerWarps + 1) {
+      // ---- PV issue of tile x = warp - 10: the whole warp runs the loop,
+      // one elected lane issues ----
+      const int x = warp - (kTpConsumerWarps + 1);
+      tc_fence_after();
+      const uint32_t idO = umma_idesc_f16(kTpRows, D, BF16, 0, 1);
+      const uint32_t ring_u = smem_u32(ring);
+      bool ok = true;
+      for (int k = 0; k < ntile; ++k) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 4 + x), k & 1));
+        if (!ok) break;
+        tc_fence_after();
         const int slot = k % NS;
         const int nbt = min(TB, my_nb - k * TB);
         const uint64_t dv = umma_desc_sw128(ring_u + slot * STAGE + TB * BLOCK_BYTES, 2048, 1024);
 #pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 4 + x), k & 1));
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int b = 0; b < TB; ++b)
-            if (b < nbt)
-              umma_f16_ts_warp(tO + x * D, tPb + x * (SC / 2) + 8 * b,
-                               dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (k > 0 || b > 0) ? 1u : 0u);
-          umma_commit_warp(smem_u32(tcb + 6 + x));  // P_x is free, O_x current
-        }
-        if (!ok) break;
-        umma_commit_warp(smem_u32(empty + slot));  // the stage may be refilled
+        for (int b = 0; b < TB; ++b)
+          if (b < nbt)
+            umma_f16_ts_warp(tO + x * D, tPb + x * (SC / 2) + 8 * b,
+                             dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (k > 0 || b > 0) ? 1u : 0u);
+        umma_commit_warp(smem_u32(tcb + 6 + x));   // P_x is free, O_x current
+        umma_commit_warp(smem_u32(empty + slot));  // (with the other tile's) the stage is free
       }
       if (!ok && lane == 0) {
         flags[0] = 1;
         atomicOr(p.status, 0x1u);
       }
-      umma_commit_warp(smem_u32(tcb + 8));  // every MMA issued above has completed
+      umma_commit_warp(smem_u32(tcb + 8));  // this warp's MMAs have completed
     } else {
       // ---- softmax: one row per thread, every stage, this tile ----
       int lo = 0, hi = 0;
@@ -725,8 +736,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           tmem_st32(tPx + lane_base, w);
         }
         // zero V of keys no row sees (outside the union, stale or NaN slots);
-        // tile 0 does it, and both tiles' PV MMAs are issued after its P
-        if (X == 0 && !(nbt == TB && key_t0 >= u_lo && key_t0 + SC <= u_hi)) {
+        // each tile does it before its own PV MMAs (the other tile's writes
+        // are the same zeros)
+        if (!(nbt == TB && key_t0 >= u_lo && key_t0 + SC <= u_hi)) {
           unsigned char *vb = ring + slot * STAGE + TB * BLOCK_BYTES;
           for (int c = 32 * (warp & 3) + lane; c < nbt * kBlockKeys; c += 128) {
             const int k = key_t0 + c;
