@@ -862,8 +862,9 @@ def run_prefill(args, world, rank, local):
         "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
                      "traffic_basis": "no ncu capture of this launch", "peak_kind": peak_kind,
-                     "note": "products on tcgen05 (128-row tiles, M = 128; Q, S, P and O "
-                             "in tensor memory; four softmax warps, one MMA-issuing thread), "
+                     "note": "products on tcgen05 (256-row tiles: two 128-row halves per "
+                             "K/V stage, M = 128; S, P and O in tensor memory; four softmax "
+                             "warps per half, one warp issuing S, one per half issuing PV), "
                              "against the measured cuBLAS bf16 peak"},
         "clocks": clk.summary(),
         "e2e": None,
