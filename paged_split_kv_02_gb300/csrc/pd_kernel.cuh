@@ -768,7 +768,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     // stage's keys, one row per thread (lanes < 16), and keeps its own
     // running (m, l) and O rows: four independent online softmaxes over
     // disjoint keys, merged in the epilogue like warp groups.  Warp 4
-    // issues the MMAs from one thread:
+    // issues the MMAs (one elected lane of the whole warp):
     //   S[64 x stage keys] = Q[64 x D] . K^T   (one MMA per 16-key block and
     //                                          16-dim step, K-major operands)
     //   O[64 x D]         += P[64 x keys] . V  (one MMA per 16-key block, V
@@ -802,57 +802,62 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     }
     const uint32_t tS = tmem_base, tO = tmem_base + 2 * SC;
     if (warp == kTcConsumerWarps - 1) {
-      if (lane == 0) {
-        // ---- MMA issue (one thread) ----
-        const uint32_t idS = umma_idesc_f16(kTcRows, kBlockKeys, BF16, 0, 0);
-        const uint32_t idO = umma_idesc_f16(kTcRows, D, BF16, 0, 1);
-        const uint32_t q_u = smem_u32(qs), p_u = smem_u32(pts), ring_u = smem_u32(ring);
-        const uint64_t dq = umma_desc_sw128(q_u, 16, NBOX * 1024);
-        bool ok = true;
-        for (int j = 0; j <= ntile; ++j) {
-          if (j < ntile) {
-            const int slot = j % NS;
-            ok = mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1);
-            if (ok && j >= 2) ok = mbar_wait_bounded(smem_u32(tcb + 2 + (j & 1)), ((j - 2) >> 1) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            const int nbt = min(TB, my_nb - j * TB);
-            // descriptors of the stage's first K block; the start-address
-            // field (bits 0-13, 16-byte units) advances with the operand
-            const uint64_t dk = umma_desc_sw128(ring_u + slot * STAGE, 16, 1024);
-            for (int b = 0; b < nbt; ++b) {
+      // ---- MMA issue: the whole warp runs the loop (every operand is
+      // warp-uniform), one elected lane issues each MMA and commit ----
+      const uint32_t idS = umma_idesc_f16(kTcRows, kBlockKeys, BF16, 0, 0);
+      const uint32_t idO = umma_idesc_f16(kTcRows, D, BF16, 0, 1);
+      const uint32_t q_u = smem_u32(qs), p_u = smem_u32(pts), ring_u = smem_u32(ring);
+      const uint64_t dq = umma_desc_sw128(q_u, 16, NBOX * 1024);
+      bool ok = true;
+      for (int j = 0; j <= ntile; ++j) {
+        if (j < ntile) {
+          const int slot = j % NS;
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1));
+          if (ok && j >= 2)
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_bounded(smem_u32(tcb + 2 + (j & 1)), ((j - 2) >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const int nbt = min(TB, my_nb - j * TB);
+          // descriptors of the stage's first K block; the start-address
+          // field (bits 0-13, 16-byte units) advances with the operand
+          const uint64_t dk = umma_desc_sw128(ring_u + slot * STAGE, 16, 1024);
+#pragma unroll
+          for (int b = 0; b < TB; ++b) {
+            if (b < nbt) {
               const uint64_t dkb = dk + (uint64_t)(b * BLOCK_BYTES / 16);
 #pragma unroll
               for (int ks = 0; ks < KS; ++ks)
-                umma_f16(tS + (j & 1) * SC + kBlockKeys * b,
-                         dq + (uint64_t)(((ks >> 2) * 1024 + (ks & 3) * 32) / 16),
-                         dkb + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) / 16), idS,
-                         ks > 0 ? 1u : 0u);
+                umma_f16_warp(tS + (j & 1) * SC + kBlockKeys * b,
+                              dq + (uint64_t)(((ks >> 2) * 1024 + (ks & 3) * 32) / 16),
+                              dkb + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) / 16), idS,
+                              ks > 0 ? 1u : 0u);
             }
-            umma_commit(smem_u32(tcb + (j & 1)));  // S of stage j is ready
           }
-          if (j >= 1) {
-            const int jj = j - 1, slot = jj % NS;
-            ok = mbar_wait_bounded(smem_u32(tcb + 4 + (jj & 1)), (jj >> 1) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            const int nbt = min(TB, my_nb - jj * TB);
-            const uint64_t dv = umma_desc_sw128(ring_u + slot * STAGE + TB * BLOCK_BYTES, 2048, 1024);
-            const uint64_t dp = umma_desc_sw128(p_u + (jj & 1) * PTILE, 16, 1024);
-            for (int b = 0; b < nbt; ++b)
-              umma_f16(tO, dp + (uint64_t)(((b >> 2) * 8192 + (b & 3) * 32) / 16),
-                       dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (jj > 0 || b > 0) ? 1u : 0u);
-            umma_commit(smem_u32(empty + slot));       // the stage may be refilled
-            umma_commit(smem_u32(tcb + 6 + (jj & 1)));  // P tile jj & 1 is free, O is current
-          }
+          umma_commit_warp(smem_u32(tcb + (j & 1)));  // S of stage j is ready
         }
-        if (!ok) {
-          flags[0] = 1;
-          atomicOr(p.status, 0x1u);
+        if (j >= 1) {
+          const int jj = j - 1, slot = jj % NS;
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 4 + (jj & 1)), (jj >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          const int nbt = min(TB, my_nb - jj * TB);
+          const uint64_t dv = umma_desc_sw128(ring_u + slot * STAGE + TB * BLOCK_BYTES, 2048, 1024);
+          const uint64_t dp = umma_desc_sw128(p_u + (jj & 1) * PTILE, 16, 1024);
+#pragma unroll
+          for (int b = 0; b < TB; ++b)
+            if (b < nbt)
+              umma_f16_warp(tO, dp + (uint64_t)(((b >> 2) * 8192 + (b & 3) * 32) / 16),
+                            dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (jj > 0 || b > 0) ? 1u : 0u);
+          umma_commit_warp(smem_u32(empty + slot));       // the stage may be refilled
+          umma_commit_warp(smem_u32(tcb + 6 + (jj & 1)));  // P tile jj & 1 is free, O is current
         }
-        umma_commit(smem_u32(tcb + 8));  // every MMA issued above has completed
       }
-      __syncwarp();
+      if (!ok && lane == 0) {
+        flags[0] = 1;
+        atomicOr(p.status, 0x1u);
+      }
+      umma_commit_warp(smem_u32(tcb + 8));  // every MMA issued above has completed
     } else {
       // ---- softmax (warp q = copy q, keys [q KPC, (q + 1) KPC) of a stage) ----
       const int r = lane & 15, prow = 16 * warp + r;  // packed row, P / MMA row
