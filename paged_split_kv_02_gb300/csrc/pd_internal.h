@@ -125,31 +125,35 @@ inline int64_t epilogue_bytes_tc(int D, int NS) {
 // Tensor-memory prefill path (TP, head size 128): two tiles of 128 packed
 // rows share each K/V stage, one row of a tile per tensor-memory lane, each
 // tile with its own four softmax warps; one warp issues the S MMAs of both
-// tiles, one warp per tile the PV MMAs.  Columns:
-// the first tile's Q (two 16-bit elements per column; the second tile's Q
-// is in shared memory), one S buffer per tile (fp32), one P buffer per tile
-// (16-bit pairs), one O per tile (fp32), rounded up to a power of two.
+// tiles, one warp per tile the PV MMAs.  Both tiles' Q are in shared
+// memory.  Columns: one S buffer per tile (fp32), two P buffers per tile
+// (16-bit pairs), one O per tile (fp32): 512 at D = 128.
 constexpr int kTpRows = 128;
 constexpr int kTpSoftmaxWarps = 8;
 constexpr int kTpConsumerWarps = kTpSoftmaxWarps + 1;  // + the warp that issues S
 // warps: softmax 0..7, S issue 8, producer 9, PV issue 10 (tile 0) and 11
 constexpr int kTpThreads = 32 * (kTpConsumerWarps + 3);
-constexpr int tp_s_col(int D) { return D / 2; }
-constexpr int tp_p_col(int D) { return D / 2 + 2 * tc_stage_keys(D); }
-constexpr int tp_o_col(int D) { return D / 2 + 3 * tc_stage_keys(D); }
+// barriers: [0,1] S full, [2,3] S read (per tile), [4..7] P written, [8..11]
+// PV done (per tile and P buffer, 4 + 2 x + b), [12] every MMA done, [13..20]
+// exponentials done (per tile and softmax warp pair, 13 + 4 x + w % 4)
+constexpr int kTpBarriers = 21;
+constexpr int kTpBlockIds = 256;  // page ids staged at a time (room for a fifth stage)
+constexpr int tp_s_col(int D) { return 0 * D; }
+constexpr int tp_p_col(int D) { return 2 * tc_stage_keys(D); }
+constexpr int tp_o_col(int D) { return 4 * tc_stage_keys(D); }
 constexpr int tp_tmem_cols(int D) {
   return tp_o_col(D) + 2 * D <= 128 ? 128 : tp_o_col(D) + 2 * D <= 256 ? 256 : 512;
 }
 static_assert(tp_o_col(128) + 2 * 128 <= 512, "tensor memory of a prefill tile");
-// Dynamic shared memory of a tensor-memory prefill launch: ring + the second
-// tile's Q + barriers + flags + staged page ids + tensor-memory address;
-// its epilogue region is the dead ring and Q tile.
+// Dynamic shared memory of a tensor-memory prefill launch: ring + both
+// tiles' Q + barriers + flags + staged page ids + tensor-memory address;
+// its epilogue region is the dead ring and Q tiles.
 inline int smem_bytes_tp(int D, int NS) {
-  return kSmemAlign + NS * kStageBytes + kTpRows * D * 2 + 2 * NS * 8 + kTcBarriers * 8 + 16 +
-         4 * kBlockIds + 16;
+  return kSmemAlign + NS * kStageBytes + 2 * kTpRows * D * 2 + 2 * NS * 8 + kTpBarriers * 8 + 16 +
+         4 * kTpBlockIds + 16;
 }
 inline int64_t epilogue_bytes_tp(int D, int NS) {
-  return (int64_t)NS * kStageBytes + (int64_t)kTpRows * D * 2;
+  return (int64_t)NS * kStageBytes + 2LL * kTpRows * D * 2;
 }
 
 // Floats the epilogue needs: combine phase and final-merge phase.

@@ -145,8 +145,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
   const int NS = p.NS, NT = p.NT, KG = p.KG,
             NC = TC ? kTcConsumerWarps : TP ? kTpConsumerWarps : RM ? (NT >> 1) * KG : NT * KG;
   const int NT8 = NT * 8;
-  // 8-row groups of the Q tile in shared memory (TP: the second tile's)
-  const int NTQ = TC ? kTcRows / 8 : TP ? kTpRows / 8 : NT;
+  // 8-row groups of the Q tile in shared memory (TP: both tiles')
+  const int NTQ = TC ? kTcRows / 8 : TP ? 2 * kTpRows / 8 : NT;
+  // page ids of 16-key blocks staged in shared memory at a time
+  constexpr int BIDS = TP ? kTpBlockIds : kBlockIds;
   unsigned char *ring = smem;
   unsigned char *qs = ring + NS * STAGE;
   unsigned char *pts = qs + NTQ * D * 16;  // TC: two P tiles
@@ -155,10 +157,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
   // TC barriers: [0,1] S full, [2,3] S read, [4,5] P written, [6,7] PV done,
   // [8] every MMA done
   uint64_t *tcb = empty + NS;
-  uint64_t *fl64 = tcb + (TC || TP ? kTcBarriers : 0);
+  uint64_t *fl64 = tcb + (TC ? kTcBarriers : TP ? kTpBarriers : 0);
   volatile int *flags = reinterpret_cast<volatile int *>(fl64);  // [0] abort, [1] last
   uint64_t *mbar_merge = fl64 + 1;                               // flags[2..3]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fl64) + 4 + kBlockIds;  // after the page ids
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fl64) + 4 + BIDS;  // after the page ids
   uint32_t tmem_base = 0;
   // Warp dot-product path (DOT): Q rows in fp32 [8][D], then one P buffer
   // [stage keys][8] fp32 per warp group, 16-byte aligned after the page ids
@@ -185,10 +187,14 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
       // RM: by its NT / 2 warps)
       mbar_init(smem_u32(empty + lane), TC ? 1 : TP ? 2 : RM ? NT >> 1 : NT);
     }
-    if constexpr (TC || TP) {
-      // (TP: every MMA done = the S warp's and both PV warps' last commits)
-      if (lane < kTcBarriers)
-        mbar_init(smem_u32(tcb + lane), (lane >= 2 && lane <= 5) ? 4 : (TP && lane == 8) ? 3 : 1);
+    if constexpr (TC) {
+      if (lane < kTcBarriers) mbar_init(smem_u32(tcb + lane), (lane >= 2 && lane <= 5) ? 4 : 1);
+    }
+    if constexpr (TP) {
+      // S read and P written: a tile's four softmax warps; every MMA done:
+      // the S warp's and both PV warps' last commits
+      if (lane < kTpBarriers)
+        mbar_init(smem_u32(tcb + lane), (lane >= 2 && lane <= 7) ? 4 : lane == 12 ? 3 : 1);
     }
     if (lane == 31) {
       mbar_init(smem_u32(mbar_merge), 1);
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     const bool spec_ok = spec_on && my_b0 == spec_b0;
     auto load_pids = [&](int base) {
       __syncwarp();
-      const int n = min(kBlockIds, my_nb - base);
+      const int n = min(BIDS, my_nb - base);
       int i0 = 0;
       if (base == 0 && spec_ok) {
 #pragma unroll
@@ -394,7 +400,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     int issued = 0;
     int slot = 0, phase = 0;  // ring slot of stage j and the parity of its round
     for (int j = 0; j < ntile; ++j) {
-      if (j * TB >= pid_base + kBlockIds) {
+      if (j * TB >= pid_base + BIDS) {
         pid_base = j * TB;
         load_pids(pid_base);
       }
@@ -463,15 +469,15 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     // own four softmax warps 4 X .. 4 X + 3 (warp w owns lanes 32 (w % 4) ..
     // 32 (w % 4) + 31, one row per thread).  Warp 8 issues the S MMAs, warp
     // 10 + X the PV MMAs of tile X, each as soon as its inputs are ready:
-    //   S_X[128 x stage keys] = Q_X . K^T  (A = Q_0 from tensor memory, Q_1
-    //                                     from shared memory; B = the stage's
-    //                                     K, landed box-major, K-major; N = 64,
-    //                                     one MMA per 16 dims)
+    //   S_X[128 x stage keys] = Q_X . K^T  (A = Q_X from shared memory; B =
+    //                                     the stage's K, landed box-major,
+    //                                     K-major; N = 64, one MMA per 16 dims)
     //   O_X[128 x D]         += P_X . V    (A = P_X from tensor memory; B = one
     //                                     V block, MN-major as the copies land)
     // S of stage j + 1 is computed while the softmax of stage j runs (its S
-    // buffer is free once the softmax has read it); P of stage j + 1 is
-    // written once the PV MMAs of stage j are done.  O_X is rescaled in
+    // buffer is free once the softmax has read it); P of stage j goes to
+    // buffer j & 1, free once the PV MMAs of stage j - 2 are done, so the
+    // softmax does not wait for the PV MMAs of stage j - 1.  O_X is rescaled in
     // tensor memory only when a row's max grows more than 8 past the
     // reference its P values use (so P <= 2^8), the online-softmax update in
     // exp2 form.  Two tiles per stage halve the K/V copies per row: the
@@ -482,12 +488,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     const int rr_tp = rr0 + kTpRows * X + r_tp;
     const bool live = warp < kTpSoftmaxWarps && rr_tp < rr1v;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t tQ = tmem_base, tS = tmem_base + tp_s_col(D), tPb = tmem_base + tp_p_col(D),
+    const uint32_t tS = tmem_base + tp_s_col(D), tPb = tmem_base + tp_p_col(D),
                    tO = tmem_base + tp_o_col(D);
     if (warp < kTpSoftmaxWarps) {
-      // Q rows: tile 0 into tensor memory (16-bit pairs in memory order),
-      // tile 1 into the 128-byte-swizzled K-major tile in shared memory
-      // ([64-dim box][128 rows][128 B]); zeros for rows past the requests
+      // Q rows of tile X into its 128-byte-swizzled K-major tile in shared
+      // memory ([tile][64-dim box][128 rows][128 B]); zeros for rows past
+      // the requests
       const uint4 *src = nullptr;
       if (live) {
         const int i = token_of(rr_tp), jq = rr_tp - i * p.G;
@@ -495,31 +501,14 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
                                               (int64_t)(q0 + i) * p.q_s0 +
                                               (int64_t)(h * p.G + jq) * p.q_s1);
       }
-      if (X == 0) {
+      unsigned char *qx = qs + X * (kTpRows * D * 2);
 #pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          uint32_t w[32];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 v = live ? __ldg(src + c0 / 4 + u) : make_uint4(0u, 0u, 0u, 0u);
-            w[4 * u] = v.x;
-            w[4 * u + 1] = v.y;
-            w[4 * u + 2] = v.z;
-            w[4 * u + 3] = v.w;
-          }
-          tmem_st32(tQ + lane_base + c0, w);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-      } else {
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4 *>(qs + (c >> 3) * (kTpRows * 128) + r_tp * 128 +
-                                     (((c & 7) ^ (r_tp & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();  // the tensor core reads the tile
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(qx + (c >> 3) * (kTpRows * 128) + r_tp * 128 +
+                                   (((c & 7) ^ (r_tp & 7)) << 4)) = v;
       }
+      fence_proxy_async_smem();  // the tensor core reads the tiles
     }
     // both Q tiles are in place (softmax warps and the S warp)
     if (warp < kTpConsumerWarps) asm volatile("bar.sync 1, %0;" ::"r"(NC * 32) : "memory");
@@ -548,12 +537,11 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           for (int ks = 0; ks < KS; ++ks) {
             const uint64_t bk =
                 umma_desc_sw128(kst + (ks >> 2) * (TB * BLOCK_BYTES / NBOX) + (ks & 3) * 32, 16, 1024);
-            if (x == 0)
-              umma_f16_ts_warp(tS, tQ + 8 * ks, bk, idS, ks > 0 ? 1u : 0u);
-            else
-              umma_f16_warp(tS + SC,
-                            umma_desc_sw128(qb_u + (ks >> 2) * (kTpRows * 128) + (ks & 3) * 32, 16, 1024),
-                            bk, idS, ks > 0 ? 1u : 0u);
+            umma_f16_warp(tS + x * SC,
+                          umma_desc_sw128(qb_u + x * (kTpRows * D * 2) + (ks >> 2) * (kTpRows * 128) +
+                                              (ks & 3) * 32,
+                                          16, 1024),
+                          bk, idS, ks > 0 ? 1u : 0u);
           }
           umma_commit_warp(smem_u32(tcb + x));  // S_x of stage j is ready
         }
@@ -567,7 +555,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         flags[0] = 1;
         atomicOr(p.status, 0x1u);
       }
-      umma_commit_warp(smem_u32(tcb + 8));  // this warp's MMAs have completed
+      umma_commit_warp(smem_u32(tcb + 12));  // this warp's MMAs have completed
     } else if (warp >= kTpConsumerWarps + 1) {
       // ---- PV issue of tile x = warp - 10: the whole warp runs the loop,
       // one elected lane issues ----
@@ -577,7 +565,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
       const uint32_t ring_u = smem_u32(ring);
       bool ok = true;
       for (int k = 0; k < ntile; ++k) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 4 + x), k & 1));
+        // P of stage k is in buffer k & 1 (its barriers complete once per
+        // two stages, so a parity never stands for two phases)
+        const int pb = k & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 4 + 2 * x + pb), (k >> 1) & 1));
         if (!ok) break;
         tc_fence_after();
         const int slot = k % NS;
@@ -586,16 +577,16 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
 #pragma unroll
         for (int b = 0; b < TB; ++b)
           if (b < nbt)
-            umma_f16_ts_warp(tO + x * D, tPb + x * (SC / 2) + 8 * b,
+            umma_f16_ts_warp(tO + x * D, tPb + x * SC + pb * (SC / 2) + 8 * b,
                              dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (k > 0 || b > 0) ? 1u : 0u);
-        umma_commit_warp(smem_u32(tcb + 6 + x));   // P_x is free, O_x current
+        umma_commit_warp(smem_u32(tcb + 8 + 2 * x + pb));  // P buffer pb free, O_x current
         umma_commit_warp(smem_u32(empty + slot));  // (with the other tile's) the stage is free
       }
       if (!ok && lane == 0) {
         flags[0] = 1;
         atomicOr(p.status, 0x1u);
       }
-      umma_commit_warp(smem_u32(tcb + 8));  // this warp's MMAs have completed
+      umma_commit_warp(smem_u32(tcb + 12));  // this warp's MMAs have completed
     } else {
       // ---- softmax: one row per thread, every stage, this tile ----
       int lo = 0, hi = 0;
@@ -603,7 +594,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         hi = max(L - ml + token_of(rr_tp) + 1, 0);
         lo = p.window ? max(0, hi - p.window) : 0;
       }
-      const uint32_t tSx = tS + X * SC, tPx = tPb + X * (SC / 2), tOx = tO + X * D;
+      const uint32_t tSx = tS + X * SC, tPx = tPb + X * SC, tOx = tO + X * D;
       float m_used = -INFINITY, lsum = 0.f;
       for (int j = 0; j < ntile; ++j) {
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + X), j & 1))) {
@@ -681,12 +672,18 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         }
         const float m_new = fmaxf(m_used, mx);
         const bool need = m_used != -INFINITY && m_new > m_used + 8.f;
-        // the PV MMAs of the previous stage have completed: P_X is free and
-        // O_X current
-        bool ok = j < 1 || __all_sync(0xffffffffu,
-                                      mbar_wait_bounded(smem_u32(tcb + 6 + X), (j - 1) & 1));
+        // a rescale needs O_X current: the PV MMAs of stage j - 1 have
+        // completed (need implies j >= 1); P buffer j & 1 is free once those
+        // of stage j - 2 have
+        const bool resc = __any_sync(0xffffffffu, need);
+        bool ok = !resc || __all_sync(0xffffffffu,
+                                      mbar_wait_bounded(smem_u32(tcb + 8 + 2 * X + ((j - 1) & 1)),
+                                                        ((j - 1) >> 1) & 1));
+        if (ok && j >= 2)
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8 + 2 * X + (j & 1)),
+                                                         ((j - 2) >> 1) & 1));
         tc_fence_after();
-        if (ok && __any_sync(0xffffffffu, need)) {
+        if (ok && resc) {
           const float alpha = need ? sfu_exp2(m_used - m_new) : 1.f;
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -712,6 +709,22 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           }
           break;
         }
+        // The two tiles' exponentials take turns on the sub-partition's
+        // exp2 unit: tile 1's of stage j after tile 0's of stage j, tile 0's
+        // of stage j after tile 1's of stage j - 1 (each tile's max and
+        // waits then run under the other tile's exponentials).
+        {
+          const int pe = 13 + 4 * (1 - X) + (warp & 3);  // the other tile's "done" barrier
+          const bool mine = X == 1 || j >= 1;
+          if (mine && !__all_sync(0xffffffffu,
+                                   mbar_wait_bounded(smem_u32(tcb + pe), (X == 1 ? j : j - 1) & 1))) {
+            if (lane == 0) {
+              flags[0] = 1;
+              atomicOr(p.status, 0x1u);
+            }
+            break;
+          }
+        }
         {
           // P = 2^(x - m) rounded to the input type; the row sum takes P as
           // rounded for the MMA (four chains), so O is normalised by the
@@ -733,8 +746,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
 #pragma unroll
           for (int c = 0; c < SC / 2; ++c) ls[c & 3] += sum2(w[c], tag{});
           lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-          tmem_st32(tPx + lane_base, w);
+          tmem_st32(tPx + (j & 1) * (SC / 2) + lane_base, w);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(tcb + 13 + 4 * X + (warp & 3)));  // exponentials done
         // zero V of keys no row sees (outside the union, stale or NaN slots);
         // each tile does it before its own PV MMAs (the other tile's writes
         // are the same zeros)
@@ -754,7 +769,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         fence_proxy_async_smem();  // the zeroed V reaches the tensor core
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(tcb + 4 + X));  // P of stage j written
+        if (lane == 0) mbar_arrive(smem_u32(tcb + 4 + 2 * X + (j & 1)));  // P of stage j written
       }
       m0 = m_used;
       l0 = lsum;
@@ -1622,7 +1637,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     // (KG = 1): row 128 X + 32 (w % 4) + lane of softmax warp w of tile X,
     // once every MMA has completed
     if (warp < kTpSoftmaxWarps) {
-      const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8), 0));
+      const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 12), 0));
       tc_fence_after();
       const int g = warp >> 2, r = kTpRows * g + 32 * (warp & 3) + lane;
       const bool keep = r < NT8;
