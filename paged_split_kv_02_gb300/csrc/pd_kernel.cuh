@@ -628,10 +628,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         // tokens have Q = 0, finite scores, and are never stored)
         const bool fast = nbt == TB && key_t0 >= v_lo && key_t0 + SC <= v_hi;
         const float sl2 = p.scale_log2;
-        float mx;
-        if (fast) {
-          // the largest scaled score: the largest (scale >= 0) or smallest
-          // raw score, eight independent chains
+        // the largest scaled score of an unmasked stage: the largest (scale
+        // >= 0) or smallest raw score, eight independent chains
+        auto fast_max = [&]() -> float {
           float a[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) a[u] = __uint_as_float(sr[u]);
@@ -650,41 +649,15 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
 #pragma unroll
               for (int v = 0; v < u; ++v) a[v] = fminf(a[v], a[v + u]);
           }
-          mx = a[0] * sl2;
-        } else {
-          // scaled scores with the mask applied (-inf), kept as fp32 bits
-          float a[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) a[u] = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < SC; ++c) {
-            const int k = key_t0 + c;
-            float x = __uint_as_float(sr[c]) * sl2;
-            if (!live || !(c < nbt * kBlockKeys && k >= lo && k < hi)) x = -INFINITY;
-            sr[c] = __float_as_uint(x);
-            a[c & 7] = fmaxf(a[c & 7], x);
-          }
-#pragma unroll
-          for (int u = 4; u >= 1; u >>= 1)
-#pragma unroll
-            for (int v = 0; v < u; ++v) a[v] = fmaxf(a[v], a[v + u]);
-          mx = a[0];
-        }
-        const float m_new = fmaxf(m_used, mx);
-        const bool need = m_used != -INFINITY && m_new > m_used + 8.f;
-        // a rescale needs O_X current: the PV MMAs of stage j - 1 have
-        // completed (need implies j >= 1); P buffer j & 1 is free once those
-        // of stage j - 2 have
-        const bool resc = __any_sync(0xffffffffu, need);
-        bool ok = !resc || __all_sync(0xffffffffu,
-                                      mbar_wait_bounded(smem_u32(tcb + 8 + 2 * X + ((j - 1) & 1)),
-                                                        ((j - 1) >> 1) & 1));
-        if (ok && j >= 2)
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8 + 2 * X + (j & 1)),
-                                                         ((j - 2) >> 1) & 1));
-        tc_fence_after();
-        if (ok && resc) {
-          const float alpha = need ? sfu_exp2(m_used - m_new) : 1.f;
+          return a[0] * sl2;
+        };
+        // O_X *= alpha row by row in tensor memory (the whole warp), once the
+        // PV MMAs of stage j - 1 have completed
+        auto rescale_o = [&](float alpha) -> bool {
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8 + 2 * X + ((j - 1) & 1)),
+                                                         ((j - 1) >> 1) & 1)))
+            return false;
+          tc_fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
@@ -696,12 +669,55 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           }
           tmem_wait_st();
           tc_fence_before();
-          if (need) {
-            lsum *= alpha;
-            m_used = m_new;
+          return true;
+        };
+        // An unmasked stage with a reference on every row takes its
+        // exponentials straight against that reference, tracking the largest
+        // P; only a row whose P exceeds 2^8 (its max grew more than 8 past
+        // the reference) needs the max, a rescale and the stage again.
+        const bool direct = fast && __all_sync(0xffffffffu, m_used != -INFINITY);
+        bool ok = true;
+        if (!direct) {
+          float mx;
+          if (fast) {
+            mx = fast_max();
+          } else {
+            // scaled scores with the mask applied (-inf), kept as fp32 bits
+            float a[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) a[u] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < SC; ++c) {
+              const int k = key_t0 + c;
+              float x = __uint_as_float(sr[c]) * sl2;
+              if (!live || !(c < nbt * kBlockKeys && k >= lo && k < hi)) x = -INFINITY;
+              sr[c] = __float_as_uint(x);
+              a[c & 7] = fmaxf(a[c & 7], x);
+            }
+#pragma unroll
+            for (int u = 4; u >= 1; u >>= 1)
+#pragma unroll
+              for (int v = 0; v < u; ++v) a[v] = fmaxf(a[v], a[v + u]);
+            mx = a[0];
           }
+          const float m_new = fmaxf(m_used, mx);
+          const bool need = m_used != -INFINITY && m_new > m_used + 8.f;
+          // (need implies j >= 1)
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? sfu_exp2(m_used - m_new) : 1.f;
+            ok = rescale_o(alpha);
+            if (need) {
+              lsum *= alpha;
+              m_used = m_new;
+            }
+          }
+          if (m_used == -INFINITY) m_used = m_new;
         }
-        if (m_used == -INFINITY) m_used = m_new;
+        // P buffer j & 1 is free once the PV MMAs of stage j - 2 have completed
+        if (ok && j >= 2)
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8 + 2 * X + (j & 1)),
+                                                         ((j - 2) >> 1) & 1));
+        tc_fence_after();
         if (!ok) {
           if (lane == 0) {
             flags[0] = 1;
@@ -729,20 +745,46 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           // P = 2^(x - m) rounded to the input type; the row sum takes P as
           // rounded for the MMA (four chains), so O is normalised by the
           // weights it was formed with
-          const float mu = m_used == -INFINITY ? 0.f : m_used;
           uint32_t w[SC / 2];
-          float ls[4] = {0.f, 0.f, 0.f, 0.f};
-          if (fast) {
+          auto exps = [&](float mu) -> float {  // returns the largest P (direct stages)
+            float pm[2] = {0.f, 0.f};
+            if (fast) {
 #pragma unroll
-            for (int c = 0; c < SC; c += 2)
-              w[c >> 1] = pack2(sfu_exp2(fmaf(__uint_as_float(sr[c]), sl2, -mu)),
-                                sfu_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -mu)), tag{});
-          } else {
+              for (int c = 0; c < SC; c += 2) {
+                const float p0 = sfu_exp2(fmaf(__uint_as_float(sr[c]), sl2, -mu));
+                const float p1 = sfu_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -mu));
+                pm[0] = fmaxf(pm[0], p0);
+                pm[1] = fmaxf(pm[1], p1);
+                w[c >> 1] = pack2(p0, p1, tag{});
+              }
+            } else {
 #pragma unroll
-            for (int c = 0; c < SC; c += 2)
-              w[c >> 1] = pack2(sfu_exp2(__uint_as_float(sr[c]) - mu),
-                                sfu_exp2(__uint_as_float(sr[c + 1]) - mu), tag{});
+              for (int c = 0; c < SC; c += 2)
+                w[c >> 1] = pack2(sfu_exp2(__uint_as_float(sr[c]) - mu),
+                                  sfu_exp2(__uint_as_float(sr[c + 1]) - mu), tag{});
+            }
+            return fmaxf(pm[0], pm[1]);
+          };
+          const float pmax = exps(m_used == -INFINITY ? 0.f : m_used);
+          // (fmaxf skips a NaN P, as the max skipped a NaN score)
+          if (direct && __any_sync(0xffffffffu, pmax > 256.f)) {
+            const float m_new = fmaxf(m_used, fast_max());
+            const bool need = m_new > m_used + 8.f;
+            const float alpha = need ? sfu_exp2(m_used - m_new) : 1.f;
+            if (!rescale_o(alpha)) {
+              if (lane == 0) {
+                flags[0] = 1;
+                atomicOr(p.status, 0x1u);
+              }
+              break;
+            }
+            if (need) {
+              lsum *= alpha;
+              m_used = m_new;
+            }
+            exps(m_used);
           }
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int c = 0; c < SC / 2; ++c) ls[c & 3] += sum2(w[c], tag{});
           lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
