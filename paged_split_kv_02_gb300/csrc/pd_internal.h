@@ -134,9 +134,8 @@ constexpr int kTpConsumerWarps = kTpSoftmaxWarps + 1;  // + the warp that issues
 // warps: softmax 0..7, S issue 8, producer 9, PV issue 10 (tile 0) and 11
 constexpr int kTpThreads = 32 * (kTpConsumerWarps + 3);
 // barriers: [0,1] S full, [2,3] S read (per tile), [4..7] P written, [8..11]
-// PV done (per tile and P buffer, 4 + 2 x + b), [12] every MMA done, [13..20]
-// exponentials done (per tile and softmax warp pair, 13 + 4 x + w % 4)
-constexpr int kTpBarriers = 21;
+// PV done (per tile and P buffer, 4 + 2 x + b), [12] every MMA done
+constexpr int kTpBarriers = 13;
 constexpr int kTpBlockIds = 256;  // page ids staged at a time (room for a fifth stage)
 constexpr int tp_s_col(int D) { return 0 * D; }
 constexpr int tp_p_col(int D) { return 2 * tc_stage_keys(D); }

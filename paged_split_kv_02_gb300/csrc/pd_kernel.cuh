@@ -725,22 +725,6 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           }
           break;
         }
-        // The two tiles' exponentials take turns on the sub-partition's
-        // exp2 unit: tile 1's of stage j after tile 0's of stage j, tile 0's
-        // of stage j after tile 1's of stage j - 1 (each tile's max and
-        // waits then run under the other tile's exponentials).
-        {
-          const int pe = 13 + 4 * (1 - X) + (warp & 3);  // the other tile's "done" barrier
-          const bool mine = X == 1 || j >= 1;
-          if (mine && !__all_sync(0xffffffffu,
-                                   mbar_wait_bounded(smem_u32(tcb + pe), (X == 1 ? j : j - 1) & 1))) {
-            if (lane == 0) {
-              flags[0] = 1;
-              atomicOr(p.status, 0x1u);
-            }
-            break;
-          }
-        }
         {
           // P = 2^(x - m) rounded to the input type; the row sum takes P as
           // rounded for the MMA (four chains), so O is normalised by the
@@ -790,8 +774,6 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
           tmem_st32(tPx + (j & 1) * (SC / 2) + lane_base, w);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(tcb + 13 + 4 * X + (warp & 3)));  // exponentials done
         // zero V of keys no row sees (outside the union, stale or NaN slots);
         // each tile does it before its own PV MMAs (the other tile's writes
         // are the same zeros)
