@@ -61,6 +61,22 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, std::false_type /*
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
 }
+// The largest element of 32 packed pairs, widened to fp32 (NaN skipped).
+template <int N>
+__device__ __forceinline__ float max2_of(const uint32_t (&w)[N], std::true_type /*bf16*/) {
+  __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162 *>(&w[0]);
+#pragma unroll
+  for (int i = 1; i < N; ++i) m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+  return fmaxf(__low2float(m), __high2float(m));
+}
+template <int N>
+__device__ __forceinline__ float max2_of(const uint32_t (&w)[N], std::false_type /*fp16*/) {
+  __half2 m = *reinterpret_cast<const __half2 *>(&w[0]);
+#pragma unroll
+  for (int i = 1; i < N; ++i) m = __hmax2(m, *reinterpret_cast<const __half2 *>(&w[i]));
+  return fmaxf(__low2float(m), __high2float(m));
+}
+
 // lo + hi of a packed pair, widened back to fp32
 __device__ __forceinline__ float sum2(uint32_t w, std::true_type /*bf16*/) {
   return __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
@@ -731,23 +747,21 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           // weights it was formed with
           uint32_t w[SC / 2];
           auto exps = [&](float mu) -> float {  // returns the largest P (direct stages)
-            float pm[2] = {0.f, 0.f};
+            float pmax = 0.f;
             if (fast) {
 #pragma unroll
-              for (int c = 0; c < SC; c += 2) {
-                const float p0 = sfu_exp2(fmaf(__uint_as_float(sr[c]), sl2, -mu));
-                const float p1 = sfu_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -mu));
-                pm[0] = fmaxf(pm[0], p0);
-                pm[1] = fmaxf(pm[1], p1);
-                w[c >> 1] = pack2(p0, p1, tag{});
-              }
+              for (int c = 0; c < SC; c += 2)
+                w[c >> 1] = pack2(sfu_exp2(fmaf(__uint_as_float(sr[c]), sl2, -mu)),
+                                  sfu_exp2(fmaf(__uint_as_float(sr[c + 1]), sl2, -mu)), tag{});
+              // the largest P as rounded: packed maxima, two per instruction
+              pmax = max2_of(w, tag{});
             } else {
 #pragma unroll
               for (int c = 0; c < SC; c += 2)
                 w[c >> 1] = pack2(sfu_exp2(__uint_as_float(sr[c]) - mu),
                                   sfu_exp2(__uint_as_float(sr[c + 1]) - mu), tag{});
             }
-            return fmaxf(pm[0], pm[1]);
+            return pmax;
           };
           const float pmax = exps(m_used == -INFINITY ? 0.f : m_used);
           // (fmaxf skips a NaN P, as the max skipped a NaN score)
