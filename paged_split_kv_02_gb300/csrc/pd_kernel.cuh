@@ -1682,8 +1682,29 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
       const bool have = ntile > 0 && done;
       const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
       float *dst = cp + (size_t)r * D;
+      if (nseg == 1) {
+        // an unsplit tile: each row normalised and stored from here
+        const float inv = (have && l0 > 0.f) ? sfu_rcp(l0) : 0.f;
+        T *orow = r < nrows ? out_row(r) : nullptr;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tmem_base + tp_o_col(D) + g * D + lane_base + c0, o);
+          tmem_wait_ld();
+          if (orow) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              const float v[8] = {__uint_as_float(o[i]) * inv,     __uint_as_float(o[i + 1]) * inv,
+                                  __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv,
+                                  __uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv,
+                                  __uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv};
+              store8<BF16>(orow + c0 + i, v);
+            }
+          }
+        }
+      }
+#pragma unroll 1
+      for (int c0 = 0; c0 < D && nseg > 1; c0 += 32) {
         uint32_t o[32];
         tmem_ld32(tmem_base + tp_o_col(D) + g * D + lane_base + c0, o);
         tmem_wait_ld();
@@ -1756,6 +1777,17 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     mrow[g_k * NT8 + r1] = m1;
     lrow[g_k * NT8 + r0] = l0;
     lrow[g_k * NT8 + r1] = l1;
+  }
+  if constexpr (TP) {
+    if (nseg == 1) {
+      // every row was stored from tensor memory above: free it and leave
+      __syncthreads();
+      if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+      }
+      return;
+    }
   }
   if (CS == 1) {
     // ---- no cluster: one pass over the warp groups' raw accumulators -------
