@@ -537,17 +537,18 @@ def make_prefill_case(name: str, *, seed: int, q_lens: Sequence[int], contexts: 
                       dtype: torch.dtype = torch.bfloat16, head_size: int = 128,
                       num_q_heads: int = 32, num_kv_heads: int = 8, page_size: int = 16,
                       layout: int = HND, window: int = 0, pad_tokens: int = 0,
-                      v_mean: float = 0.0, device: str = "cpu",
+                      v_mean: float = 0.0, std: float = 1.0, device: str = "cpu",
                       gen_device: str = "cpu") -> DecodeCase:
     """A prefill batch: request s has q_lens[s] new tokens after contexts[s]
     cached ones (seq_lens = context + q_len, the new tokens' keys included),
-    rows as in ``make_varlen_case``."""
+    rows as in ``make_varlen_case``; q, K and V drawn with standard
+    deviation ``std``."""
     lens = [int(c) + int(m) for c, m in zip(contexts, q_lens)]
     return make_varlen_case(name, seed=seed, q_lens=q_lens, pad_tokens=pad_tokens, dtype=dtype,
                             head_size=head_size, num_q_heads=num_q_heads,
                             num_kv_heads=num_kv_heads, page_size=page_size, seq_lens=lens,
-                            layout=layout, window=window, v_mean=v_mean, device=device,
-                            gen_device=gen_device)
+                            layout=layout, window=window, v_mean=v_mean, std=std,
+                            device=device, gen_device=gen_device)
 
 
 def prefill_flops(case) -> int:

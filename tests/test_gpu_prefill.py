@@ -6,6 +6,8 @@ sees seq_len - q_len + (t - query_start[r]) + 1 keys).  Bounds as for
 decode: max-abs 2e-3 (fp16) / 1e-2 (bf16) and, row by row, 2^-10 / 2^-7 of
 the row's largest oracle value."""
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -110,6 +112,22 @@ def test_tensor_memory_tiles_d128_split_nhd():
                             layout=W.NHD, v_mean=1.0)
     _, info = _run(c, num_sms=4000, expect_split=True)
     assert info.num_split_tiles >= 4
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("scale", [12.0, -10.0, 0.0])
+def test_tensor_memory_tiles_d128_large_scores(scale, dtype):
+    # q, K, V of std 0.4 and scores of std |scale| 0.16 sqrt(D) log2(e) (~30):
+    # a row's max often grows by more than 8 (log2 units) past its reference
+    # on an unmasked stage, so the rescale of O and the stage's exponentials
+    # taken again are exercised (fp16 P then overflows before the retake); a
+    # negative scale takes the smallest raw score as the max; zero gives
+    # uniform weights.  The outputs stay below ~2, where the max-abs bound
+    # is above the output's own rounding.
+    c = W.make_prefill_case(f"pf_tp_scale{scale}", seed=41, q_lens=[300, 64],
+                            contexts=[1500, 700], dtype=dtype, head_size=128, num_q_heads=32,
+                            num_kv_heads=8, page_size=16, std=0.4)
+    _run(dataclasses.replace(c, scale=scale))
 
 
 def test_prefill_sized_batch_sampled_rows():
