@@ -268,6 +268,19 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
     const int64_t seg_floor = (window > 0 && rg > 1) ? 2 : min_seg_blocks;
     nseg = std::max<int64_t>(1, target / std::max<int64_t>(units, 1));
     nseg = std::min(nseg, std::max<int64_t>(1, nb_max / seg_floor));
+    // With 1-8 MiB of K and V per (sequence, kv head), fewer and longer
+    // segments: the merge's parts then cost more than the shorter stream
+    // saves.  Measured at D=128, 8 kv heads, M=1 and 4 (us per call,
+    // segments per head): 2k keys 9.3 (12) against 10.1 (19); 4k 11.4 (14)
+    // against 12.1 (19); 8k 14.3 (16) against 14.7 (19); 16k and 32k as
+    // good or better with 19.  The CTAs are capped at (12 + 7/3 log2(MiB))
+    // / 19 of the resident ones, which passes through those optima.
+    const int64_t unit_bytes = nb_max * kBlockKeys * 4LL * D;  // K + V of a unit
+    if (!(window > 0 && rg > 1) && unit_bytes >= (1LL << 20) && unit_bytes < (8LL << 20)) {
+      const double frac = (12.0 + 7.0 / 3.0 * std::log2((double)unit_bytes / (1 << 20))) / 19.0;
+      const int64_t cap = (int64_t)(frac * (double)target) / std::max<int64_t>(units, 1);
+      nseg = std::min(nseg, std::max<int64_t>(1, cap));
+    }
     // a CTA that would move at most kNoSplitBytes of K and V alone is not
     // split: the merge's round trips cost more than the stream time a split
     // saves (300 keys at D=128: 5.8 us unsplit, 6.6 us in 3 segments)

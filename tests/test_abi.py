@@ -84,6 +84,24 @@ def test_plan_invariants(shape):
         assert p["grid_x"] >= 128                      # a long sequence fills the SMs
 
 
+def test_plan_segments_grow_with_the_context():
+    # one sequence, 8 kv heads, D=128, M=4: with 1-8 MiB of K and V per kv
+    # head the CTAs are capped at (12 + 7/3 log2(MiB)) / 19 of the SMs
+    # (fewer, longer segments: fewer parts to merge), below and above that
+    # the SM count and the segment floor decide
+    want = {1024: 10, 2048: 12, 4096: 14, 8192: 16, 16384: 19, 32768: 19}
+    for L, nseg in want.items():
+        sd = _fake_scratch(1, 32, 8, 128, 4, 256)
+        p = pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, L // 16, 152, scratch_desc=sd)
+        assert p["max_segments"] == nseg, (L, p["max_segments"])
+    # the cap is a fraction of the resident CTAs, shared by the units: two
+    # kv heads at 8k keys (4 MiB each) get (12 + 14/3) / 19 x 152 / 2 = 66
+    # segments (the SM share alone gives 76, the floor 512 / 6 = 85)
+    sd = _fake_scratch(1, 8, 2, 128, 4, 256)
+    p = pd.paged_decode_plan(1, 8, 2, 128, 16, 4, 0, 8192 // 16, 152, scratch_desc=sd)
+    assert p["max_segments"] == 66
+
+
 def test_counters_per_pair_matches_header():
     text = open(pd.HEADER).read()
     assert f"#define PD_COUNTERS_PER_PAIR {pd.COUNTERS_PER_PAIR}" in text
