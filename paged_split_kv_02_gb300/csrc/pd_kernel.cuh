@@ -29,8 +29,9 @@
 // A second consumer (TC = true) runs the products on the 5th-generation
 // tensor cores instead: tcgen05 MMAs issued by one thread, accumulators in
 // tensor memory, four softmax warps (see the TC branch below).  A third
-// (TP = true) does the same for prefill tiles of 128 packed rows, one row
-// per tensor-memory lane, with Q and P read by the MMAs from tensor memory.
+// (TP = true) serves prefill tiles of 256 packed rows: two halves of 128
+// rows share each K/V stage, one row per tensor-memory lane, with S, P and
+// O in tensor memory (see the TP branch).
 //
 // Epilogue: the warp groups' (acc, m, l) are combined in shared memory into
 // the CTA's partial.  A sequence cut into several segments publishes the

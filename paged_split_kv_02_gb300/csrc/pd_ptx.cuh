@@ -191,29 +191,13 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, bool bf16, i
          ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] . B[smem], issued by one thread.
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D[tmem] (+)= A[tmem] . B[smem], issued by one thread: A (M = 128 rows, one
-// per tensor-memory lane, two 16-bit elements per 32-bit column along K) is
-// read from tensor memory.
-__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// The same MMAs (A from tensor or shared memory) and the commit, issued by
-// the whole warp with warp-uniform operands (kept in uniform registers):
-// one elected lane issues.
+// D[tmem] (+)= A . B[smem] (kind::f16, fp32 accumulate, `accumulate` = 0
+// overwrites D), A from shared memory (umma_f16_warp) or tensor memory
+// (umma_f16_ts_warp: M = 128 rows, one per tensor-memory lane, two 16-bit
+// elements per 32-bit column along K); and the commit that arrives once on
+// an mbarrier when every earlier tcgen05 op of the issuing thread has
+// completed.  Issued by the whole warp with warp-uniform operands (kept in
+// uniform registers): one elected lane issues.
 __device__ __forceinline__ void umma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -237,14 +221,6 @@ __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
           bar)
       : "memory");
 }
-// Arrive (once) on an mbarrier when every earlier tcgen05 op of this thread
-// has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
-}
-
 // 32 consecutive columns of this warp's 32 tensor-memory lanes (one lane per
 // thread), and the matching store.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
