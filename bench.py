@@ -11,6 +11,9 @@ L2) passes, so every call reads its K/V from HBM.  Per-case times come from
 CUDA graphs that cycle through enough replicas of the case to exceed 2.2x
 the L2 size.  Times are CUDA events on the launching stream around graph
 replays; the clocks are sampled with nvidia-smi during the timed region.
+Each call reads its block table, seq_lens and older pages while the
+previous call finishes (early reads, programmatic dependent launch); the
+same steps and cases are also timed with every call waiting first.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -209,8 +212,17 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(device=device)
     keys = sorted(cases)
 
-    def call(k, r, st=None):
-        pd.decode_case(cases[k][r], out=outs[k][r], scratch=scratch, stream=st)
+    # Every call of the sweep reads inputs written before the previous call
+    # started, so it may read its block table, seq_lens and pages while that
+    # call finishes (pd_options.early_reads); the same steps are also timed
+    # with every call waiting for the previous one first.
+    opts = pd.options(early_reads=1) if args.early_reads else None
+
+    def n_reps(k):
+        return len(cases[k])
+
+    def call(k, r, st=None, o=opts):
+        pd.decode_case(cases[k][r], out=outs[k][r], scratch=scratch, stream=st, opts=o)
 
     # warm the library (attributes, tensor maps) outside capture
     with torch.cuda.stream(stream):
@@ -221,14 +233,19 @@ def run_ours(args, world, rank, local):
 
     # ---- step graphs: one call per case, replicas alternating ------------
     n_step_graphs = 2
-    step_graphs = []
-    for gi in range(n_step_graphs):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in keys:
-                call(k, gi % len(cases[k]))
-        step_graphs.append(g)
-    torch.cuda.synchronize()
+
+    def step_graphs_for(o):
+        gs = []
+        for gi in range(n_step_graphs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for k in keys:
+                    call(k, gi % len(cases[k]), o=o)
+            gs.append(g)
+        torch.cuda.synchronize()
+        return gs
+
+    step_graphs = step_graphs_for(opts)
 
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -254,14 +271,31 @@ def run_ours(args, world, rank, local):
     value = world * kv_step / (step_ms * 1e-3) / 1e9
     launches = args.steps * len(keys)
 
+    # the same steps with every call waiting for the previous one first
+    wait_first = None
+    if opts is not None:
+        del step_graphs
+        graphs_w = step_graphs_for(None)
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                graphs_w[i % n_step_graphs].replay()
+            ev0.record(stream)
+            for i in range(args.steps):
+                graphs_w[i % n_step_graphs].replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        ms_w = _max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+        wait_first = {"value": round(world * kv_step / (ms_w * 1e-3) / 1e9, 1),
+                      "ms_per_step": round(ms_w, 5)}
+        del graphs_w
+
     # ---- per case: graphs over the case's replicas -------------------------
-    per_case = []
-    for k in keys:
+    def case_us(k, o):
         g = torch.cuda.CUDAGraph()
         n = len(cases[k])
         with torch.cuda.graph(g, stream=stream):
             for r in range(n):
-                call(k, r)
+                call(k, r, o=o)
         with torch.cuda.stream(stream):
             for _ in range(2):
                 g.replay()
@@ -273,15 +307,26 @@ def run_ours(args, world, rank, local):
                 g.replay()
             e1.record(stream)
         torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (reps * n)
+        return e0.elapsed_time(e1) * 1e3 / (reps * n)
+
+    per_case, pct_w = [], []
+    for k in keys:
+        us = case_us(k, opts)
         c = cases[k][0]
         kv_gbs = c.kv_bytes_touched() / (us * 1e-6) / 1e9
         alg_gbs = c.algorithmic_bytes() / (us * 1e-6) / 1e9
-        per_case.append({"M": k[0], "context": k[1], "us": round(us, 3),
-                         "kv_gbs": round(kv_gbs, 1), "pct_hbm": round(100 * alg_gbs / peak, 2),
-                         "replicas": n})
-        del g
+        row = {"M": k[0], "context": k[1], "us": round(us, 3),
+               "kv_gbs": round(kv_gbs, 1), "pct_hbm": round(100 * alg_gbs / peak, 2),
+               "replicas": n_reps(k)}
+        if opts is not None:
+            us_w = case_us(k, None)
+            row["us_wait_first"] = round(us_w, 3)
+            if k[1] >= 4096:
+                pct_w.append(100 * c.algorithmic_bytes() / (us_w * 1e-6) / 1e9 / peak)
+        per_case.append(row)
     long_ctx = [c["pct_hbm"] for c in per_case if c["context"] >= 4096]
+    if wait_first is not None and pct_w:
+        wait_first["median_pct_hbm_4k_32k"] = round(statistics.median(pct_w), 2)
     traffic, traffic_basis = None, "no ncu capture of these kernel sources"
     if _kernel_sources_digest() == TRAFFIC_CAPTURE["sources"]:
         traffic = round(TRAFFIC_CAPTURE["dram_over_algorithmic"] * alg_step / len(keys))
@@ -291,7 +336,7 @@ def run_ours(args, world, rank, local):
     # ---- the other decode configurations, timed the same way ----------------
     configs = None
     if not args.no_configs:
-        configs = measure_other_configs(pd, device, l2, peak, stream)
+        configs = measure_other_configs(pd, device, l2, peak, stream, opts=opts)
 
     # ---- end to end through the C ABI with host buffers --------------------
     e2e = None
@@ -324,6 +369,10 @@ def run_ours(args, world, rank, local):
             "workload": workload,
             "l2": "inputs larger than L2: rotating replicas, >= 2.2x L2 per case",
             "timing": "CUDA graphs of the calls, CUDA events on the launching stream",
+            "launch": ("early reads: a call reads its block table, seq_lens and older pages "
+                       "while the previous call finishes (programmatic dependent launch); "
+                       "wait_first: every call waits for the previous one")
+                      if opts is not None else "every call waits for the previous one",
             "parallelism": f"replicas x{world}",
         },
         "gpu_launches": launches,
@@ -338,6 +387,7 @@ def run_ours(args, world, rank, local):
             "peak_kind": peak_kind,
         },
         "median_pct_hbm_4k_32k": round(statistics.median(long_ctx), 2) if long_ctx else None,
+        "wait_first": wait_first,
         "cases": per_case,
         "other_configs": configs,
         "clocks": clk.summary(),
@@ -387,7 +437,8 @@ def run_configs(args, world, rank, local):
     l2 = int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 126 << 20))
     peak, peak_kind = _peaks()
     stream = torch.cuda.Stream(device=device)
-    res = measure_other_configs(pd, device, l2, peak, stream, args.config_filter)
+    res = measure_other_configs(pd, device, l2, peak, stream, args.config_filter,
+                                opts=pd.options(early_reads=1) if args.early_reads else None)
     status = pd.paged_decode_device_status(reset=True)
     if rank == 0:
         print(json.dumps({"metric": METRIC, "unit": "us per call", "n_gpus": world,
@@ -395,7 +446,7 @@ def run_configs(args, world, rank, local):
                           "device_status": status}), flush=True)
 
 
-def measure_other_configs(pd, device, l2, peak, stream, name_filter=""):
+def measure_other_configs(pd, device, l2, peak, stream, name_filter="", opts=None):
     """µs per call, K+V GB/s and % of the HBM peak of each configuration
     (CUDA graphs over replicas that exceed 2.2 x L2, as for the sweep; a
     windowed or 300-key call moves under 1 MB and is timed on 16 replicas
@@ -411,7 +462,8 @@ def measure_other_configs(pd, device, l2, peak, stream, name_filter=""):
         sc = pd.Scratch(first.num_seqs, first.num_q_heads, first.num_kv_heads, first.head_size,
                         first.max_query_len, max_splits=256, device=device)
         outs = [torch.empty_like(c.q) for c in reps]
-        calls = [(lambda c=c, o=o: pd.decode_case(c, out=o, scratch=sc)) for c, o in zip(reps, outs)]
+        calls = [(lambda c=c, o=o: pd.decode_case(c, out=o, scratch=sc, opts=opts))
+                 for c, o in zip(reps, outs)]
         with torch.cuda.stream(stream):
             for c in calls:
                 c()
@@ -458,6 +510,7 @@ def measure_e2e(pd, cases, outs, scratch, stream, keys, args):
     for t, off in zip(ins, in_offs):
         view(host_in, off, t).copy_(t.cpu())
     lib = pd.lib()
+    early = pd.options(early_reads=1)
     calls = []
     for i, k in enumerate(keys):
         c = cases[k][0]
@@ -469,15 +522,20 @@ def measure_e2e(pd, cases, outs, scratch, stream, keys, args):
             c.num_q_heads, c.num_kv_heads, c.head_size, c.page_size, c.max_query_len, c.window,
             ctypes.c_float(c.scale), c.layout, ctypes.byref(scratch.desc),
             ctypes.c_void_p(stream.cuda_stream)]
+        if args.early_reads:
+            # (q, block table and seq_lens come from the step's one host copy,
+            # made before the first call: every call may read early)
+            cargs = cargs + [ctypes.byref(early)]
         calls.append((descs, cargs))
     h2d, d2h = in_bytes, out_bytes
+    entry = lib.paged_decode_attn_opts if args.early_reads else lib.paged_decode_attn
     kv_step = sum(cases[k][0].kv_bytes_touched() for k in keys)
 
     def step():
         with torch.cuda.stream(stream):
             dev_in.copy_(host_in, non_blocking=True)
             for _, a in calls:
-                rc = lib.paged_decode_attn(*a)
+                rc = entry(*a)
                 if rc != 0:
                     raise RuntimeError(f"paged_decode_attn: {rc}")
             host_out.copy_(dev_out, non_blocking=True)
@@ -492,7 +550,9 @@ def measure_e2e(pd, cases, outs, scratch, stream, keys, args):
     return {"value": round(kv_step / dt / 1e9, 1), "unit": UNIT, "ms_per_step": round(dt * 1e3, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "transfers": "one pinned host->device copy of every call's inputs and one "
-                         "device->host copy of every output per step"}
+                         "device->host copy of every output per step",
+            "call": "paged_decode_attn_opts (early reads)" if args.early_reads
+                    else "paged_decode_attn"}
 
 
 def _oracle_sweep(host_cases, keys, nthreads):
@@ -895,6 +955,10 @@ def main():
                     help="requests of the varlen batch (fewer for profiling runs)")
     ap.add_argument("--cases", default="",
                     help="restrict the sweep, e.g. 4:32768,1:4096 (profiling runs only)")
+    ap.add_argument("--early-reads", type=int, default=1, choices=[0, 1],
+                    help="1 (default): decode calls read their block table, seq_lens and "
+                         "older pages while the previous call finishes "
+                         "(pd_options.early_reads); 0: every call waits for the previous one")
     args = ap.parse_args()
     args.only = None
     if args.cases:

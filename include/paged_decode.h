@@ -181,6 +181,26 @@ typedef struct pd_options {
                         arrivals before it gives up and reports
                         PD_DEV_WAIT_TIMEOUT (0 = one second); for tests of
                         that path                                              */
+  int early_reads;   /* 1 = the caller vouches that block_table, seq_lens,
+                        query_start and every cached key and value older than
+                        each sequence's newest max_query_len tokens were
+                        written before the previous kernel on the stream
+                        started.  The call then reads them, and streams those
+                        pages into shared memory, while that kernel finishes
+                        (programmatic dependent launch); q, the newest keys
+                        and values, and every write still wait for it to
+                        complete.  This is the case of a decode step whose
+                        previous kernel writes only the new tokens' keys and
+                        values (paged_rope_cache_write) or is an attention
+                        call of another layer.  A split call whose grid
+                        fills more than ~58 % of the SMs is then launched
+                        without the cooperative attribute (so that it starts
+                        on the SMs the previous call frees); its mergers
+                        still wait for every CTA of the call, which a kernel
+                        on another stream holding SMs for longer than the
+                        wait limit would turn into PD_DEV_WAIT_TIMEOUT.
+                        0 = read nothing before the previous kernel has
+                        completed.  Anything else: PD_EINVAL.                  */
 } pd_options;
 
 /* paged_decode_attn with explicit knobs (opts may be NULL). */

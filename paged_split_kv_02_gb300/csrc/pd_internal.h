@@ -66,6 +66,11 @@ struct Params {
   int mergers;         // K_max of the cooperative merge (a power of two)
   unsigned long long wait_limit_ns;  // bound of a cooperative merger's wait for arrivals
   int num_seqs;                      // sequences of the call (rows of seq_lens)
+  // 1: the block table, seq_lens, query_start and every key / value older
+  // than a sequence's newest M tokens are complete before the previous grid
+  // on the stream started, so they are read (and those pages streamed)
+  // before the dependency wait; q, the newest keys and every write wait
+  int early;
   // prefill: the work list (int32 [items][8]: sequence, tile, segment,
   // segments, split tile, first partial slot, blocks, 0), or null; the
   // split tiles and partial slots (per kv head) the scratch holds

@@ -262,7 +262,11 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
   // Launched with programmatic stream serialisation: wait here until the
   // previous grid on the stream (which may have written q, the caches, the
   // block table or the scratch) has completed, before reading any of them.
-  grid_dependency_wait();
+  // With p.early the caller vouches for the block table, seq_lens,
+  // query_start and the older keys: the producer streams those pages while
+  // the previous grid finishes, and every other warp waits at the top of
+  // its branch below.
+  if (!p.early) grid_dependency_wait();
 
   // prefill: the work item (sequence, tile, segment, segments, split tile,
   // first partial slot), checked against the launch before anything is
@@ -416,10 +420,17 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     if (my_nb > 0) load_pids(0);
     int issued = 0;
     int slot = 0, phase = 0;  // ring slot of stage j and the parity of its round
+    // (p.early: keys at and past `fresh` may come from the previous grid)
+    bool waited = !p.early;
+    const int fresh = max(L - p.M, 0);
     for (int j = 0; j < ntile; ++j) {
       if (j * TB >= pid_base + BIDS) {
         pid_base = j * TB;
         load_pids(pid_base);
+      }
+      if (!waited && (my_b0 + j * TB + min(TB, my_nb - j * TB)) * kBlockKeys > fresh) {
+        grid_dependency_wait();
+        waited = true;
       }
       if (j >= NS) {
         int ok = 1;
@@ -478,7 +489,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
       for (int j = max(0, issued - NS); j < issued; ++j)
         if (!mbar_wait_bounded(smem_u32(full + j % NS), (j / NS) & 1)) atomicOr(p.status, 0x1u);
     }
+    if (!waited) grid_dependency_wait();  // before the epilogue's writes
   } else {
+    if (p.early) grid_dependency_wait();  // before q and any write
     if constexpr (TP) {
     // ================= tensor-memory prefill consumers ====================
     // Two tiles of 128 packed rows share every K/V stage: tile X (X = 0, 1)

@@ -26,7 +26,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_strerror(lib):
-    assert pd.paged_decode_version() == 10200
+    assert pd.paged_decode_version() == 10300
     for code in range(0, -9, -1):
         assert lib.paged_decode_strerror(code)
     assert b"unknown" in lib.paged_decode_strerror(-99)
@@ -160,6 +160,20 @@ def test_wait_limit_option_checked():
     with pytest.raises(pd.PagedDecodeError):
         pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 256, 152,
                              opts=pd.options(wait_limit_us=-1))
+
+
+def test_early_reads_option_checked():
+    for v in (-1, 2):
+        with pytest.raises(pd.PagedDecodeError):
+            pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 256, 152,
+                                 opts=pd.options(early_reads=v))
+    # the option does not change the plan
+    a = pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 2048, 152,
+                             scratch_desc=_fake_scratch(1, 32, 8, 128, 4, 64))
+    b = pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 2048, 152,
+                             scratch_desc=_fake_scratch(1, 32, 8, 128, 4, 64),
+                             opts=pd.options(early_reads=1))
+    assert a == b
 
 
 def test_plan_without_scratch_does_not_split():

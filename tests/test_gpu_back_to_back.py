@@ -100,6 +100,35 @@ def test_back_to_back_calls_share_one_scratch():
     assert pd.paged_decode_device_status(reset=True) == 0
 
 
+def _early(o):
+    """The launch options `o` with early reads on."""
+    d = {n: getattr(o, n) for n, _ in o._fields_} if o is not None else {}
+    d["early_reads"] = 1
+    return pd.options(**d)
+
+
+def test_back_to_back_calls_with_early_reads():
+    """Every call reads its block table, seq_lens and older pages while the
+    previous call finishes (its own inputs were written before that call
+    started); outputs, q and the scratch wait for it."""
+    cases = _cases()
+    sc = _shared_scratch(cases)
+    gpu = [(c.to("cuda"), _early(o)) for c, o in cases]
+    stream = torch.cuda.Stream()
+    outs = []
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for g, o in gpu:
+                outs.append(pd.decode_case(g, scratch=sc, opts=o, stream=stream))
+    torch.cuda.synchronize()
+    expected = [c for c, _ in cases] * 2
+    for c, out in zip(expected, outs):
+        check(c, out)
+    assert int(sc.counters().abs().sum()) == 0, "counters not left at zero"
+    assert pd.paged_decode_device_status(reset=True) == 0
+
+
 def test_graph_replays_with_inputs_changed_between_replays():
     cases = [_cases()[i] for i in (0, 1, 4, 6)]
     sc = _shared_scratch(cases)

@@ -4,7 +4,9 @@ case, replicas alternating between graphs, one shared scratch, calls
 overlapping through programmatic dependent launch) and replays the graphs
 back to back.  Here the same pattern runs on a reduced sweep, and after the
 replays every call's output is checked on sampled rows against the oracle,
-with the counters left at zero."""
+with the counters left at zero; both with the bench's early reads (a call
+reads its block table, seq_lens and older pages while the previous call
+finishes) and with every call waiting first."""
 
 import pytest
 import torch
@@ -16,11 +18,15 @@ from gpu_helpers import check, sample_rows
 pytestmark = pytest.mark.gpu
 
 
-def test_bench_step_graph_replays_match_the_oracle():
+@pytest.mark.parametrize("early", [0, 1])
+def test_bench_step_graph_replays_match_the_oracle(early):
     pd.build()
     device = "cuda"
     l2 = int(torch.cuda.get_device_properties(0).L2_cache_size)
-    only = {(1, 4096), (4, 4096), (2, 128), (3, 16384)}
+    # (1024 keys: a cooperative launch under early reads; 4096 and 16384: a
+    # plain one)
+    only = {(1, 4096), (4, 4096), (2, 128), (3, 16384), (2, 1024)}
+    opts = pd.options(early_reads=1) if early else None
     # (two replicas per case are enough here: the check is of the outputs)
     cases = bench.build_sweep(device, l2, only=only, rep_factor=0.0)
     first = next(iter(cases.values()))[0]
@@ -31,7 +37,7 @@ def test_bench_step_graph_replays_match_the_oracle():
     keys = sorted(cases)
 
     def call(k, r):
-        pd.decode_case(cases[k][r], out=outs[k][r], scratch=scratch, stream=stream)
+        pd.decode_case(cases[k][r], out=outs[k][r], scratch=scratch, stream=stream, opts=opts)
 
     with torch.cuda.stream(stream):
         for k in keys:

@@ -152,13 +152,17 @@ def test_rope_out_of_range_position_and_slot_reported():
                        k0.permute(0, 2, 1, 3)[mask.cuda()])
 
 
-def test_rope_then_decode_sees_the_new_tokens():
+@pytest.mark.parametrize("early", [0, 1])
+def test_rope_then_decode_sees_the_new_tokens(early):
     """The M new tokens of every sequence of a decode batch: rotate q and k,
-    write k and v into their cache slots, then decode over that cache."""
+    write k and v into their cache slots, then decode over that cache.  With
+    early reads the decode streams the older pages while the rotary kernel
+    still runs, and must wait for it before the newest keys and q."""
     M = 4
-    case = W.make_case("rope_then_decode", seed=21, dtype=torch.bfloat16, head_size=128,
+    lens = [1500, 37, 900] if not early else [6000, 37, 900, 2051]
+    case = W.make_case("rope_then_decode", seed=21 + early, dtype=torch.bfloat16, head_size=128,
                        num_q_heads=32, num_kv_heads=8, page_size=16, max_query_len=M,
-                       seq_lens=[1500, 37, 900], layout=W.HND)
+                       seq_lens=lens, layout=W.HND)
     S, P, Hkv, D = case.num_seqs, case.page_size, case.num_kv_heads, case.head_size
     # slots and positions of the last M tokens of every sequence
     slots, positions = [], []
@@ -171,7 +175,7 @@ def test_rope_then_decode_sees_the_new_tokens():
     gen = torch.Generator().manual_seed(5)
     k_new = torch.randn(T, Hkv, D, generator=gen).to(case.dtype)
     v_new = torch.randn(T, Hkv, D, generator=gen).to(case.dtype)
-    table = W.rope_cos_sin_table(4096, D)
+    table = W.rope_cos_sin_table(8192, D)
     g = case.to("cuda")
     q_rot = torch.empty_like(g.q)
     pd.paged_rope_cache_write(g.q, k_new.cuda(), v_new.cuda(),
@@ -180,7 +184,8 @@ def test_rope_then_decode_sees_the_new_tokens():
                               table.cuda(), q_rot, g.k_cache, g.v_cache, 32, Hkv, D, D, P,
                               W.HND, True)
     sc = scratch_for(case)
-    out = pd.decode_case(dataclasses.replace(g, q=q_rot), scratch=sc)
+    out = pd.decode_case(dataclasses.replace(g, q=q_rot), scratch=sc,
+                         opts=pd.options(early_reads=1) if early else None)
     torch.cuda.synchronize()
     assert pd.paged_decode_device_status(reset=True) == 0
     # the rope step against its oracle ...
