@@ -201,6 +201,10 @@ typedef struct pd_options {
                         wait limit would turn into PD_DEV_WAIT_TIMEOUT.
                         0 = read nothing before the previous kernel has
                         completed.  Anything else: PD_EINVAL.                  */
+  int mergers;       /* at most this many mergers K of the cooperative merge
+                        (a power of two; 0 = auto: the largest power of two
+                        <= min(D / 8, 64, segments, max(4, rows per CTA x
+                        D / 256)))                                             */
 } pd_options;
 
 /* paged_decode_attn with explicit knobs (opts may be NULL). */

@@ -66,7 +66,7 @@ class PdScratch(ctypes.Structure):
 class PdOptions(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("segments", "row_groups", "key_groups", "stages", "cluster", "path",
-                 "max_ctas_hint", "merge", "wait_limit_us", "early_reads")]
+                 "max_ctas_hint", "merge", "wait_limit_us", "early_reads", "mergers")]
 
 
 class PdPlan(ctypes.Structure):

@@ -200,6 +200,7 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   if (o.path < 0 || o.path > 3) return PD_EINVAL;
   if (o.wait_limit_us < 0) return PD_EINVAL;
   if (o.early_reads != 0 && o.early_reads != 1) return PD_EINVAL;
+  if (o.mergers < 0 || (o.mergers & (o.mergers - 1)) != 0) return PD_EINVAL;
   const bool tc = o.path == 3, dot = o.path == 2;
   if ((tc || dot) && D > 256) return PD_EINVAL;
   if ((tc || dot) && o.cluster > 1) return PD_EINVAL;
@@ -386,8 +387,15 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
     merge = 2;
     // a power of two <= min(D / 8, 64, parts): each merger takes a slice of
     // D / mergers >= 8 columns, so many parts are merged by many CTAs
+    // and about 256 (row, column) elements of a CTA's rows per merger, at
+    // least 4 mergers: a merger's time is mostly round trips, not its share,
+    // while every extra merger holds an SM the next call could start on
+    // (measured at D = 128, 2k-32k keys: K = 4 at 4 rows, 8 at 16 rows, 2-4 %
+    // faster per call than K = 16)
+    const int64_t by_work = std::max<int64_t>(4, (int64_t)rows_cta * D / 256);
     mergers = 1;
-    while (2 * mergers <= std::min<int64_t>({(int64_t)D / 8, 64, max_parts})) mergers *= 2;
+    while (2 * mergers <= std::min<int64_t>({(int64_t)D / 8, 64, max_parts, by_work})) mergers *= 2;
+    if (o.mergers > 0) mergers = std::min(mergers, o.mergers);
   } else if (o.merge == 2 && max_parts > 1) {
     return PD_EINVAL;  // the grid does not fit at once, or a cluster was asked for
   }

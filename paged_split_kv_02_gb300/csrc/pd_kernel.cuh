@@ -298,6 +298,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     bt_row = p.block_table + (int64_t)s * p.bt_stride;
   }
 
+  // (the block-table entries of the segment's first blocks are loaded in
+  // the same round trip as seq_lens)
+  if (spec_on) {
+#pragma unroll
+    for (int k = 0; k < kSpec / 32; ++k) spec[k] = spec[k] >= 0 ? ld_nc_now(bt_row + spec[k]) : 0;
+  }
   int L = __ldg(p.seq_lens + s);
   // q / out rows of the sequence: [s * M, s * M + M), or from query_start
   int qa, qb;
@@ -307,10 +313,6 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
   } else {
     qa = s * p.M;
     qb = qa + p.M;
-  }
-  if (spec_on) {
-#pragma unroll
-    for (int k = 0; k < kSpec / 32; ++k) spec[k] = spec[k] >= 0 ? __ldg(bt_row + spec[k]) : 0;
   }
 
   // ---- key ranges --------------------------------------------------------

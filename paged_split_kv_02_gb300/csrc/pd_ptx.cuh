@@ -271,6 +271,15 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *addr) {
   return v;
 }
 
+// A read-only 32-bit global load issued where it stands: the compiler does
+// not sink it into the branch that uses it, so its latency overlaps the
+// loads and arithmetic that follow.
+__device__ __forceinline__ int ld_nc_now(const int *addr) {
+  int v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
 // Programmatic dependent launch: wait for the prerequisite grid to complete
 // (and its writes to be visible); allow the dependent grid to launch.
 __device__ __forceinline__ void grid_dependency_wait() {

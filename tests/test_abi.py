@@ -176,6 +176,30 @@ def test_early_reads_option_checked():
     assert a == b
 
 
+def test_merger_count_rule():
+    """K of the cooperative merge: the largest power of two <= min(D / 8, 64,
+    segments, max(4, rows per CTA x D / 256)), capped by pd_options.mergers."""
+    sc = _fake_scratch(1, 32, 8, 128, 4, 64)
+
+    def plan(M, **kw):
+        return pd.paged_decode_plan(1, 32, 8, 128, 16, M, 0, 1024, 152, scratch_desc=sc,
+                                    opts=pd.options(**kw) if kw else None)
+    # 16k keys, 19 segments: 4 rows -> 4 mergers, 8 and 12 rows -> 4, 16 -> 8
+    assert [plan(M)["mergers"] for M in (1, 2, 3, 4)] == [4, 4, 4, 8]
+    assert all(plan(M)["merge"] == 2 for M in (1, 2, 3, 4))
+    assert plan(4, mergers=2)["mergers"] == 2
+    assert plan(4, mergers=1)["mergers"] == 1
+    assert plan(1, mergers=16)["mergers"] == 4       # a cap, not a request
+    for bad in (-1, 3, 6):
+        with pytest.raises(pd.PagedDecodeError):
+            plan(1, mergers=bad)
+    # the wide head (D = 512, M = 8: 64 rows, 16 per CTA in 4 row groups) and
+    # few segments: the segments bound K
+    p = pd.paged_decode_plan(1, 8, 1, 512, 16, 8, 0, 2048, 152,
+                             scratch_desc=_fake_scratch(1, 8, 1, 512, 8, 64))
+    assert p["merge"] == 2 and p["mergers"] == min(32, 1 << (p["max_segments"].bit_length() - 1))
+
+
 def test_plan_without_scratch_does_not_split():
     p = pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 2048, 152)
     assert p["max_parts"] == 0 and p["scratch_needed"] == 0

@@ -74,6 +74,15 @@ def test_merge_modes(merge, M, L, seg):
     _parity(W.spec_decode_hnd(M, L, seed=14), opts=pd.options(segments=seg, merge=merge))
 
 
+@pytest.mark.parametrize("k", [1, 2, 4, 16])
+@pytest.mark.parametrize("early", [0, 1])
+def test_merger_counts(k, early):
+    """The cooperative merge with 1..16 mergers (each a D/K slice of every
+    part), launched cooperatively and, with early reads, plainly."""
+    _parity(W.spec_decode_hnd(4, 4096, seed=17),
+            opts=pd.options(segments=19, merge=2, mergers=k, early_reads=early))
+
+
 def test_cooperative_merge_refused_when_grid_does_not_fit():
     case = W.spec_decode_hnd(2, 1024, seed=15)
     g = case.to("cuda")
