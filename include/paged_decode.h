@@ -203,8 +203,9 @@ typedef struct pd_options {
                         completed.  Anything else: PD_EINVAL.                  */
   int mergers;       /* at most this many mergers K of the cooperative merge
                         (a power of two; 0 = auto: the largest power of two
-                        <= min(D / 8, 64, segments, max(4, rows per CTA x
-                        D / 256)))                                             */
+                        <= min(D / 8, 64, segments, W), W the smallest power
+                        of two >= 4 with W x 8192 >= segments x rows per CTA
+                        x D, i.e. about 8192 partial elements per merger)     */
 } pd_options;
 
 /* paged_decode_attn with explicit knobs (opts may be NULL). */

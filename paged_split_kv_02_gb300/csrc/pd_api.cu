@@ -387,12 +387,15 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
     merge = 2;
     // a power of two <= min(D / 8, 64, parts): each merger takes a slice of
     // D / mergers >= 8 columns, so many parts are merged by many CTAs
-    // and about 256 (row, column) elements of a CTA's rows per merger, at
-    // least 4 mergers: a merger's time is mostly round trips, not its share,
-    // while every extra merger holds an SM the next call could start on
-    // (measured at D = 128, 2k-32k keys: K = 4 at 4 rows, 8 at 16 rows, 2-4 %
-    // faster per call than K = 16)
-    const int64_t by_work = std::max<int64_t>(4, (int64_t)rows_cta * D / 256);
+    // and no more than it takes to keep a merger's share of the parts near
+    // 8192 fp32 elements, at least 4: a merger's time is mostly round trips
+    // until its share grows past that, while every extra merger holds an SM
+    // the next call could start on (measured at D = 128, 4k-32k keys: 4
+    // mergers for 4-12 rows, 8 for 16 rows at 16k, 2-5 % faster per call than
+    // 16; at D = 512 and 152 parts the bound stays at 64)
+    const int64_t share = max_parts * rows_cta * (int64_t)D;
+    int64_t by_work = 4;
+    while (by_work * 8192 < share) by_work *= 2;
     mergers = 1;
     while (2 * mergers <= std::min<int64_t>({(int64_t)D / 8, 64, max_parts, by_work})) mergers *= 2;
     if (o.mergers > 0) mergers = std::min(mergers, o.mergers);

@@ -178,13 +178,15 @@ def test_early_reads_option_checked():
 
 def test_merger_count_rule():
     """K of the cooperative merge: the largest power of two <= min(D / 8, 64,
-    segments, max(4, rows per CTA x D / 256)), capped by pd_options.mergers."""
+    segments, W), W the smallest power of two >= 4 with W x 8192 >= segments x
+    rows per CTA x D; capped by pd_options.mergers."""
     sc = _fake_scratch(1, 32, 8, 128, 4, 64)
 
     def plan(M, **kw):
         return pd.paged_decode_plan(1, 32, 8, 128, 16, M, 0, 1024, 152, scratch_desc=sc,
                                     opts=pd.options(**kw) if kw else None)
-    # 16k keys, 19 segments: 4 rows -> 4 mergers, 8 and 12 rows -> 4, 16 -> 8
+    # 16k keys, 19 segments: 4, 8 and 12 rows -> 4 mergers, 16 -> 8 (19 x 16
+    # x 128 = 38912 > 4 x 8192)
     assert [plan(M)["mergers"] for M in (1, 2, 3, 4)] == [4, 4, 4, 8]
     assert all(plan(M)["merge"] == 2 for M in (1, 2, 3, 4))
     assert plan(4, mergers=2)["mergers"] == 2
@@ -198,6 +200,13 @@ def test_merger_count_rule():
     p = pd.paged_decode_plan(1, 8, 1, 512, 16, 8, 0, 2048, 152,
                              scratch_desc=_fake_scratch(1, 8, 1, 512, 8, 64))
     assert p["merge"] == 2 and p["mergers"] == min(32, 1 << (p["max_segments"].bit_length() - 1))
+    # 4k keys, 14 segments: 14 x 16 x 128 = 28672 <= 4 x 8192 -> 4 mergers
+    p = pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, 256, 152, scratch_desc=sc)
+    assert p["max_segments"] == 14 and p["mergers"] == 4
+    # D = 512, M = 1: 152 segments of 8 rows -> the D / 8 = 64 bound
+    p = pd.paged_decode_plan(1, 8, 1, 512, 16, 1, 0, 2048, 152,
+                             scratch_desc=_fake_scratch(1, 8, 1, 512, 8, 256))
+    assert p["max_segments"] == 152 and p["mergers"] == 64
 
 
 def test_plan_without_scratch_does_not_split():
