@@ -63,7 +63,7 @@ __device__ __forceinline__ uint4 pack8(const float (&y)[8]) {
   return w;
 }
 
-template <bool BF16, bool NEOX>
+template <bool BF16, bool NEOX, int kU>
 __global__ void __launch_bounds__(128) pd_rope_cache(const __grid_constant__ RopeParams p) {
   const int t = blockIdx.x;
   // the inputs may be the previous kernel's outputs
@@ -107,58 +107,92 @@ __global__ void __launch_bounds__(128) pd_rope_cache(const __grid_constant__ Rop
     return reinterpret_cast<uint4 *>(b + d);
   };
 
+  auto v_src = [&](int h, int c) -> const uint4 * {
+    return reinterpret_cast<const uint4 *>(static_cast<const unsigned short *>(p.v) +
+                                           (int64_t)t * p.v_s0 + (int64_t)h * p.v_s1 + 8 * c);
+  };
+  auto v_dst = [&](int h, int c) -> uint4 * {
+    return reinterpret_cast<uint4 *>(static_cast<unsigned short *>(p.v_cache) +
+                                     (int64_t)page * p.vc_page + (int64_t)off * p.vc_tok +
+                                     (int64_t)h * p.vc_head + 8 * c);
+  };
+  // Up to kU items per thread per pass: every item's loads are issued before
+  // any item is computed and stored, so a thread has several 16-byte loads
+  // in flight.  A few tokens (a decode batch) leave most warp slots empty and
+  // take kU = 4; many tokens fill the SMs with warps instead and take kU = 1
+  // (more registers per thread would cost resident CTAs).  Items touch
+  // disjoint chunks and each chunk is loaded and stored by the same thread,
+  // so the early loads are safe when q_out is q.
 #pragma unroll 1
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    if (i < n_rot) {
-      const int hh = i / rot_items, c = i - hh * rot_items;
-      const bool store = hh < p.Hq || write_kv;
-      if (NEOX) {
-        // dims [8c, 8c + 8) pair with [half + 8c, half + 8c + 8), angles 8c..
-        float x1[8], x2[8], co[8], si[8], y1[8], y2[8];
-        unpack8<BF16>(*src_ptr(hh, 8 * c), x1);
-        unpack8<BF16>(*src_ptr(hh, half + 8 * c), x2);
-        const float4 c0 = __ldg(reinterpret_cast<const float4 *>(cs + 8 * c));
-        const float4 c1 = __ldg(reinterpret_cast<const float4 *>(cs + 8 * c + 4));
-        const float4 s0 = __ldg(reinterpret_cast<const float4 *>(cs + half + 8 * c));
-        const float4 s1 = __ldg(reinterpret_cast<const float4 *>(cs + half + 8 * c + 4));
-        co[0] = c0.x; co[1] = c0.y; co[2] = c0.z; co[3] = c0.w;
-        co[4] = c1.x; co[5] = c1.y; co[6] = c1.z; co[7] = c1.w;
-        si[0] = s0.x; si[1] = s0.y; si[2] = s0.z; si[3] = s0.w;
-        si[4] = s1.x; si[5] = s1.y; si[6] = s1.z; si[7] = s1.w;
+  for (int i0 = threadIdx.x; i0 < n; i0 += kU * blockDim.x) {
+    uint4 w1[kU], w2[kU];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          y1[e] = x1[e] * co[e] - x2[e] * si[e];
-          y2[e] = x2[e] * co[e] + x1[e] * si[e];
-        }
-        if (store) {
-          *dst_ptr(hh, 8 * c) = pack8<BF16>(y1);
-          *dst_ptr(hh, half + 8 * c) = pack8<BF16>(y2);
-        }
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * blockDim.x;
+      w1[u] = w2[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (i >= n) continue;
+      if (i < n_rot) {
+        const int hh = i / rot_items, c = i - hh * rot_items;
+        w1[u] = *src_ptr(hh, 8 * c);
+        if (NEOX) w2[u] = *src_ptr(hh, half + 8 * c);
+      } else if (i < n_rot + n_pass) {
+        const int j = i - n_rot, hh = j / pass_items, c = j - hh * pass_items;
+        w1[u] = *src_ptr(hh, p.rot + 8 * c);
       } else {
-        // dims [8c, 8c + 8): pairs (2j, 2j + 1) of angles 4c .. 4c + 3
-        float x[8], y[8];
-        unpack8<BF16>(*src_ptr(hh, 8 * c), x);
-        const float4 cc = __ldg(reinterpret_cast<const float4 *>(cs + 4 * c));
-        const float4 ss = __ldg(reinterpret_cast<const float4 *>(cs + half + 4 * c));
-        const float co[4] = {cc.x, cc.y, cc.z, cc.w}, si[4] = {ss.x, ss.y, ss.z, ss.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          y[2 * j] = x[2 * j] * co[j] - x[2 * j + 1] * si[j];
-          y[2 * j + 1] = x[2 * j + 1] * co[j] + x[2 * j] * si[j];
-        }
-        if (store) *dst_ptr(hh, 8 * c) = pack8<BF16>(y);
+        const int j = i - n_rot - n_pass, h = j / (p.D / 8), c = j - h * (p.D / 8);
+        w1[u] = *v_src(h, c);
       }
-    } else if (i < n_rot + n_pass) {
-      const int j = i - n_rot, hh = j / pass_items, c = j - hh * pass_items;
-      if (hh < p.Hq || write_kv) *dst_ptr(hh, p.rot + 8 * c) = *src_ptr(hh, p.rot + 8 * c);
-    } else {
-      const int j = i - n_rot - n_pass, h = j / (p.D / 8), c = j - h * (p.D / 8);
-      const uint4 w = *reinterpret_cast<const uint4 *>(
-          static_cast<const unsigned short *>(p.v) + (int64_t)t * p.v_s0 + (int64_t)h * p.v_s1 +
-          8 * c);
-      *reinterpret_cast<uint4 *>(static_cast<unsigned short *>(p.v_cache) +
-                                 (int64_t)page * p.vc_page + (int64_t)off * p.vc_tok +
-                                 (int64_t)h * p.vc_head + 8 * c) = w;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i >= n) continue;
+      if (i < n_rot) {
+        const int hh = i / rot_items, c = i - hh * rot_items;
+        const bool store = hh < p.Hq || write_kv;
+        if (NEOX) {
+          // dims [8c, 8c + 8) pair with [half + 8c, half + 8c + 8), angles 8c..
+          float x1[8], x2[8], co[8], si[8], y1[8], y2[8];
+          unpack8<BF16>(w1[u], x1);
+          unpack8<BF16>(w2[u], x2);
+          const float4 c0 = __ldg(reinterpret_cast<const float4 *>(cs + 8 * c));
+          const float4 c1 = __ldg(reinterpret_cast<const float4 *>(cs + 8 * c + 4));
+          const float4 s0 = __ldg(reinterpret_cast<const float4 *>(cs + half + 8 * c));
+          const float4 s1 = __ldg(reinterpret_cast<const float4 *>(cs + half + 8 * c + 4));
+          co[0] = c0.x; co[1] = c0.y; co[2] = c0.z; co[3] = c0.w;
+          co[4] = c1.x; co[5] = c1.y; co[6] = c1.z; co[7] = c1.w;
+          si[0] = s0.x; si[1] = s0.y; si[2] = s0.z; si[3] = s0.w;
+          si[4] = s1.x; si[5] = s1.y; si[6] = s1.z; si[7] = s1.w;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            y1[e] = x1[e] * co[e] - x2[e] * si[e];
+            y2[e] = x2[e] * co[e] + x1[e] * si[e];
+          }
+          if (store) {
+            *dst_ptr(hh, 8 * c) = pack8<BF16>(y1);
+            *dst_ptr(hh, half + 8 * c) = pack8<BF16>(y2);
+          }
+        } else {
+          // dims [8c, 8c + 8): pairs (2j, 2j + 1) of angles 4c .. 4c + 3
+          float x[8], y[8];
+          unpack8<BF16>(w1[u], x);
+          const float4 cc = __ldg(reinterpret_cast<const float4 *>(cs + 4 * c));
+          const float4 ss = __ldg(reinterpret_cast<const float4 *>(cs + half + 4 * c));
+          const float co[4] = {cc.x, cc.y, cc.z, cc.w}, si[4] = {ss.x, ss.y, ss.z, ss.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            y[2 * j] = x[2 * j] * co[j] - x[2 * j + 1] * si[j];
+            y[2 * j + 1] = x[2 * j + 1] * co[j] + x[2 * j] * si[j];
+          }
+          if (store) *dst_ptr(hh, 8 * c) = pack8<BF16>(y);
+        }
+      } else if (i < n_rot + n_pass) {
+        const int j = i - n_rot, hh = j / pass_items, c = j - hh * pass_items;
+        if (hh < p.Hq || write_kv) *dst_ptr(hh, p.rot + 8 * c) = w1[u];
+      } else {
+        const int j = i - n_rot - n_pass, h = j / (p.D / 8), c = j - h * (p.D / 8);
+        *v_dst(h, c) = w1[u];
+      }
     }
   }
 }
@@ -278,13 +312,26 @@ extern "C" PD_API int paged_rope_cache_write(
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool bf16 = dt == PD_BF16;
+  int num_sms = 0;
+  if ((rc = device_check(&num_sms, nullptr)) != PD_OK) return rc;
+  // (4 warps per token; a GB300 SM holds 64)
+  const bool few = T * 4 < (int64_t)num_sms * 32;
   cudaError_t e;
-  if (bf16)
-    e = is_neox ? cudaLaunchKernelEx(&cfg, pd_rope_cache<true, true>, p)
-                : cudaLaunchKernelEx(&cfg, pd_rope_cache<true, false>, p);
-  else
-    e = is_neox ? cudaLaunchKernelEx(&cfg, pd_rope_cache<false, true>, p)
-                : cudaLaunchKernelEx(&cfg, pd_rope_cache<false, false>, p);
+  if (few) {
+    if (bf16)
+      e = is_neox ? cudaLaunchKernelEx(&cfg, pd_rope_cache<true, true, 4>, p)
+                  : cudaLaunchKernelEx(&cfg, pd_rope_cache<true, false, 4>, p);
+    else
+      e = is_neox ? cudaLaunchKernelEx(&cfg, pd_rope_cache<false, true, 4>, p)
+                  : cudaLaunchKernelEx(&cfg, pd_rope_cache<false, false, 4>, p);
+  } else {
+    if (bf16)
+      e = is_neox ? cudaLaunchKernelEx(&cfg, pd_rope_cache<true, true, 1>, p)
+                  : cudaLaunchKernelEx(&cfg, pd_rope_cache<true, false, 1>, p);
+    else
+      e = is_neox ? cudaLaunchKernelEx(&cfg, pd_rope_cache<false, true, 1>, p)
+                  : cudaLaunchKernelEx(&cfg, pd_rope_cache<false, false, 1>, p);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return PD_ECUDA;

@@ -109,6 +109,18 @@ def test_rope_cache_layouts_and_packed_pool(layout, packed):
     _run_and_check(c)
 
 
+@pytest.mark.parametrize("neox", [True, False])
+@pytest.mark.parametrize("inplace", [False, True])
+def test_rope_many_tokens(neox, inplace):
+    """Enough tokens to fill the SMs with warps (the kernel then takes one
+    item per thread per pass instead of four): 1400 tokens, partial rotary."""
+    c = W.make_rope_case("rope_many", seed=13, dtype=torch.bfloat16, num_tokens=1400,
+                         num_q_heads=32, num_kv_heads=8, head_size=128, rot_dim=96 if neox else 64,
+                         page_size=16, num_pages=100, layout=W.HND, is_neox=neox, max_pos=4096,
+                         pad_tokens=7)
+    _run_and_check(c, inplace=inplace)
+
+
 def test_rope_in_place_and_hybrid_page():
     # q_out = q, a 784-token page, 16 q / 2 kv heads at D = 256, 64 rotary dims
     c = W.make_rope_case("rope_inplace", seed=9, dtype=torch.bfloat16, num_tokens=64,
