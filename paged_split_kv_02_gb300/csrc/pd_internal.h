@@ -138,12 +138,13 @@ constexpr int kTpSoftmaxWarps = 8;
 constexpr int kTpConsumerWarps = kTpSoftmaxWarps + 1;  // + the warp that issues S
 // warps: softmax 0..7, S issue 8, producer 9, PV issue 10 (tile 0) and 11
 constexpr int kTpThreads = 32 * (kTpConsumerWarps + 3);
-// barriers: [0,1] S full, [2,3] S read (per tile), [4..7] P written, [8..11]
-// PV done (per tile and P buffer, 4 + 2 x + b), [12] every MMA done
+// barriers (per tile x and S / P buffer b): [0..3] S full (2 x + b), [4..7]
+// P written (4 + 2 x + b), [8..11] PV done (8 + 2 x + b), [12] every MMA done
 constexpr int kTpBarriers = 13;
 constexpr int kTpBlockIds = 256;  // page ids staged at a time (room for a fifth stage)
+// tensor-memory columns of a prefill CTA: two S buffers per tile (P of a
+// stage overwrites its S), then O of both tiles
 constexpr int tp_s_col(int D) { return 0 * D; }
-constexpr int tp_p_col(int D) { return 2 * tc_stage_keys(D); }
 constexpr int tp_o_col(int D) { return 4 * tc_stage_keys(D); }
 constexpr int tp_tmem_cols(int D) {
   return tp_o_col(D) + 2 * D <= 128 ? 128 : tp_o_col(D) + 2 * D <= 256 ? 256 : 512;

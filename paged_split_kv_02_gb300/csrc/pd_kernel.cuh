@@ -78,13 +78,21 @@ __device__ __forceinline__ float max2_of(const uint32_t (&w)[N], std::false_type
   return fmaxf(__low2float(m), __high2float(m));
 }
 
-// lo + hi of a packed pair, widened back to fp32
-__device__ __forceinline__ float sum2(uint32_t w, std::true_type /*bf16*/) {
-  return __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+// acc + lo + hi of a packed pair, each half widened exactly to fp32 inside a
+// mixed-precision add (one instruction per element)
+__device__ __forceinline__ float add2_f32(float acc, uint32_t w, std::true_type /*bf16*/) {
+  asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\nadd.rn.f32.bf16 %0, lo, %0;\n"
+      "add.rn.f32.bf16 %0, hi, %0;\n}\n"
+      : "+f"(acc)
+      : "r"(w));
+  return acc;
 }
-__device__ __forceinline__ float sum2(uint32_t w, std::false_type /*fp16*/) {
-  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
-  return f.x + f.y;
+__device__ __forceinline__ float add2_f32(float acc, uint32_t w, std::false_type /*fp16*/) {
+  asm("{\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\nadd.rn.f32.f16 %0, lo, %0;\n"
+      "add.rn.f32.f16 %0, hi, %0;\n}\n"
+      : "+f"(acc)
+      : "r"(w));
+  return acc;
 }
 
 // Column swizzle of the fp32 partial tiles in shared memory: rows 2x and 2x+1
@@ -208,10 +216,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
       if (lane < kTcBarriers) mbar_init(smem_u32(tcb + lane), (lane >= 2 && lane <= 5) ? 4 : 1);
     }
     if constexpr (TP) {
-      // S read and P written: a tile's four softmax warps; every MMA done:
-      // the S warp's and both PV warps' last commits
+      // P written: a tile's four softmax warps; every MMA done: the S warp's
+      // and both PV warps' last commits
       if (lane < kTpBarriers)
-        mbar_init(smem_u32(tcb + lane), (lane >= 2 && lane <= 7) ? 4 : lane == 12 ? 3 : 1);
+        mbar_init(smem_u32(tcb + lane), (lane >= 4 && lane <= 7) ? 4 : lane == 12 ? 3 : 1);
     }
     if (lane == 31) {
       mbar_init(smem_u32(mbar_merge), 1);
@@ -520,8 +528,11 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     const int rr_tp = rr0 + kTpRows * X + r_tp;
     const bool live = warp < kTpSoftmaxWarps && rr_tp < rr1v;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t tS = tmem_base + tp_s_col(D), tPb = tmem_base + tp_p_col(D),
-                   tO = tmem_base + tp_o_col(D);
+    // S of tile x, stage j in buffer tS + (2 x + (j & 1)) * SC; P of that
+    // stage overwrites the buffer's first SC / 2 columns once the softmax has
+    // read S (so S of stage j + 1 is computed while the softmax of stage j
+    // runs, and S of stage j + 2 once the PV MMAs of stage j have read P)
+    const uint32_t tS = tmem_base + tp_s_col(D), tO = tmem_base + tp_o_col(D);
     if (warp < kTpSoftmaxWarps) {
       // Q rows of tile X into its 128-byte-swizzled K-major tile in shared
       // memory ([tile][64-dim box][128 rows][128 B]); zeros for rows past
@@ -550,17 +561,17 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
       tc_fence_after();
       const uint32_t idS = umma_idesc_f16(kTpRows, SC, BF16, 0, 0);
       const uint32_t ring_u = smem_u32(ring), qb_u = smem_u32(qs);
-      // S of both tiles for stage j, once its stage has landed and (j >= 1)
-      // each tile's softmax has read its S buffer
+      // S of both tiles for stage j, once its stage has landed and (j >= 2)
+      // the PV MMAs of stage j - 2 have read the P in its buffer
       auto issue_s = [&](int j) -> bool {
-        const int slot = j % NS;
+        const int slot = j % NS, sb = j & 1;
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(full + slot), (j / NS) & 1)))
           return false;
         const uint32_t kst = ring_u + slot * STAGE;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          if (j >= 1 &&
-              !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 2 + x), (j - 1) & 1)))
+          if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8 + 2 * x + sb),
+                                                                  ((j - 2) >> 1) & 1)))
             return false;
           tc_fence_after();
           // all SC keys of the stage at once (keys of blocks a short stage
@@ -569,18 +580,18 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           for (int ks = 0; ks < KS; ++ks) {
             const uint64_t bk =
                 umma_desc_sw128(kst + (ks >> 2) * (TB * BLOCK_BYTES / NBOX) + (ks & 3) * 32, 16, 1024);
-            umma_f16_warp(tS + x * SC,
+            umma_f16_warp(tS + (2 * x + sb) * SC,
                           umma_desc_sw128(qb_u + x * (kTpRows * D * 2) + (ks >> 2) * (kTpRows * 128) +
                                               (ks & 3) * 32,
                                           16, 1024),
                           bk, idS, ks > 0 ? 1u : 0u);
           }
-          umma_commit_warp(smem_u32(tcb + x));  // S_x of stage j is ready
+          umma_commit_warp(smem_u32(tcb + 2 * x + sb));  // S_x of stage j is ready
         }
         return true;
       };
-      // S of stage 0, then of each next stage as soon as both softmaxes have
-      // read the S of the stage before (the PV MMAs are the PV warps')
+      // S of stage 0, then of each next stage as soon as its buffer is free
+      // (the PV MMAs are the PV warps')
       bool ok = ntile == 0 || issue_s(0);
       for (int k = 1; k < ntile && ok; ++k) ok = issue_s(k);
       if (!ok && lane == 0) {
@@ -609,7 +620,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
 #pragma unroll
         for (int b = 0; b < TB; ++b)
           if (b < nbt)
-            umma_f16_ts_warp(tO + x * D, tPb + x * SC + pb * (SC / 2) + 8 * b,
+            umma_f16_ts_warp(tO + x * D, tS + (2 * x + pb) * SC + 8 * b,
                              dv + (uint64_t)(b * BLOCK_BYTES / 16), idO, (k > 0 || b > 0) ? 1u : 0u);
         umma_commit_warp(smem_u32(tcb + 8 + 2 * x + pb));  // P buffer pb free, O_x current
         umma_commit_warp(smem_u32(empty + slot));  // (with the other tile's) the stage is free
@@ -626,10 +637,12 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         hi = max(L - ml + token_of(rr_tp) + 1, 0);
         lo = p.window ? max(0, hi - p.window) : 0;
       }
-      const uint32_t tSx = tS + X * SC, tPx = tPb + X * SC, tOx = tO + X * D;
+      const uint32_t tOx = tO + X * D;
       float m_used = -INFINITY, lsum = 0.f;
       for (int j = 0; j < ntile; ++j) {
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + X), j & 1))) {
+        const uint32_t tSx = tS + (2 * X + (j & 1)) * SC;  // S, then P, of stage j
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_bounded(smem_u32(tcb + 2 * X + (j & 1)), (j >> 1) & 1))) {
           if (lane == 0) {
             flags[0] = 1;
             atomicOr(p.status, 0x1u);
@@ -649,9 +662,6 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
             sr[32 + i] = x1[i];
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(tcb + 2 + X));  // S buffer read
         const int nbt = min(TB, my_nb - j * TB);
         const int key_t0 = (my_b0 + j * TB) * kBlockKeys;
         const int slot = j % NS;
@@ -745,11 +755,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           }
           if (m_used == -INFINITY) m_used = m_new;
         }
-        // P buffer j & 1 is free once the PV MMAs of stage j - 2 have completed
-        if (ok && j >= 2)
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(tcb + 8 + 2 * X + (j & 1)),
-                                                         ((j - 2) >> 1) & 1));
-        tc_fence_after();
+        // (P goes over S in the buffer this warp has just read: its other
+        // readers, the PV MMAs of stage j - 2, completed before S of stage j
+        // was written there)
         if (!ok) {
           if (lane == 0) {
             flags[0] = 1;
@@ -800,9 +808,9 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
           }
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c = 0; c < SC / 2; ++c) ls[c & 3] += sum2(w[c], tag{});
+          for (int c = 0; c < SC / 2; ++c) ls[c & 3] = add2_f32(ls[c & 3], w[c], tag{});
           lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-          tmem_st32(tPx + (j & 1) * (SC / 2) + lane_base, w);
+          tmem_st32(tSx + lane_base, w);
         }
         // zero V of keys no row sees (outside the union, stale or NaN slots);
         // each tile does it before its own PV MMAs (the other tile's writes
