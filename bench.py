@@ -482,8 +482,13 @@ def measure_e2e(pd, cases, outs, scratch, stream, keys, args):
     """The same sweep through the C ABI with pinned host buffers, driven the
     way a serving loop would: each step copies every case's q, block table
     and seq_lens host->device in one transfer (one pinned staging buffer),
-    makes the C calls with descriptors built once, and copies every output
-    back in one transfer before the step's single synchronisation."""
+    makes the C calls with descriptors built once, copies every output back
+    in one transfer, and the host reads the step's outputs once that copy has
+    landed.  Two sets of buffers alternate, so a step's host->device copy
+    (its own stream) and the device->host copy of the step before (a third
+    stream) overlap the calls, as a serving loop overlaps its next batch's
+    transfers with the current one's compute; the host waits for a step's
+    outputs two steps later, before it reuses that step's buffers."""
     import ctypes
 
     def layout_of(tensors):
@@ -498,59 +503,88 @@ def measure_e2e(pd, cases, outs, scratch, stream, keys, args):
     out_shapes = [cases[k][0].q for k in keys]
     out_offs, out_bytes = layout_of(out_shapes)
     dev = ins[0].device
-    host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
-    dev_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-    host_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
-    dev_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+    nb = 2  # buffer sets in flight
+    host_in = [torch.empty(in_bytes, dtype=torch.uint8).pin_memory() for _ in range(nb)]
+    dev_in = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(nb)]
+    host_out = [torch.empty(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(nb)]
+    dev_out = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(nb)]
 
     def view(buf, off, like):
         n = like.numel() * like.element_size()
         return buf[off:off + n].view(like.dtype).view(like.shape)
 
-    for t, off in zip(ins, in_offs):
-        view(host_in, off, t).copy_(t.cpu())
+    for b in range(nb):
+        for t, off in zip(ins, in_offs):
+            view(host_in[b], off, t).copy_(t.cpu())
     lib = pd.lib()
     early = pd.options(early_reads=1)
-    calls = []
-    for i, k in enumerate(keys):
-        c = cases[k][0]
-        q, bt, sl = (view(dev_in, in_offs[3 * i + j], t)
-                     for j, t in enumerate((c.q, c.block_table, c.seq_lens)))
-        o = view(dev_out, out_offs[i], c.q)
-        descs = [pd.tensor_desc(t) for t in (q, c.k_cache, c.v_cache, bt, sl, o)]
-        cargs = [ctypes.byref(d) for d in descs] + [
-            c.num_q_heads, c.num_kv_heads, c.head_size, c.page_size, c.max_query_len, c.window,
-            ctypes.c_float(c.scale), c.layout, ctypes.byref(scratch.desc),
-            ctypes.c_void_p(stream.cuda_stream)]
-        if args.early_reads:
-            # (q, block table and seq_lens come from the step's one host copy,
-            # made before the first call: every call may read early)
-            cargs = cargs + [ctypes.byref(early)]
-        calls.append((descs, cargs))
+    calls = [[] for _ in range(nb)]
+    for b in range(nb):
+        for i, k in enumerate(keys):
+            c = cases[k][0]
+            q, bt, sl = (view(dev_in[b], in_offs[3 * i + j], t)
+                         for j, t in enumerate((c.q, c.block_table, c.seq_lens)))
+            o = view(dev_out[b], out_offs[i], c.q)
+            descs = [pd.tensor_desc(t) for t in (q, c.k_cache, c.v_cache, bt, sl, o)]
+            cargs = [ctypes.byref(d) for d in descs] + [
+                c.num_q_heads, c.num_kv_heads, c.head_size, c.page_size, c.max_query_len,
+                c.window, ctypes.c_float(c.scale), c.layout, ctypes.byref(scratch.desc),
+                ctypes.c_void_p(stream.cuda_stream)]
+            if args.early_reads:
+                # (q, block table and seq_lens come from the step's one host
+                # copy, complete before the step's first call: every call may
+                # read early)
+                cargs = cargs + [ctypes.byref(early)]
+            calls[b].append((descs, cargs))
     h2d, d2h = in_bytes, out_bytes
     entry = lib.paged_decode_attn_opts if args.early_reads else lib.paged_decode_attn
     kv_step = sum(cases[k][0].kv_bytes_touched() for k in keys)
+    h2d_stream = torch.cuda.Stream(device=dev)
+    d2h_stream = torch.cuda.Stream(device=dev)
+    in_ready = [torch.cuda.Event() for _ in range(nb)]
+    out_ready = [torch.cuda.Event() for _ in range(nb)]
+    out_landed = [torch.cuda.Event() for _ in range(nb)]
+    checksum = [0.0]
 
-    def step():
-        with torch.cuda.stream(stream):
-            dev_in.copy_(host_in, non_blocking=True)
-            for _, a in calls:
-                rc = entry(*a)
-                if rc != 0:
-                    raise RuntimeError(f"paged_decode_attn: {rc}")
-            host_out.copy_(dev_out, non_blocking=True)
-        stream.synchronize()
+    def consume(b):
+        out_landed[b].synchronize()
+        checksum[0] += float(host_out[b][:2].view(torch.bfloat16)[0])  # the host reads it
 
-    for _ in range(args.warmup):
-        step()
+    def issue(i):
+        b = i % nb
+        if i >= nb:
+            consume(b)  # step i - nb's outputs; its buffers are free again
+        with torch.cuda.stream(h2d_stream):
+            dev_in[b].copy_(host_in[b], non_blocking=True)
+            in_ready[b].record(h2d_stream)
+        stream.wait_event(in_ready[b])
+        for _, a in calls[b]:
+            rc = entry(*a)
+            if rc != 0:
+                raise RuntimeError(f"paged_decode_attn: {rc}")
+        out_ready[b].record(stream)
+        d2h_stream.wait_event(out_ready[b])
+        with torch.cuda.stream(d2h_stream):
+            host_out[b].copy_(dev_out[b], non_blocking=True)
+            out_landed[b].record(d2h_stream)
+
+    def run(n):
+        for i in range(n):
+            issue(i)
+        for i in range(max(0, n - nb), n):
+            consume(i % nb)
+
+    run(args.warmup)
+    torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
+    run(args.steps)
     dt = (time.perf_counter() - t0) / args.steps
     return {"value": round(kv_step / dt / 1e9, 1), "unit": UNIT, "ms_per_step": round(dt * 1e3, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "transfers": "one pinned host->device copy of every call's inputs and one "
-                         "device->host copy of every output per step",
+                         "device->host copy of every output per step, read by the host; two "
+                         "buffer sets alternate, so the copies of neighbouring steps overlap "
+                         "the calls",
             "call": "paged_decode_attn_opts (early reads)" if args.early_reads
                     else "paged_decode_attn"}
 

@@ -183,10 +183,13 @@ typedef struct pd_options {
                         that path                                              */
   int early_reads;   /* 1 = the caller vouches that block_table, seq_lens,
                         query_start and every cached key and value older than
-                        each sequence's newest max_query_len tokens were
-                        written before the previous kernel on the stream
-                        started.  The call then reads them, and streams those
-                        pages into shared memory, while that kernel finishes
+                        each sequence's newest max_query_len tokens are not
+                        written by the kernel that precedes this call on the
+                        stream (anything else that writes them completes
+                        before the call is launched: earlier kernels, copies
+                        the stream waits for).  The call then reads them,
+                        and streams those pages into shared memory, while
+                        that kernel finishes
                         (programmatic dependent launch); q, the newest keys
                         and values, and every write still wait for it to
                         complete.  This is the case of a decode step whose
