@@ -89,7 +89,7 @@ def test_plan_segments_grow_with_the_context():
     # head the CTAs are capped at (12 + 7/3 log2(MiB)) / 19 of the SMs
     # (fewer, longer segments: fewer parts to merge), below and above that
     # the SM count and the segment floor decide
-    want = {1024: 10, 2048: 12, 4096: 14, 8192: 16, 16384: 19, 32768: 19}
+    want = {1024: 6, 2048: 12, 4096: 14, 8192: 16, 16384: 19, 32768: 19}
     for L, nseg in want.items():
         sd = _fake_scratch(1, 32, 8, 128, 4, 256)
         p = pd.paged_decode_plan(1, 32, 8, 128, 16, 4, 0, L // 16, 152, scratch_desc=sd)
