@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     // S of stage j goes to buffer j & 1 of its tile and P of stage j over it,
     // so S of stage j + 1 is computed while the softmax of stage j runs, and
     // buffer j & 1 takes S of stage j + 2 once the PV MMAs of stage j have
-    // read its P; the softmax never waits for a PV MMA.  O_X is rescaled in
+    // read its P; only a rescale of O waits for a PV MMA.  O_X is rescaled in
     // tensor memory only when a row's max grows more than 8 past the
     // reference its P values use (so P <= 2^8), the online-softmax update in
     // exp2 form.  Two tiles per stage halve the K/V copies per row: the
