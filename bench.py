@@ -718,11 +718,8 @@ def run_varlen(args, world, rank, local):
     outs_v = [torch.empty_like(c.q) for c in var]
     outs_u = [torch.empty_like(c.q) for c in uni]
     stream = torch.cuda.Stream(device=device)
-    opts = pd.options(early_reads=1) if args.early_reads else None
-    calls_v = [(lambda c=c, o=o: pd.decode_case(c, out=o, scratch=scratch, opts=opts))
-               for c, o in zip(var, outs_v)]
-    calls_u = [(lambda c=c, o=o: pd.decode_case(c, out=o, scratch=scratch, opts=opts))
-               for c, o in zip(uni, outs_u)]
+    calls_v = [(lambda c=c, o=o: pd.decode_case(c, out=o, scratch=scratch)) for c, o in zip(var, outs_v)]
+    calls_u = [(lambda c=c, o=o: pd.decode_case(c, out=o, scratch=scratch)) for c, o in zip(uni, outs_u)]
     with torch.cuda.stream(stream):
         for c in calls_v + calls_u:
             c()
@@ -769,7 +766,6 @@ def run_varlen(args, world, rank, local):
         "config": {"workload": VARLEN_WORKLOAD.replace("32 requests", f"{nreq} requests"),
                    "l2": f"inputs larger than L2: {n_rep} rotating replicas",
                    "timing": "CUDA graph of the calls, CUDA events on the launching stream",
-                   "launch": "early reads" if opts is not None else "every call waits first",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": args.steps * n_rep,
         "us_per_call": round(us, 3),
