@@ -67,6 +67,31 @@ def test_wide_head_full(M, L):
     _full_size(W.wide_head(M, L, seed=300 + M, device="cuda", gen_device="cuda"), seed=M)
 
 
+@pytest.mark.parametrize("make", [
+    lambda: W.spec_decode_hnd(4, 32768, seed=150, device="cuda", gen_device="cuda"),
+    lambda: W.wide_head(8, 32768, seed=350, device="cuda", gen_device="cuda"),
+    lambda: W.hybrid_page(784, 4, 16384, seed=360, device="cuda", gen_device="cuda"),
+    lambda: W.batched_hybrid_pages(seed=450, device="cuda", gen_device="cuda"),
+], ids=["spec_decode_M4_32k", "wide_head_M8_32k", "hybrid_P784_16k", "batched_64"])
+def test_full_size_with_early_reads(make):
+    """The way the benchmark launches them: two calls of a case back to back
+    on one stream with early reads (the second reads its metadata and streams
+    pages while the first finishes; a full grid is launched without the
+    cooperative attribute), both checked on sampled rows."""
+    case = make()
+    sc = scratch_for(case)
+    o = pd.options(early_reads=1)
+    a = pd.decode_case(case, scratch=sc, opts=o)
+    b = pd.decode_case(case, scratch=sc, opts=o)
+    torch.cuda.synchronize()
+    assert int(sc.counters().abs().sum()) == 0, "counters not left at zero"
+    assert pd.paged_decode_device_status(reset=True) == 0
+    case_cpu = case.to("cpu")
+    rows = sample_rows(case_cpu, N_ROWS, seed=7)
+    check(case_cpu, a, rows=rows)
+    check(case_cpu, b, rows=rows)
+
+
 def test_batched_hybrid_pages_full():
     """bf16, D=256, 16/2 heads, P=1056, 64 sequences U[1, 16384] with an
     empty slot, M=4: every sequence's first and last rows are sampled."""
