@@ -487,7 +487,8 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   if (query_start && plan.path == 3) return PD_EINVAL;  // not built for variable lengths
 
   CUtensorMap tk, tv;
-  if ((rc = encode_cache_map(k_cache, layout, &tk)) != PD_OK) return rc;
+  // (the tensor-memory path lands K box-major: one box per 64 dims)
+  if ((rc = encode_cache_map(k_cache, layout, &tk, plan.path == 3)) != PD_OK) return rc;
   if ((rc = encode_cache_map(v_cache, layout, &tv)) != PD_OK) return rc;
 
   Params p{};

@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
       const int nbt = min(TB, my_nb - j * TB);
       if (lane == 0) mbar_arrive_expect_tx(smem_u32(full + slot), nbt * 2 * BLOCK_BYTES);
       __syncwarp();
-      if (TP && lane < nbt * NBOX) {
+      if ((TP || TC) && lane < nbt * NBOX) {
         // TP's K: one copy per (16-key block, 64-dim box), box-major in the
         // stage ([box][block][16 keys][128 B]) so that one box's keys are
         // consecutive 128-byte rows (one MMA descriptor spans the stage)
@@ -473,10 +473,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         const uint32_t dst = smem_u32(ring + slot * STAGE + x * (TB * BLOCK_BYTES / NBOX) +
                                       b * (BLOCK_BYTES / NBOX));
         tma_load_5d(dst, &tmK, smem_u32(full + slot), 0, key_in_page, x, h, phys, pol);
-      } else if (TP ? lane >= nbt * NBOX && lane < nbt * (NBOX + 1) : lane < 2 * nbt) {
+      } else if ((TP || TC) ? lane >= nbt * NBOX && lane < nbt * (NBOX + 1) : lane < 2 * nbt) {
         // one copy per 16-key block of K or V (all D/64 swizzle rows at once;
         // TP: V only)
-        const int kv = TP ? 1 : lane >= nbt, b = TP ? lane - nbt * NBOX : lane - kv * nbt;
+        const int kv = (TP || TC) ? 1 : lane >= nbt, b = (TP || TC) ? lane - nbt * NBOX : lane - kv * nbt;
         const int blk = my_b0 + j * TB + b;
         const int key_in_page = (lg_bpp >= 0 ? blk & (bpp - 1) : blk % bpp) * kBlockKeys;
         int phys = pids[j * TB + b - pid_base];
@@ -881,7 +881,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
     if (warp == kTcConsumerWarps - 1) {
       // ---- MMA issue: the whole warp runs the loop (every operand is
       // warp-uniform), one elected lane issues each MMA and commit ----
-      const uint32_t idS = umma_idesc_f16(kTcRows, kBlockKeys, BF16, 0, 0);
+      const uint32_t idS = umma_idesc_f16(kTcRows, SC, BF16, 0, 0);
       const uint32_t idO = umma_idesc_f16(kTcRows, D, BF16, 0, 1);
       const uint32_t q_u = smem_u32(qs), p_u = smem_u32(pts), ring_u = smem_u32(ring);
       const uint64_t dq = umma_desc_sw128(q_u, 16, NBOX * 1024);
@@ -895,22 +895,18 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
                             mbar_wait_bounded(smem_u32(tcb + 2 + (j & 1)), ((j - 2) >> 1) & 1));
           if (!ok) break;
           tc_fence_after();
-          const int nbt = min(TB, my_nb - j * TB);
-          // descriptors of the stage's first K block; the start-address
-          // field (bits 0-13, 16-byte units) advances with the operand
-          const uint64_t dk = umma_desc_sw128(ring_u + slot * STAGE, 16, 1024);
+          // K landed box-major ([64-dim box][block][16 keys][128 B]), so one
+          // 128-byte-swizzled K-major descriptor spans the stage's keys: one
+          // MMA per 16-dim step with N = every key of the stage (keys of
+          // blocks a short stage did not load give scores the softmax masks)
+          const uint32_t kst = ring_u + slot * STAGE;
 #pragma unroll
-          for (int b = 0; b < TB; ++b) {
-            if (b < nbt) {
-              const uint64_t dkb = dk + (uint64_t)(b * BLOCK_BYTES / 16);
-#pragma unroll
-              for (int ks = 0; ks < KS; ++ks)
-                umma_f16_warp(tS + (j & 1) * SC + kBlockKeys * b,
-                              dq + (uint64_t)(((ks >> 2) * 1024 + (ks & 3) * 32) / 16),
-                              dkb + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) / 16), idS,
-                              ks > 0 ? 1u : 0u);
-            }
-          }
+          for (int ks = 0; ks < KS; ++ks)
+            umma_f16_warp(tS + (j & 1) * SC,
+                          dq + (uint64_t)(((ks >> 2) * 1024 + (ks & 3) * 32) / 16),
+                          umma_desc_sw128(kst + (ks >> 2) * (TB * BLOCK_BYTES / NBOX) + (ks & 3) * 32,
+                                          16, 1024),
+                          idS, ks > 0 ? 1u : 0u);
           umma_commit_warp(smem_u32(tcb + (j & 1)));  // S of stage j is ready
         }
         if (j >= 1) {
