@@ -18,7 +18,7 @@ __device__ unsigned int g_status;  // PD_DEV_* bits; read by paged_decode_device
 
 namespace {
 
-constexpr int kVersion = 10300;  // 1.2.0
+constexpr int kVersion = 10300;  // 1.3.0
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block on sm_100-class parts
 constexpr int kMaxDevices = 64;
 
@@ -390,14 +390,14 @@ int make_plan(int S, int Hq, int Hkv, int D, int P, int M, int window, int bt_wi
   int merge = max_parts > 1 ? 1 : 0, mergers = 0;
   if (coop_ok && o.merge != 1) {
     merge = 2;
-    // a power of two <= min(D / 8, 64, parts): each merger takes a slice of
-    // D / mergers >= 8 columns, so many parts are merged by many CTAs
-    // and no more than it takes to keep a merger's share of the parts near
-    // 8192 fp32 elements, at least 4: a merger's time is mostly round trips
-    // until its share grows past that, while every extra merger holds an SM
-    // the next call could start on (measured at D = 128, 4k-32k keys: 4
-    // mergers for 4-12 rows, 8 for 16 rows at 16k, 2-5 % faster per call than
-    // 16; at D = 512 and 152 parts the bound stays at 64)
+    // K mergers, each taking a slice of D / K >= 8 columns of every part: K a
+    // power of two <= min(D / 8, 64, parts), and no larger than it takes to
+    // keep a merger's share of the parts near 8192 fp32 elements (at least
+    // 4).  A merger's time is mostly round trips until its share grows past
+    // that, while every extra merger holds an SM the next call could start
+    // on (measured at D = 128, 4k-32k keys: 4 mergers for 4-12 rows, 8 for
+    // 16 rows at 16k, 2-5 % faster per call than 16; at D = 512 with 152
+    // parts the bound stays at 64)
     const int64_t share = max_parts * rows_cta * (int64_t)D;
     int64_t by_work = 4;
     while (by_work * 8192 < share) by_work *= 2;
@@ -557,11 +557,12 @@ int attn_impl(const pd_tensor *q, const pd_tensor *k_cache, const pd_tensor *v_c
   // early reads a grid that fills more than ~58 % of the SMs is launched
   // plainly: its CTAs then start, and stream the older pages, on the SMs the
   // previous call frees while that call's mergers finish (measured at 32 / 8
-  // heads, D = 128, 2k-32k keys: 0.4-1.5 us less per call; at 1k keys, 80
-  // CTAs, the cooperative launch was 1.1 us faster).  Nothing a later grid
-  // runs waits for this one to make progress, so all of its CTAs still
-  // become resident; a kernel on another stream that held SMs for longer
-  // than the mergers' wait limit would end in PD_DEV_WAIT_TIMEOUT.
+  // heads, D = 128, 2k-32k keys: 0.4-1.5 us less per call; with 80 CTAs the
+  // cooperative launch was 1.1 us faster).  This grid never waits on a later
+  // one (the next call launches only once every CTA of this one has
+  // started), so all of its CTAs still become resident; a kernel on another
+  // stream that held SMs for longer than the mergers' wait limit would end
+  // in PD_DEV_WAIT_TIMEOUT.
   const int64_t ctas = (int64_t)plan.max_segments * num_kv_heads * plan.row_groups * plan.grid_y;
   l.cooperative = plan.merge == 2 && !(p.early && ctas * 100 > 58LL * dev.num_sms) ? 1 : 0;
   cudaError_t e = launch_mma(head_size, q->dtype == PD_BF16, plan.path, tk, tv, p, l,
