@@ -459,9 +459,10 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
       if (lane == 0) mbar_arrive_expect_tx(smem_u32(full + slot), nbt * 2 * BLOCK_BYTES);
       __syncwarp();
       if ((TP || TC) && lane < nbt * NBOX) {
-        // TP's K: one copy per (16-key block, 64-dim box), box-major in the
-        // stage ([box][block][16 keys][128 B]) so that one box's keys are
-        // consecutive 128-byte rows (one MMA descriptor spans the stage)
+        // K of the tensor-memory consumers: one copy per (16-key block,
+        // 64-dim box), box-major in the stage ([box][block][16 keys][128 B])
+        // so that one box's keys are consecutive 128-byte rows (one MMA
+        // descriptor spans the stage)
         const int b = lane / NBOX, x = lane - b * NBOX;
         const int blk = my_b0 + j * TB + b;
         const int key_in_page = (lg_bpp >= 0 ? blk & (bpp - 1) : blk % bpp) * kBlockKeys;
@@ -475,7 +476,7 @@ __global__ void __launch_bounds__(TC ? kTcThreads : TP ? kTpThreads : kMaxThread
         tma_load_5d(dst, &tmK, smem_u32(full + slot), 0, key_in_page, x, h, phys, pol);
       } else if ((TP || TC) ? lane >= nbt * NBOX && lane < nbt * (NBOX + 1) : lane < 2 * nbt) {
         // one copy per 16-key block of K or V (all D/64 swizzle rows at once;
-        // TP: V only)
+        // the tensor-memory consumers: V only)
         const int kv = (TP || TC) ? 1 : lane >= nbt, b = (TP || TC) ? lane - nbt * NBOX : lane - kv * nbt;
         const int blk = my_b0 + j * TB + b;
         const int key_in_page = (lg_bpp >= 0 ? blk & (bpp - 1) : blk % bpp) * kBlockKeys;
